@@ -7,8 +7,9 @@ shares no code with it.
 
 What it computes: Algorithm 2 ("Single-GPU MoE Forward (OlmoeExperts)") of
 the page "MoE 分布式推理基础（基于 vLLM）", §1.2 "MoE Forward", together with
-the router's optional renormalisation shown in the same section
-(OlmoeTopKRouter: `top_val /= top_val.sum(-1)` when norm_topk_prob).  All
+the router's optional renormalisation shown in the same section (when
+norm_topk_prob is set, the K selected probabilities are divided by their
+sum).  All
 arithmetic is float64 on exactly upcast inputs; nothing is rounded to the
 GPU's storage types.  Library primitives used as steps: numpy matmul (BLAS),
 exp, and a stable argsort.
@@ -22,8 +23,8 @@ reason in the design notes):
   * Dispatch layout: the (token, slot) pairs are flattened to f = t*K + k and
     stably sorted by expert, i.e. ascending f inside each expert -- the order
     that the `moe_align_block_size` worked example of §2.3 prints.
-  * SwiGLU: gate = first I columns of X_e·W13[e], up = last I columns
-    (`gate_up.chunk(2, -1)` in §1.2, "SwiGLU expert 的两段 GEMM").
+  * SwiGLU: gate = first I columns of X_e·W13[e], up = last I columns (the
+    2I outputs are split in two halves in §1.2, "SwiGLU expert 的两段 GEMM").
 """
 from __future__ import annotations
 
@@ -147,15 +148,25 @@ def permute(x, perm, K):
     return _f64(x)[np.asarray(perm) // K]
 
 
-def swiglu_expert(X_e, W13_e, W2_e):
-    """Steps 8-9: G_e = SiLU(X_e W13[:, :I]) * (X_e W13[:, I:]); Y_e = G_e W2.
-    SiLU(g) = g * sigmoid(g) = g / (1 + exp(-g)).  Returns (G_e, Y_e)."""
-    I = W2_e.shape[0]
+def expert_up(X_e, W13_e):
+    """Step 8: G_e = SiLU(X_e W13[:, :I]) * (X_e W13[:, I:]), with
+    SiLU(g) = g * sigmoid(g) = g / (1 + exp(-g))."""
+    I = W13_e.shape[1] // 2
     gate_up = X_e @ W13_e
     gate, up = gate_up[:, :I], gate_up[:, I:]
     with np.errstate(over="ignore"):
-        G_e = gate / (1.0 + np.exp(-gate)) * up
-    return G_e, G_e @ W2_e
+        return gate / (1.0 + np.exp(-gate)) * up
+
+
+def expert_down(G_e, W2_e):
+    """Step 9: Y_e = G_e W2."""
+    return G_e @ W2_e
+
+
+def swiglu_expert(X_e, W13_e, W2_e):
+    """Steps 8-9 for one expert.  Returns (G_e, Y_e)."""
+    G_e = expert_up(X_e, W13_e)
+    return G_e, expert_down(G_e, W2_e)
 
 
 def grouped_swiglu(x_perm, offsets, w13, w2):

@@ -18,23 +18,21 @@ def _fresh_oracle():
 
 
 def _swap_gate_up(M):
-    def swiglu_expert(X_e, W13_e, W2_e):
-        I = W2_e.shape[0]
+    def expert_up(X_e, W13_e):
+        I = W13_e.shape[1] // 2
         gu = X_e @ W13_e
         up, gate = gu[:, :I], gu[:, I:]
-        G = gate / (1.0 + np.exp(-gate)) * up
-        return G, G @ W2_e
-    M.swiglu_expert = swiglu_expert
+        return gate / (1.0 + np.exp(-gate)) * up
+    M.expert_up = expert_up
 
 
 def _silu_sign(M):
-    def swiglu_expert(X_e, W13_e, W2_e):
-        I = W2_e.shape[0]
+    def expert_up(X_e, W13_e):
+        I = W13_e.shape[1] // 2
         gu = X_e @ W13_e
         gate, up = gu[:, :I], gu[:, I:]
-        G = gate / (1.0 + np.exp(gate)) * up
-        return G, G @ W2_e
-    M.swiglu_expert = swiglu_expert
+        return gate / (1.0 + np.exp(gate)) * up
+    M.expert_up = expert_up
 
 
 def _drop_renorm(M):
@@ -118,13 +116,7 @@ def _gather_by_flat_not_token(M):
 
 
 def _w2_rows_reversed(M):
-    def swiglu_expert(X_e, W13_e, W2_e):
-        I = W2_e.shape[0]
-        gu = X_e @ W13_e
-        gate, up = gu[:, :I], gu[:, I:]
-        G = gate / (1.0 + np.exp(-gate)) * up
-        return G, G @ W2_e[::-1]              # wrong row index into W2
-    M.swiglu_expert = swiglu_expert
+    M.expert_down = lambda G_e, W2_e: G_e @ W2_e[::-1]       # wrong row index into W2
 
 
 MUTATIONS = [_swap_gate_up, _silu_sign, _drop_renorm, _ascending_topk, _ties_to_higher_index,
