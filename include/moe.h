@@ -1,0 +1,215 @@
+/*
+ * moe.h -- C ABI of the single-GPU MoE expert-layer forward (GB300, sm_103a).
+ *
+ * The layer is Algorithm 2 ("Single-GPU MoE Forward (OlmoeExperts)") of the
+ * page "MoE 分布式推理基础（基于 vLLM）", §1.2 "MoE Forward": router GEMM,
+ * softmax, TopK with optional renormalisation, the dispatch layout, the SwiGLU
+ * expert GEMMs and the weighted scatter-add combine.  One extra call runs two
+ * (or more) micro-batches on two CUDA streams so that one micro-batch's
+ * dispatch and combine overlap another's expert GEMMs (the cross-micro-batch
+ * schedule of the page "XTuner Domino EP", section "执行路径").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  The library
+ *    never allocates device memory on these calls and never synchronises the
+ *    host; work is enqueued on the stream(s) given.  Only moe_check_status()
+ *    blocks.
+ *  - Argument errors are returned synchronously, before anything is enqueued:
+ *    MOE_ERR_INVALID_ARG (null pointer, bad size, misaligned pointer),
+ *    MOE_ERR_UNSUPPORTED (a size this build does not handle),
+ *    MOE_ERR_WORKSPACE (workspace too small).  A failed launch returns
+ *    MOE_ERR_CUDA.
+ *  - Problems found on the device (an expert id outside [0, E), an
+ *    inconsistent layout, a pipeline wait that ran out of time) are OR-ed
+ *    into a caller-provided int32 status word as MOE_DEV_* bits; kernels then
+ *    skip the offending access instead of faulting.  The status word is never
+ *    cleared by the library except where stated; read it with
+ *    moe_check_status().
+ *  - Layouts are row-major.  Shapes (n tokens, hidden H, intermediate I,
+ *    E experts, K experts per token):
+ *        x       (n, H)        dtype
+ *        w_gate  (H, E)        dtype
+ *        bias    (E)           float32, optional per-expert logit bias
+ *        w13     (E, H, 2I)    dtype; columns [0, I) gate, [I, 2I) up
+ *        w2      (E, I, H)     dtype
+ *        logits  (n, E)        float32
+ *        topk_idx(n, K)        int32, slot order = descending logit
+ *        topk_w  (n, K)        float32
+ *        counts  (E), offsets (E+1), perm (n*K), inv_perm (n*K)   int32
+ *        x_perm  (n*K, H), h (n*K, I), y_perm (n*K, H), y (n, H)   dtype
+ *    dtype is float32 (MOE_F32) or bfloat16 (MOE_BF16).  Accumulation is
+ *    float32 in every GEMM and in the combine.
+ *  - bf16 layers need H % 64 == 0 and I % 128 == 0; float32 layers need
+ *    H % 4 == 0 and I % 4 == 0.  E <= 256, 1 <= K <= min(E, 16).
+ *    Pointers must be 16-byte aligned.
+ */
+#ifndef TOP_ROUTING_DISPATCH_GB300_MOE_H
+#define TOP_ROUTING_DISPATCH_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 (NULL) is the legacy default stream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_WORKSPACE = 3,
+  MOE_ERR_BAD_ROUTING = 4, /* from moe_check_status: an expert id was out of range */
+  MOE_ERR_CUDA = 5,
+  MOE_ERR_TIMEOUT = 6,     /* from moe_check_status: a device pipeline wait gave up */
+  MOE_ERR_BAD_LAYOUT = 7   /* from moe_check_status: offsets/perm inconsistent */
+} moe_status_t;
+
+/* Bits of the device status word. */
+#define MOE_DEV_BAD_ROUTING 0x1
+#define MOE_DEV_BAD_LAYOUT 0x2
+#define MOE_DEV_TIMEOUT 0x4
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+typedef struct {
+  int32_t n;              /* tokens (may be 0) */
+  int32_t H;              /* hidden size */
+  int32_t I;              /* expert intermediate size */
+  int32_t E;              /* experts */
+  int32_t K;              /* experts per token */
+  int32_t dtype;          /* moe_dtype_t */
+  int32_t norm_topk_prob; /* nonzero: divide the K weights by their sum */
+} moe_layer_desc_t;
+
+/* Library version string and a human-readable name of a status code. */
+const char *moe_version(void);
+const char *moe_status_string(moe_status_t status);
+
+/*
+ * Router: Algorithm 2 steps 1-3 and the renormalisation of the router shown
+ * in §1.2.  logits = x·w_gate (+ bias), p = softmax(logits) over E, then the
+ * K experts of largest logit in descending order (an exact tie goes to the
+ * lower expert index), topk_w = p at those experts, divided by their sum
+ * when norm_topk_prob.
+ *   x (n,H) dtype; w_gate (H,E) dtype; bias (E) float32 or NULL;
+ *   topk_idx (n,K) int32 out; topk_w (n,K) float32 out; logits (n,E) float32 out.
+ * The selection is made on float32 logits, except for tokens whose top-(K+1)
+ * float32 logits lie closer than a rounding margin: their candidate experts
+ * are rescored in double-float (about 48-bit) precision and selected on that.
+ */
+moe_status_t moe_route_topk(const moe_layer_desc_t *desc, const void *x, const void *w_gate,
+                            const float *bias, int32_t *topk_idx, float *topk_w, float *logits,
+                            moe_stream_t stream);
+
+/*
+ * Dispatch layout: Algorithm 2 steps 4-5 (hit counts n_e and the sets I_e),
+ * in the expert-sorted form of the moe_align_block_size example of §2.3
+ * (without block padding).  With f = t*K + k the flat index of a (token,
+ * slot) pair:
+ *   counts[e]   = number of pairs routed to e
+ *   offsets[e]  = sum of counts[e'] for e' < e; offsets[E] = pairs with a valid id
+ *   perm[r]     = f of the r-th pair after a stable sort by expert (ascending f
+ *                 inside each expert)
+ *   inv_perm[f] = r
+ * Deterministic (integer only).  Pairs whose id is outside [0, E) set
+ * MOE_DEV_BAD_ROUTING in *status_word and are placed after offsets[E], so
+ * perm stays a permutation of [0, n*K).
+ *   topk_idx (n,K) int32; status_word: one int32 (device), OR-ed into;
+ *   ws: moe_layout_workspace_size(desc) bytes of device scratch (contents
+ *   need no initialisation; not used after the call returns on the stream).
+ */
+size_t moe_layout_workspace_size(const moe_layer_desc_t *desc);
+moe_status_t moe_dispatch_layout(const moe_layer_desc_t *desc, const int32_t *topk_idx,
+                                 int32_t *counts, int32_t *offsets, int32_t *perm,
+                                 int32_t *inv_perm, int32_t *status_word, void *ws,
+                                 size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Permute (the gather of Algorithm 2 step 7 for all experts at once):
+ * x_perm[r] = x[perm[r] / K].  x (n,H), x_perm (n*K,H), perm (n*K).
+ * A perm entry outside [0, n*K) gives a zero row and sets MOE_DEV_BAD_LAYOUT
+ * in *status_word (status_word may be NULL, then such rows are only zeroed).
+ */
+moe_status_t moe_permute(const moe_layer_desc_t *desc, const void *x, const int32_t *perm,
+                         void *x_perm, int32_t *status_word, moe_stream_t stream);
+
+/*
+ * Grouped SwiGLU experts: Algorithm 2 steps 8-9 for every expert with a
+ * non-empty segment [offsets[e], offsets[e+1]) of x_perm:
+ *   [G | U] = x_perm[seg] · w13[e];  h[seg] = SiLU(G) * U;  y_perm[seg] = h[seg] · w2[e]
+ * with SiLU(g) = g / (1 + exp(-g)).  h is rounded to dtype before the second
+ * GEMM.  bf16 layers run on the tcgen05 tensor cores (TMA-fed, TMEM
+ * accumulators, SiLU*up in the first GEMM's epilogue); float32 layers run on
+ * float32 FMA units.  Rows of y_perm at or after offsets[E] are not written.
+ * sm_reserve: number of SMs left free for work on other streams (0 = all).
+ * offsets must be as produced by moe_dispatch_layout; an inconsistent table
+ * sets MOE_DEV_BAD_LAYOUT and nothing is computed.  No workspace is needed.
+ */
+moe_status_t moe_grouped_swiglu(const moe_layer_desc_t *desc, const void *x_perm, const void *w13,
+                                const void *w2, const int32_t *offsets, void *h, void *y_perm,
+                                int sm_reserve, int32_t *status_word, moe_stream_t stream);
+
+/*
+ * Combine (Algorithm 2 steps 10-11, as a gather per token instead of a
+ * scatter-add): y[t] = sum_{k=0..K-1} topk_w[t,k] * y_perm[inv_perm[t*K+k]],
+ * accumulated in float32 in slot order k = 0..K-1 and rounded once.  No
+ * atomics: the result is bitwise reproducible.  An inv_perm entry outside
+ * [0, n*K) contributes nothing and sets MOE_DEV_BAD_LAYOUT (status_word may
+ * be NULL).
+ */
+moe_status_t moe_combine(const moe_layer_desc_t *desc, const void *y_perm, const float *topk_w,
+                         const int32_t *inv_perm, void *y, int32_t *status_word,
+                         moe_stream_t stream);
+
+/*
+ * Whole layer for num_mb micro-batches that share one set of weights,
+ * scheduled on two streams as in "XTuner Domino EP" (执行路径) and the
+ * two-micro-batch interleave of "大模型系统中的通算融合" §3.1:
+ *   dispatch stream: route, layout, permute of micro-batch j+1 while the
+ *                    compute stream runs micro-batch j's expert GEMMs;
+ *                    combine of micro-batch j while the compute stream runs
+ *                    micro-batch j+1's GEMMs.
+ * Events order producer and consumer only; the host never waits.  When the
+ * call returns, all work is enqueued; `compute` is made to wait for the last
+ * combine, so completion of `compute` means every y[j] is final.  With
+ * dispatch == compute (or NULL) everything runs in order on one stream.
+ *   x[j], y[j]: arrays of num_mb device pointers, each (n,H) dtype.
+ *   ws: num_mb * moe_workspace_size(desc) bytes, 256-byte aligned; it holds
+ *   each micro-batch's intermediates (logits, topk, layout, x_perm, h, y_perm).
+ *   status_word: one int32 (device) or NULL; cleared at the start of the call
+ *   (stream-ordered) and then OR-ed into.  NULL uses a word inside ws.
+ *   sm_reserve: SMs the GEMMs leave free for the dispatch stream.
+ * Results are bitwise identical to running the micro-batches one after
+ * another (no result depends on grid size or stream timing).
+ */
+size_t moe_workspace_size(const moe_layer_desc_t *desc);
+moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
+                                      const void *const *x, const void *w_gate, const float *bias,
+                                      const void *w13, const void *w2, void *const *y, void *ws,
+                                      size_t ws_bytes, int sm_reserve, int32_t *status_word,
+                                      moe_stream_t compute, moe_stream_t dispatch);
+
+/*
+ * Device-side pointers into a micro-batch's slice of the workspace used by
+ * moe_forward_microbatches (for inspection in tests).  `which`:
+ * 0 logits, 1 topk_idx, 2 topk_w, 3 counts, 4 offsets, 5 perm, 6 inv_perm,
+ * 7 x_perm, 8 h, 9 y_perm, 10 internal status word.  Returns NULL on a bad
+ * argument.  No device access.
+ */
+void *moe_workspace_slot(const moe_layer_desc_t *desc, void *ws, int mb, int which);
+
+/*
+ * Blocks until `stream` is idle, then reads *status_word and maps it to
+ * MOE_OK, MOE_ERR_BAD_ROUTING, MOE_ERR_BAD_LAYOUT or MOE_ERR_TIMEOUT (first
+ * match in that order).  Intended for tests and debugging.
+ */
+moe_status_t moe_check_status(const int32_t *status_word, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,154 @@
+"""The C ABI library builds, loads, exports what include/moe.h declares, and
+its host-only calls behave -- no GPU needed (no call here reaches the device)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+needs_nvcc = pytest.mark.skipif(
+    not (shutil.which("nvcc") or os.path.exists("/usr/local/cuda/bin/nvcc")),
+    reason="CUDA toolkit not installed")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_routing_dispatch_gb300 import build as B
+    B.build()
+    from top_routing_dispatch_gb300 import _lib
+    return _lib.load()
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"\b(moe_[a-z_]+)\s*\(", src)
+
+
+def test_header_matches_binding_list():
+    from top_routing_dispatch_gb300 import _lib
+    assert sorted(set(header_functions())) == sorted(_lib.SYMBOLS)
+
+
+@needs_nvcc
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+@needs_nvcc
+def test_exported_dynamic_symbols(lib):
+    out = os.popen(f"nm -D --defined-only {lib._name}").read()
+    exported = set(re.findall(r"\bT (moe_[a-z_]+)\b", out))
+    assert set(header_functions()) <= exported
+
+
+@needs_nvcc
+def test_version_and_status_strings(lib):
+    assert b"sm_103a" in lib.moe_version()
+    for code in range(8):
+        assert lib.moe_status_string(code)
+    assert lib.moe_status_string(99) == b"unknown status"
+
+
+def _desc(**kw):
+    from top_routing_dispatch_gb300._lib import LayerDesc
+    d = dict(n=4096, H=2048, I=1024, E=64, K=8, dtype=1, norm_topk_prob=0)
+    d.update(kw)
+    return LayerDesc(**d)
+
+
+@needs_nvcc
+def test_workspace_sizes(lib):
+    d = _desc()
+    ws = lib.moe_workspace_size(ctypes.byref(d))
+    nK = 4096 * 8
+    # x_perm + h + y_perm dominate
+    assert ws >= nK * 2048 * 2 * 2 + nK * 1024 * 2
+    assert ws % 256 == 0
+    lw = lib.moe_layout_workspace_size(ctypes.byref(d))
+    assert lw == 2 * ((nK + 2047) // 2048) * 65 * 4
+    assert lib.moe_workspace_size(ctypes.byref(_desc(E=0))) == 0
+    assert lib.moe_workspace_size(None) == 0
+
+
+@needs_nvcc
+def test_workspace_slots_are_ordered_and_aligned(lib):
+    d = _desc(n=100, H=256, I=128, E=8, K=2)
+    base = 1 << 20
+    per = lib.moe_workspace_size(ctypes.byref(d))
+    prev = None
+    for mb in range(2):
+        for which in range(11):
+            p = lib.moe_workspace_slot(ctypes.byref(d), ctypes.c_void_p(base), mb, which)
+            assert p % 256 == 0
+            assert base + mb * per <= p < base + (mb + 1) * per
+            if prev is not None:
+                assert p > prev
+            prev = p
+    assert lib.moe_workspace_slot(ctypes.byref(d), ctypes.c_void_p(base), 0, 11) is None
+    assert lib.moe_workspace_slot(ctypes.byref(d), None, 0, 0) is None
+
+
+@needs_nvcc
+@pytest.mark.parametrize("bad", [
+    dict(n=-1), dict(H=0), dict(E=0), dict(K=0), dict(K=9, E=8), dict(dtype=7),
+])
+def test_invalid_desc_rejected_before_any_launch(lib, bad):
+    d = _desc(**bad)
+    nullp = ctypes.c_void_p(None)
+    st = lib.moe_route_topk(ctypes.byref(d), nullp, nullp, nullp, nullp, nullp, nullp, nullp)
+    assert st == 1  # MOE_ERR_INVALID_ARG
+    st = lib.moe_permute(ctypes.byref(d), nullp, nullp, nullp, nullp, nullp)
+    assert st == 1
+
+
+@needs_nvcc
+@pytest.mark.parametrize("bad,code", [
+    (dict(E=300), 2), (dict(K=17, E=64), 2), (dict(H=2047), 2),
+])
+def test_unsupported_sizes(lib, bad, code):
+    d = _desc(**bad)
+    nullp = ctypes.c_void_p(None)
+    st = lib.moe_combine(ctypes.byref(d), nullp, nullp, nullp, nullp, nullp, nullp)
+    assert st == code
+
+
+@needs_nvcc
+def test_gemm_shape_rules(lib):
+    nullp = ctypes.c_void_p(None)
+    for kw in (dict(I=1000), dict(H=2048 + 32)):   # bf16 needs I % 128, H % 64
+        d = _desc(**kw)
+        st = lib.moe_grouped_swiglu(ctypes.byref(d), nullp, nullp, nullp, nullp, nullp, nullp, 0,
+                                    nullp, nullp)
+        assert st == 2
+    # null pointers with a valid shape
+    st = lib.moe_grouped_swiglu(ctypes.byref(_desc()), nullp, nullp, nullp, nullp, nullp, nullp,
+                                0, nullp, nullp)
+    assert st == 1
+
+
+@needs_nvcc
+def test_forward_microbatches_argument_checks(lib):
+    d = _desc(n=64, H=256, I=128, E=8, K=2)
+    nullp = ctypes.c_void_p(None)
+    xs = (ctypes.c_void_p * 2)(4096, 8192)
+    # misaligned workspace
+    st = lib.moe_forward_microbatches(ctypes.byref(d), 2, xs, ctypes.c_void_p(256), nullp,
+                                      ctypes.c_void_p(256), ctypes.c_void_p(256), xs,
+                                      ctypes.c_void_p(16), 1 << 30, 0, nullp, nullp, nullp)
+    assert st == 1
+    # too small a workspace
+    st = lib.moe_forward_microbatches(ctypes.byref(d), 2, xs, ctypes.c_void_p(256), nullp,
+                                      ctypes.c_void_p(256), ctypes.c_void_p(256), xs,
+                                      ctypes.c_void_p(1 << 20), 1024, 0, nullp, nullp, nullp)
+    assert st == 3
+    # bad micro-batch count
+    st = lib.moe_forward_microbatches(ctypes.byref(d), 0, xs, ctypes.c_void_p(256), nullp,
+                                      ctypes.c_void_p(256), ctypes.c_void_p(256), xs,
+                                      ctypes.c_void_p(1 << 20), 1 << 30, 0, nullp, nullp, nullp)
+    assert st == 1

@@ -1,0 +1,167 @@
+"""GPU parity: every step of the layer against the fp64 oracle, through the
+C ABI.  Sizes the oracle finishes in seconds are compared element by element;
+the full workloads are compared on every token for routing/layout and on
+sampled tokens for the expert outputs."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from tests.gpu_helpers import Run, TOL, rel_fro, valid_near_tie_choice, f64
+from workloads import TINY, OLMOE, SKEW, DSV3
+from workloads.configs import MoEConfig
+
+pytestmark = pytest.mark.gpu
+
+# small shapes that still span several tiles and a ragged tail
+SMALL = [
+    TINY,
+    OLMOE.with_(name="olmoe_n512", n=512),
+    MoEConfig("ragged_bf16", n=333, H=192, I=256, E=16, K=4, dtype="bf16",
+              norm_topk_prob=True, seed=21),
+    MoEConfig("ragged_skew_bf16", n=300, H=256, I=128, E=12, K=3, dtype="bf16",
+              norm_topk_prob=False, seed=22, skew=True),
+    MoEConfig("one_expert_bf16", n=130, H=128, I=128, E=1, K=1, dtype="bf16",
+              norm_topk_prob=False, seed=23),
+    MoEConfig("k_equals_e_f32", n=50, H=64, I=32, E=4, K=4, dtype="f32",
+              norm_topk_prob=True, seed=24),
+    MoEConfig("one_token_bf16", n=1, H=128, I=128, E=8, K=2, dtype="bf16",
+              norm_topk_prob=True, seed=25),
+]
+FULL = [OLMOE, SKEW, DSV3]
+
+
+def check_router(run, rows=None):
+    cfg = run.cfg
+    lo = run.oracle_logits()
+    lg = run.np("logits")
+    near = O.near_tie_tokens(lo, cfg.K)
+    gi = run.np("topk_idx")
+    gw = run.np("topk_w")
+    oe, ow = O.topk(lo, cfg.K, cfg.norm_topk_prob)
+    ok = ~near
+    assert np.array_equal(gi[ok], oe[ok]), "TopK indices differ on non-near-tie tokens"
+    for t in np.where(near)[0]:
+        assert valid_near_tie_choice(lo[t], gi[t], cfg.K), f"token {t}: invalid near-tie choice"
+    rel = np.abs(gw[ok] - ow[ok]) / np.maximum(np.abs(ow[ok]), 1e-30)
+    assert rel.max(initial=0) <= 1e-5, rel.max()
+    fin = np.isfinite(lo)
+    err = np.abs(lg[fin] - lo[fin]).max(initial=0)
+    # float32 logits: far inside the near-tie rescoring margin (1e-3 * max(1, |l|))
+    assert err < 2.5e-4, err
+    return err, int(near.sum())
+
+
+def check_layout(run):
+    cfg = run.cfg
+    gi = run.np("topk_idx")
+    counts, offsets, perm, inv = O.dispatch_layout(gi, cfg.E)
+    assert np.array_equal(run.np("counts"), counts)
+    assert np.array_equal(run.np("offsets"), offsets)
+    assert np.array_equal(run.np("perm"), perm)
+    assert np.array_equal(run.np("inv_perm"), inv)
+
+
+def check_permute(run, sample_rows=None):
+    """x_perm against the oracle's gather, exactly (bf16/f32 -> f64 is exact)."""
+    perm = run.np("perm")
+    xp = run.view("x_perm")
+    if sample_rows is None:
+        assert np.array_equal(f64(xp), O.permute(f64(run.x), perm, run.cfg.K))
+        return
+    r = np.asarray(sample_rows)
+    got = f64(xp[torch.as_tensor(r, device=xp.device)])
+    ref = O.permute(f64(run.x), perm[r], run.cfg.K)
+    assert np.array_equal(got, ref)
+
+
+def check_experts(run, sample_rows=None):
+    """GPU h and y_perm against the oracle's SwiGLU of the GPU's own x_perm."""
+    cfg = run.cfg
+    off = run.np("offsets")
+    xp = run.view("x_perm")
+    h = run.view("h")
+    yp = run.view("y_perm")
+    nK = cfg.nK
+    rows = np.arange(nK) if sample_rows is None else np.asarray(sorted(set(sample_rows)))
+    experts = np.searchsorted(off, rows, side="right") - 1
+    hs, ys, ho, yo = [], [], [], []
+    for e in np.unique(experts):
+        r = rows[experts == e]
+        ri = torch.as_tensor(r, device=xp.device)
+        # GEMM1+SwiGLU on the GPU's x_perm; GEMM2 on the GPU's (rounded) h
+        ho.append(O.expert_up(f64(xp[ri]), run.w13_get(int(e))))
+        yo.append(O.expert_down(f64(h[ri]), run.w2_get(int(e))))
+        hs.append(f64(h[ri]))
+        ys.append(f64(yp[ri]))
+    tol = TOL[cfg.dtype]
+    eh = rel_fro(np.concatenate(hs), np.concatenate(ho))
+    ey = rel_fro(np.concatenate(ys), np.concatenate(yo))
+    assert eh <= tol, f"h error {eh:.3e}"
+    assert ey <= tol, f"y_perm error {ey:.3e}"
+    return eh, ey
+
+
+def check_combine(run):
+    cfg = run.cfg
+    yo = O.combine(run.np("y_perm"), run.np("topk_w"), run.np("inv_perm"))
+    err = rel_fro(f64(run.y), yo)
+    assert err <= (4e-3 if cfg.dtype == "bf16" else 1e-6), err
+
+
+def check_layer(run, rows=None):
+    r = run.oracle_layer(rows)
+    y = f64(run.y) if rows is None else f64(run.y[torch.as_tensor(rows, device=run.y.device)])
+    err = rel_fro(y, r["y"])
+    assert err <= TOL[run.cfg.dtype], f"layer error {err:.3e}"
+    gi = run.np("topk_idx") if rows is None else run.np("topk_idx")[np.asarray(rows)]
+    ok = ~r["near"]
+    assert np.array_equal(gi[ok], r["e_top"][ok])
+    return err
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_small_all_steps(cfg):
+    run = Run(cfg)
+    assert run.status == 0
+    check_router(run)
+    check_layout(run)
+    check_permute(run)
+    check_experts(run)
+    check_combine(run)
+    check_layer(run)
+
+
+@pytest.mark.parametrize("cfg", FULL, ids=lambda c: c.name)
+def test_full_size(cfg):
+    run = Run(cfg)
+    assert run.status == 0
+    err, n_near = check_router(run)
+    check_layout(run)
+    rng = np.random.default_rng(0)
+    check_permute(run, rng.choice(cfg.nK, size=4096, replace=False))
+    off = run.np("offsets")
+    # rows at every expert-segment start/end and tile seams, plus random rows,
+    # restricted to a few experts (the hottest, the coldest non-empty, random)
+    counts = run.np("counts")
+    nz = np.where(counts > 0)[0]
+    pick = {int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])}
+    pick |= set(int(e) for e in rng.choice(nz, size=min(4, len(nz)), replace=False))
+    rows = []
+    for e in sorted(pick):
+        lo, hi = off[e], off[e + 1]
+        seg = np.arange(lo, hi)
+        rows += list(seg[:3]) + list(seg[-3:]) + list(seg[127:130]) + list(
+            rng.choice(seg, size=min(64, len(seg)), replace=False))
+    check_experts(run, rows)
+    check_combine(run)
+    toks = sorted(set(rng.choice(cfg.n, size=96, replace=False).tolist() + [0, cfg.n - 1]))
+    check_layer(run, toks)
+
+
+def test_skew_workload_is_skewed():
+    run = Run(SKEW)
+    counts = run.np("counts")
+    cv = O.count_cv(counts)
+    assert 1.35 <= cv <= 1.65, cv
+    assert int((counts == 0).sum()) == 4

@@ -1,0 +1,80 @@
+"""ctypes binding of libmoe_gb300.so (the C ABI declared in include/moe.h).
+
+Argument marshalling only.  Loading fails loudly if the library has not been
+built: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_NAME = "libmoe_gb300.so"
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
+
+# C ABI symbols, in header order (tests check the library exports each one).
+SYMBOLS = (
+    "moe_version", "moe_status_string", "moe_route_topk", "moe_layout_workspace_size",
+    "moe_dispatch_layout", "moe_permute", "moe_grouped_swiglu", "moe_combine",
+    "moe_workspace_size", "moe_forward_microbatches", "moe_workspace_slot", "moe_check_status",
+)
+
+MOE_F32, MOE_BF16 = 0, 1
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT",
+          7: "MOE_ERR_BAD_LAYOUT"}
+DEV_BAD_ROUTING, DEV_BAD_LAYOUT, DEV_TIMEOUT = 0x1, 0x2, 0x4
+
+# workspace slots of moe_workspace_slot
+SLOT = dict(logits=0, topk_idx=1, topk_w=2, counts=3, offsets=4, perm=5, inv_perm=6,
+            x_perm=7, h=8, y_perm=9, status=10)
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("K", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("norm_topk_prob", ctypes.c_int32)]
+
+
+_vp = ctypes.c_void_p
+_desc_p = ctypes.POINTER(LayerDesc)
+_st = ctypes.c_int
+
+
+def _declare(lib):
+    sig = {
+        "moe_version": (ctypes.c_char_p, []),
+        "moe_status_string": (ctypes.c_char_p, [_st]),
+        "moe_route_topk": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+        "moe_layout_workspace_size": (ctypes.c_size_t, [_desc_p]),
+        "moe_dispatch_layout": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                      ctypes.c_size_t, _vp]),
+        "moe_permute": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp]),
+        "moe_grouped_swiglu": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
+                                     _vp, _vp]),
+        "moe_combine": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp]),
+        "moe_workspace_size": (ctypes.c_size_t, [_desc_p]),
+        "moe_forward_microbatches": (_st, [_desc_p, ctypes.c_int, ctypes.POINTER(_vp), _vp, _vp,
+                                           _vp, _vp, ctypes.POINTER(_vp), _vp, ctypes.c_size_t,
+                                           ctypes.c_int, _vp, _vp, _vp]),
+        "moe_workspace_slot": (_vp, [_desc_p, _vp, ctypes.c_int, ctypes.c_int]),
+        "moe_check_status": (_st, [_vp, _vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_LIB = None
+
+
+def load():
+    """The loaded library (cached).  Raises ImportError when it is missing."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing; build it with `python -m top_routing_dispatch_gb300.build`")
+        _LIB = _declare(ctypes.CDLL(LIB_PATH))
+    return _LIB

@@ -1,0 +1,183 @@
+"""Python face of the C ABI: the same calls, taking torch tensors.
+
+torch provides device memory and streams only; every step of the layer runs
+in the library's CUDA kernels.  Each function checks the returned status and
+raises MoEError on anything but MOE_OK.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import LayerDesc, MOE_BF16, MOE_F32, SLOT  # noqa: F401
+
+_DT = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16}
+_TORCH = {MOE_F32: torch.float32, MOE_BF16: torch.bfloat16}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        lib = _lib.load()
+        msg = lib.moe_status_string(status).decode()
+        super().__init__(f"{where}: {_lib.STATUS.get(status, status)} ({msg})")
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MoEError(status, where)
+
+
+def _p(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(s):
+    if s is None:
+        s = torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
+
+
+def make_desc(n, H, I, E, K, dtype, norm_topk_prob) -> LayerDesc:
+    if isinstance(dtype, torch.dtype):
+        dtype = _DT[dtype]
+    elif isinstance(dtype, str):
+        dtype = {"f32": MOE_F32, "bf16": MOE_BF16}[dtype]
+    return LayerDesc(int(n), int(H), int(I), int(E), int(K), int(dtype), int(bool(norm_topk_prob)))
+
+
+def desc_for(cfg, n=None) -> LayerDesc:
+    """LayerDesc of a workload config (anything with n, H, I, E, K, dtype, norm_topk_prob)."""
+    return make_desc(cfg.n if n is None else n, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype,
+                     cfg.norm_topk_prob)
+
+
+def torch_dtype(desc: LayerDesc):
+    return _TORCH[desc.dtype]
+
+
+# ------------------------------------------------------------ the six calls
+def moe_route_topk(desc, x, w_gate, bias, topk_idx, topk_w, logits, stream=None):
+    _check(_lib.load().moe_route_topk(ctypes.byref(desc), _p(x), _p(w_gate), _p(bias),
+                                      _p(topk_idx), _p(topk_w), _p(logits), _stream(stream)),
+           "moe_route_topk")
+
+
+def moe_layout_workspace_size(desc) -> int:
+    return int(_lib.load().moe_layout_workspace_size(ctypes.byref(desc)))
+
+
+def moe_dispatch_layout(desc, topk_idx, counts, offsets, perm, inv_perm, status_word, ws,
+                        stream=None):
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(_lib.load().moe_dispatch_layout(ctypes.byref(desc), _p(topk_idx), _p(counts),
+                                           _p(offsets), _p(perm), _p(inv_perm), _p(status_word),
+                                           _p(ws), nbytes, _stream(stream)),
+           "moe_dispatch_layout")
+
+
+def moe_permute(desc, x, perm, x_perm, status_word=None, stream=None):
+    _check(_lib.load().moe_permute(ctypes.byref(desc), _p(x), _p(perm), _p(x_perm),
+                                   _p(status_word), _stream(stream)), "moe_permute")
+
+
+def moe_grouped_swiglu(desc, x_perm, w13, w2, offsets, h, y_perm, sm_reserve=0, status_word=None,
+                       stream=None):
+    _check(_lib.load().moe_grouped_swiglu(ctypes.byref(desc), _p(x_perm), _p(w13), _p(w2),
+                                          _p(offsets), _p(h), _p(y_perm), int(sm_reserve),
+                                          _p(status_word), _stream(stream)),
+           "moe_grouped_swiglu")
+
+
+def moe_combine(desc, y_perm, topk_w, inv_perm, y, status_word=None, stream=None):
+    _check(_lib.load().moe_combine(ctypes.byref(desc), _p(y_perm), _p(topk_w), _p(inv_perm),
+                                   _p(y), _p(status_word), _stream(stream)), "moe_combine")
+
+
+def moe_workspace_size(desc) -> int:
+    return int(_lib.load().moe_workspace_size(ctypes.byref(desc)))
+
+
+def moe_forward_microbatches(desc, xs, w_gate, bias, w13, w2, ys, ws, sm_reserve=0,
+                             status_word=None, compute=None, dispatch=None):
+    n = len(xs)
+    xa = (ctypes.c_void_p * n)(*[x.data_ptr() for x in xs])
+    ya = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
+    nbytes = ws.numel() * ws.element_size()
+    _check(_lib.load().moe_forward_microbatches(
+        ctypes.byref(desc), n, xa, _p(w_gate), _p(bias), _p(w13), _p(w2), ya, _p(ws), nbytes,
+        int(sm_reserve), _p(status_word), _stream(compute),
+        _stream(dispatch) if dispatch is not None else ctypes.c_void_p(None)),
+        "moe_forward_microbatches")
+
+
+def moe_workspace_slot(desc, ws, mb, which) -> int:
+    if isinstance(which, str):
+        which = SLOT[which]
+    p = _lib.load().moe_workspace_slot(ctypes.byref(desc), _p(ws), int(mb), int(which))
+    if not p:
+        raise ValueError("bad workspace slot request")
+    return int(p)
+
+
+def moe_check_status(status_word, stream=None) -> int:
+    """Synchronises `stream` and returns the mapped status code (0 = OK)."""
+    return int(_lib.load().moe_check_status(_p(status_word), _stream(stream)))
+
+
+# ------------------------------------------------------------ conveniences
+def workspace_view(desc, ws, mb, name):
+    """A torch view of one micro-batch's intermediate inside the workspace."""
+    dt = torch_dtype(desc)
+    nK = desc.n * desc.K
+    shapes = dict(logits=((desc.n, desc.E), torch.float32), topk_idx=((desc.n, desc.K), torch.int32),
+                  topk_w=((desc.n, desc.K), torch.float32), counts=((desc.E,), torch.int32),
+                  offsets=((desc.E + 1,), torch.int32), perm=((nK,), torch.int32),
+                  inv_perm=((nK,), torch.int32), x_perm=((nK, desc.H), dt), h=((nK, desc.I), dt),
+                  y_perm=((nK, desc.H), dt), status=((1,), torch.int32))
+    shape, dtype = shapes[name]
+    addr = moe_workspace_slot(desc, ws, mb, name)
+    base = ws.data_ptr()
+    off = addr - base
+    esz = torch.empty((), dtype=dtype).element_size()
+    count = 1
+    for s in shape:
+        count *= s
+    flat = ws.view(torch.uint8)[off:off + count * esz].view(dtype)
+    return flat.view(*shape)
+
+
+class MoELayer:
+    """One MoE expert layer with resident weights and a reusable workspace.
+
+    weights: w_gate (H,E), w13 (E,H,2I), w2 (E,I,H) in the layer dtype on the
+    device, bias (E,) float32 or None.
+    """
+
+    def __init__(self, desc: LayerDesc, w_gate, bias, w13, w2, num_mb=1):
+        self.desc = desc
+        self.w_gate, self.bias, self.w13, self.w2 = w_gate, bias, w13, w2
+        dev = w13.device
+        self.num_mb = num_mb
+        self.ws = torch.empty(moe_workspace_size(desc) * num_mb, dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def forward(self, xs, ys=None, sm_reserve=0, compute=None, dispatch=None):
+        if ys is None:
+            ys = [torch.empty_like(x) for x in xs]
+        moe_forward_microbatches(self.desc, xs, self.w_gate, self.bias, self.w13, self.w2, ys,
+                                 self.ws, sm_reserve, self.status, compute, dispatch)
+        return ys
+
+    def __call__(self, x):
+        return self.forward([x])[0]
+
+    def view(self, name, mb=0):
+        return workspace_view(self.desc, self.ws, mb, name)
+
+    def check(self, stream=None):
+        _check(moe_check_status(self.status, stream), "device status")

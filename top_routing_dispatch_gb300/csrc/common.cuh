@@ -1,0 +1,65 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 16;
+
+struct Desc {
+  int n, H, I, E, K;
+  bool bf16;
+  bool norm;
+  long long nK() const { return (long long)n * K; }
+};
+
+inline size_t elem_bytes(const Desc &d) { return d.bf16 ? 2 : 4; }
+
+// ---- router.cu
+cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, const float *bias,
+                          int32_t *topk_idx, float *topk_w, float *logits, cudaStream_t s);
+
+// ---- layout.cu
+size_t layout_ws_bytes(const Desc &d);
+cudaError_t launch_layout(const Desc &d, const int32_t *topk_idx, int32_t *counts,
+                          int32_t *offsets, int32_t *perm, int32_t *inv_perm, int32_t *status,
+                          void *ws, cudaStream_t s);
+
+// ---- permute_combine.cu
+cudaError_t launch_permute(const Desc &d, const void *x, const int32_t *perm, void *x_perm,
+                           int32_t *status, cudaStream_t s);
+cudaError_t launch_combine(const Desc &d, const void *y_perm, const float *topk_w,
+                           const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s);
+
+// ---- gemm_tc.cu (bf16, tcgen05) and gemm_simt.cu (float32)
+cudaError_t launch_grouped_swiglu_tc(const Desc &d, const void *x_perm, const void *w13,
+                                     const void *w2, const int32_t *offsets, void *h,
+                                     void *y_perm, int sm_reserve, int32_t *status,
+                                     cudaStream_t s);
+cudaError_t launch_grouped_swiglu_simt(const Desc &d, const void *x_perm, const void *w13,
+                                       const void *w2, const int32_t *offsets, void *h,
+                                       void *y_perm, int sm_reserve, int32_t *status,
+                                       cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace moe
+
+// ---- device helpers
+namespace moe {
+
+__device__ __forceinline__ void flag_status(int32_t *status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// Number of m-tiles of `bm` rows for segment lengths given by offsets.
+__device__ __forceinline__ int ceil_div_dev(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace moe

@@ -1,0 +1,421 @@
+// Grouped SwiGLU expert GEMMs on the tcgen05 tensor cores (bf16 in, f32
+// accumulate in TMEM), "MoE 分布式推理基础（基于 vLLM）" §1.2, Algorithm 2
+// steps 8-9 and "SwiGLU expert 的两段 GEMM":
+//   GEMM1: [G | U] = X_e · W13[e] (H x 2I), h = SiLU(G) * U   (fused epilogue)
+//   GEMM2: Y_e = h · W2[e] (I x H)
+// over the expert segments [offsets[e], offsets[e+1]) of the expert-sorted
+// rows.  Putting SiLU*up in the first GEMM's epilogue follows the L1
+// epilogue of the DeepGEMM Mega MoE kernel described in "大模型系统中的通算
+// 融合" §4 (one L1 GEMM produces gate and up, the epilogue applies SwiGLU).
+//
+// Design (one persistent CTA per SM, 6 warps):
+//   warp 0      TMA producer: A tile (128 rows x 64 k) of the activations and
+//               four B boxes (64 k x 64 n) of the expert's weights per stage.
+//   warp 1      TMEM allocator and MMA issuer: 4 x tcgen05.mma 128x256x16 per
+//               stage into one of two 256-column TMEM accumulators.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
+//               SiLU(gate)*up (GEMM1) or plain conversion (GEMM2), bf16 stores
+//               of the rows that belong to the tile's expert.
+// A tile is (m-tile, n-tile).  m-tiles are 128-row windows that start at each
+// expert's segment start, so every tile belongs to exactly one expert; its
+// rows past the segment end are computed but not stored (TMA zero-fills rows
+// past the tensor).  Tiles are dealt to CTAs round-robin; every tile costs the
+// same (full K loop), so the static schedule balances.  Each tile is computed
+// entirely by one CTA with a fixed k order: results do not depend on the grid
+// size.
+//
+// B is the weight matrix as stored (k rows, n contiguous): an MN-major UMMA
+// operand with 128-byte swizzle.  A is K-major with 128-byte swizzle.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BK = 64, UMMA_N = 256, UMMA_K = 16, STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_BOX_BYTES = 64 * BK * 2;            // 8 KB: 64 n x 64 k
+constexpr int B_STAGE_BYTES = 4 * B_BOX_BYTES;      // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;                      // two 256-column accumulators
+
+struct SmemTail {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int ok;
+  int total_mtiles;
+  int off[kMaxE + 1];
+  int tp[kMaxE + 1];  // first m-tile of each expert (exclusive prefix)
+};
+
+constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES +
+                              sizeof(SmemTail);
+
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/true);
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
+                                              volatile int *abort_flag, int32_t *status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > ptx::kWaitLimitCycles) {
+      *abort_flag = 1;
+      flag_status(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+struct TileInfo {
+  int e, row0, rows, nt;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const SmemTail &s, int t, int n_tiles, int E) {
+  TileInfo ti;
+  const int mt = t / n_tiles;
+  ti.nt = t - mt * n_tiles;
+  int lo = 0, hi = E;  // largest e with tp[e] <= mt
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s.tp[mid] <= mt)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  ti.e = lo;
+  ti.row0 = s.off[lo] + (mt - s.tp[lo]) * BM;
+  const int left = s.off[lo + 1] - ti.row0;
+  ti.rows = left < BM ? left : BM;
+  return ti;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+// MODE 1: GEMM1 + SwiGLU (B = W13, out = h, n-tile = 128 h columns)
+// MODE 2: GEMM2          (B = W2,  out = y_perm, n-tile = 256 columns)
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const int32_t *__restrict__ offsets, int E, int nK, int Kdim, int I,
+                           int Nout, __nv_bfloat16 *__restrict__ out, int32_t *status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *smemA = smem;
+  uint8_t *smemB = smem + STAGES * A_STAGE_BYTES;
+  SmemTail &st = *reinterpret_cast<SmemTail *>(smem + STAGES * STAGE_BYTES);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_tiles = MODE == 1 ? I / 128 : (Nout + UMMA_N - 1) / UMMA_N;
+  const int KB = Kdim / BK;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&st.full[s], 1);
+      ptx::mbar_init(&st.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&st.tfull[a], 1);
+      ptx::mbar_init(&st.tempty[a], 4);
+    }
+    ptx::mbar_init(&st.drain, 1);
+    st.abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  for (int c = tid; c <= E; c += NUM_THREADS) st.off[c] = offsets[c];
+  __syncthreads();
+  if (tid == 0) {
+    bool ok = st.off[0] == 0 && st.off[E] <= nK;
+    int run = 0;
+    for (int e = 0; e < E; ++e) {
+      const int len = st.off[e + 1] - st.off[e];
+      ok = ok && len >= 0;
+      st.tp[e] = run;
+      run += len > 0 ? (len + BM - 1) / BM : 0;
+    }
+    st.tp[E] = run;
+    st.total_mtiles = run;
+    st.ok = ok;
+    if (!ok && blockIdx.x == 0) flag_status(status, MOE_DEV_BAD_LAYOUT);
+  }
+  __syncthreads();
+  if (!st.ok) return;
+  const int total = st.total_mtiles * n_tiles;
+  if ((int)blockIdx.x >= total) return;
+
+  if (warp == 1) {
+    ptx::tmem_alloc(&st.tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = st.tmem_base;
+  volatile int *abort_flag = &st.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t used = 0, last_par = 0;  // per stage: ever used, parity of last issue
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const TileInfo ti = decode_tile(st, t, n_tiles, E);
+        bool stop = false;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_or_abort(&st.empty[stage], phase ^ 1u, abort_flag, status)) {
+            stop = true;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&st.full[stage], STAGE_BYTES);
+          ptx::tma_load_2d(smemA + stage * A_STAGE_BYTES, &tmA, &st.full[stage], kb * BK,
+                           ti.row0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            int ncol;
+            if (MODE == 1)
+              ncol = (q < 2 ? 0 : I) + ti.nt * 128 + (q & 1) * 64;
+            else
+              ncol = ti.nt * UMMA_N + q * 64;
+            ptx::tma_load_3d(smemB + stage * B_STAGE_BYTES + q * B_BOX_BYTES, &tmB,
+                             &st.full[stage], ncol, kb * BK, ti.e);
+          }
+          used |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (stop) break;
+      }
+      // never leave a TMA copy in flight: wait for the last load of every stage
+      for (int s = 0; s < STAGES; ++s)
+        if (used >> s & 1u) ptx::mbar_wait(&st.full[s], last_par >> s & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        if (!wait_or_abort(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status)) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * UMMA_N);
+        bool stop = false;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_or_abort(&st.full[stage], phase, abort_flag, status)) {
+            stop = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_u32(smemA + stage * A_STAGE_BYTES);
+          const uint32_t b0 = ptx::smem_u32(smemB + stage * B_STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // A: K-major SW128, k step of 16 elements = 32 bytes inside the atom
+            const uint64_t adesc = ptx::smem_desc(a0 + kk * 32, 16, 1024);
+            // B: MN-major SW128, 64-wide n atoms 8 KB apart, k step = 16 rows
+            const uint64_t bdesc = ptx::smem_desc(b0 + kk * 2048, B_BOX_BYTES, 1024);
+            ptx::mma_bf16(d, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&st.empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (stop) break;
+        ptx::mma_commit(&st.tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // wait until every MMA this thread issued has finished
+      ptx::mma_commit(&st.drain);
+      ptx::mbar_wait(&st.drain, 0);
+    }
+  } else {
+    // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileInfo ti = decode_tile(st, t, n_tiles, E);
+      if (!wait_or_abort(&st.tfull[acc], acc_phase, abort_flag, status)) break;
+      ptx::tc_fence_after();
+      const uint32_t tbase = tmem + (uint32_t)(acc * UMMA_N) + ((uint32_t)(q * 32) << 16);
+      const bool valid = r < ti.rows;
+      if (MODE == 1) {
+        __nv_bfloat16 *orow = out + (size_t)(ti.row0 + (valid ? r : 0)) * I + ti.nt * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld_32x32b_x32(tbase + c * 32, g);
+          ptx::tmem_ld_32x32b_x32(tbase + 128 + c * 32, u);
+          ptx::tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+            const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+            pk[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+          }
+          if (valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      } else {
+        __nv_bfloat16 *orow = out + (size_t)(ti.row0 + (valid ? r : 0)) * Nout + ti.nt * UMMA_N;
+#pragma unroll 1
+        for (int c = 0; c < UMMA_N / 32; ++c) {
+          if (ti.nt * UMMA_N + c * 32 >= Nout) break;  // uniform across the warp
+          uint32_t a[32];
+          ptx::tmem_ld_32x32b_x32(tbase + c * 32, a);
+          ptx::tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+          if (valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&st.tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    __syncwarp();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                 uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint32_t b0, uint32_t b1) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t set_smem_attr() {
+  static int done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_swiglu_tc(const Desc &d, const void *x_perm, const void *w13,
+                                     const void *w2, const int32_t *offsets, void *h,
+                                     void *y_perm, int sm_reserve, int32_t *status,
+                                     cudaStream_t s) {
+  const long long nK = d.nK();
+  if (nK == 0) return cudaSuccess;
+  CUtensorMap mA1, mB1, mA2, mB2;
+  if (!make_map_2d(&mA1, x_perm, d.H, nK, BK, BM) ||
+      !make_map_3d(&mB1, w13, 2ull * d.I, d.H, d.E, 64, BK) ||
+      !make_map_2d(&mA2, h, d.I, nK, BK, BM) ||
+      !make_map_3d(&mB2, w2, d.H, d.I, d.E, 64, BK))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr<1>();
+  if (e != cudaSuccess) return e;
+  e = set_smem_attr<2>();
+  if (e != cudaSuccess) return e;
+  int grid = device_sm_count() - (sm_reserve > 0 ? sm_reserve : 0);
+  if (grid < 1) grid = 1;
+  grouped_gemm_tc_kernel<1><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(
+      mA1, mB1, offsets, d.E, (int)nK, d.H, d.I, d.I, reinterpret_cast<__nv_bfloat16 *>(h),
+      status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  grouped_gemm_tc_kernel<2><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(
+      mA2, mB2, offsets, d.E, (int)nK, d.I, d.I, d.H, reinterpret_cast<__nv_bfloat16 *>(y_perm),
+      status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,334 @@
+// C ABI of the MoE layer: argument checks, workspace layout, and the
+// two-stream micro-batch schedule.  Kernels live in the other .cu files.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int sms = 1;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared checks of the layer description.
+moe_status_t check_desc(const moe_layer_desc_t *d, Desc *out) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->n < 0 || d->H < 1 || d->I < 1 || d->E < 1 || d->K < 1) return MOE_ERR_INVALID_ARG;
+  if (d->K > d->E) return MOE_ERR_INVALID_ARG;
+  if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (d->E > kMaxE || d->K > kMaxK) return MOE_ERR_UNSUPPORTED;
+  if ((long long)d->n * d->K > 0x7fffffffll) return MOE_ERR_UNSUPPORTED;
+  const bool bf16 = d->dtype == MOE_BF16;
+  // rows move as 16-byte vectors
+  if (bf16 ? (d->H % 8) : (d->H % 4)) return MOE_ERR_UNSUPPORTED;
+  out->n = d->n;
+  out->H = d->H;
+  out->I = d->I;
+  out->E = d->E;
+  out->K = d->K;
+  out->bf16 = bf16;
+  out->norm = d->norm_topk_prob != 0;
+  return MOE_OK;
+}
+
+moe_status_t check_gemm_shape(const Desc &d) {
+  if (d.bf16) {
+    if (d.H % 64 || d.I % 128) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (d.I % 4) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+constexpr size_t kAlign = 256;
+inline size_t up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+enum Slot {
+  S_LOGITS = 0, S_TOPK_IDX, S_TOPK_W, S_COUNTS, S_OFFSETS, S_PERM, S_INV_PERM,
+  S_X_PERM, S_H, S_Y_PERM, S_STATUS, S_LAYOUT_WS, S_COUNT
+};
+
+void slot_sizes(const Desc &d, size_t sz[S_COUNT]) {
+  const size_t nK = (size_t)d.nK(), eb = elem_bytes(d);
+  sz[S_LOGITS] = (size_t)d.n * d.E * 4;
+  sz[S_TOPK_IDX] = nK * 4;
+  sz[S_TOPK_W] = nK * 4;
+  sz[S_COUNTS] = (size_t)d.E * 4;
+  sz[S_OFFSETS] = (size_t)(d.E + 1) * 4;
+  sz[S_PERM] = nK * 4;
+  sz[S_INV_PERM] = nK * 4;
+  sz[S_X_PERM] = nK * d.H * eb;
+  sz[S_H] = nK * d.I * eb;
+  sz[S_Y_PERM] = nK * d.H * eb;
+  sz[S_STATUS] = 4;
+  sz[S_LAYOUT_WS] = layout_ws_bytes(d);
+}
+
+size_t mb_bytes(const Desc &d) {
+  size_t sz[S_COUNT];
+  slot_sizes(d, sz);
+  size_t tot = 0;
+  for (int i = 0; i < S_COUNT; ++i) tot += up(sz[i] ? sz[i] : 1);
+  return tot;
+}
+
+uint8_t *slot_ptr(const Desc &d, void *ws, int mb, int which) {
+  size_t sz[S_COUNT];
+  slot_sizes(d, sz);
+  size_t off = mb_bytes(d) * (size_t)mb;
+  for (int i = 0; i < which; ++i) off += up(sz[i] ? sz[i] : 1);
+  return reinterpret_cast<uint8_t *>(ws) + off;
+}
+
+// Events reused by moe_forward_microbatches, per device.  A wait captures the
+// most recent record at the time it is enqueued, so reuse across calls is
+// safe; the mutex serialises enqueueing from several host threads.
+constexpr int kMaxMB = 64;
+struct EventPool {
+  cudaEvent_t ev[2 * kMaxMB + 2];
+  bool ready = false;
+};
+EventPool g_pools[64];
+std::mutex g_pool_mu;
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_version(void) { return "top_routing_dispatch_gb300 0.1 (sm_103a)"; }
+
+const char *moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size or configuration";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_BAD_ROUTING: return "expert id out of range in topk_idx";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case MOE_ERR_BAD_LAYOUT: return "inconsistent dispatch layout";
+  }
+  return "unknown status";
+}
+
+moe_status_t moe_route_topk(const moe_layer_desc_t *desc, const void *x, const void *w_gate,
+                            const float *bias, int32_t *topk_idx, float *topk_w, float *logits,
+                            moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  if (d.n == 0) return MOE_OK;
+  if (!x || !w_gate || !topk_idx || !topk_w || !logits) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router(d, x, w_gate, bias, topk_idx, topk_w, logits, stream));
+}
+
+size_t moe_layout_workspace_size(const moe_layer_desc_t *desc) {
+  Desc d;
+  if (check_desc(desc, &d) != MOE_OK) return 0;
+  return layout_ws_bytes(d);
+}
+
+moe_status_t moe_dispatch_layout(const moe_layer_desc_t *desc, const int32_t *topk_idx,
+                                 int32_t *counts, int32_t *offsets, int32_t *perm,
+                                 int32_t *inv_perm, int32_t *status_word, void *ws,
+                                 size_t ws_bytes, moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  if (!counts || !offsets || !status_word) return MOE_ERR_INVALID_ARG;
+  if (d.nK() > 0 && (!topk_idx || !perm || !inv_perm || !ws)) return MOE_ERR_INVALID_ARG;
+  if (d.nK() > 0 && ws_bytes < layout_ws_bytes(d)) return MOE_ERR_WORKSPACE;
+  return cuda_status(
+      launch_layout(d, topk_idx, counts, offsets, perm, inv_perm, status_word, ws, stream));
+}
+
+moe_status_t moe_permute(const moe_layer_desc_t *desc, const void *x, const int32_t *perm,
+                         void *x_perm, int32_t *status_word, moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  if (d.nK() == 0) return MOE_OK;
+  if (!x || !perm || !x_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_permute(d, x, perm, x_perm, status_word, stream));
+}
+
+moe_status_t moe_grouped_swiglu(const moe_layer_desc_t *desc, const void *x_perm, const void *w13,
+                                const void *w2, const int32_t *offsets, void *h, void *y_perm,
+                                int sm_reserve, int32_t *status_word, moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  st = check_gemm_shape(d);
+  if (st != MOE_OK) return st;
+  if (d.nK() == 0) return MOE_OK;
+  if (!x_perm || !w13 || !w2 || !offsets || !h || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w13) || !aligned16(w2) || !aligned16(h) ||
+      !aligned16(y_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (sm_reserve < 0) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = d.bf16 ? launch_grouped_swiglu_tc(d, x_perm, w13, w2, offsets, h, y_perm,
+                                                    sm_reserve, status_word, stream)
+                         : launch_grouped_swiglu_simt(d, x_perm, w13, w2, offsets, h, y_perm,
+                                                      sm_reserve, status_word, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_combine(const moe_layer_desc_t *desc, const void *y_perm, const float *topk_w,
+                         const int32_t *inv_perm, void *y, int32_t *status_word,
+                         moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  if (d.n == 0) return MOE_OK;
+  if (!y_perm || !topk_w || !inv_perm || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(d, y_perm, topk_w, inv_perm, y, status_word, stream));
+}
+
+size_t moe_workspace_size(const moe_layer_desc_t *desc) {
+  Desc d;
+  if (check_desc(desc, &d) != MOE_OK) return 0;
+  return mb_bytes(d);
+}
+
+void *moe_workspace_slot(const moe_layer_desc_t *desc, void *ws, int mb, int which) {
+  Desc d;
+  if (!ws || mb < 0 || which < 0 || which >= S_LAYOUT_WS) return nullptr;
+  if (check_desc(desc, &d) != MOE_OK) return nullptr;
+  return slot_ptr(d, ws, mb, which);
+}
+
+moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
+                                      const void *const *x, const void *w_gate, const float *bias,
+                                      const void *w13, const void *w2, void *const *y, void *ws,
+                                      size_t ws_bytes, int sm_reserve, int32_t *status_word,
+                                      moe_stream_t compute, moe_stream_t dispatch) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  st = check_gemm_shape(d);
+  if (st != MOE_OK) return st;
+  if (num_mb < 1 || num_mb > kMaxMB || !x || !y || sm_reserve < 0) return MOE_ERR_INVALID_ARG;
+  if (!w_gate || !w13 || !w2 || !ws) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < mb_bytes(d) * (size_t)num_mb) return MOE_ERR_WORKSPACE;
+  for (int j = 0; j < num_mb; ++j) {
+    if (d.n > 0 && (!x[j] || !y[j] || !aligned16(x[j]) || !aligned16(y[j])))
+      return MOE_ERR_INVALID_ARG;
+  }
+  if (!aligned16(w13) || !aligned16(w2)) return MOE_ERR_INVALID_ARG;
+  int32_t *status = status_word ? status_word
+                                : reinterpret_cast<int32_t *>(slot_ptr(d, ws, 0, S_STATUS));
+  cudaStream_t sc = compute;
+  cudaStream_t sd = dispatch ? dispatch : compute;
+  const bool two = sd != sc;
+
+  auto front = [&](int j, cudaStream_t s) -> cudaError_t {  // route + layout + permute
+    int32_t *idx = (int32_t *)slot_ptr(d, ws, j, S_TOPK_IDX);
+    cudaError_t e = launch_router(d, x[j], w_gate, bias, idx,
+                                  (float *)slot_ptr(d, ws, j, S_TOPK_W),
+                                  (float *)slot_ptr(d, ws, j, S_LOGITS), s);
+    if (e != cudaSuccess) return e;
+    e = launch_layout(d, idx, (int32_t *)slot_ptr(d, ws, j, S_COUNTS),
+                      (int32_t *)slot_ptr(d, ws, j, S_OFFSETS),
+                      (int32_t *)slot_ptr(d, ws, j, S_PERM),
+                      (int32_t *)slot_ptr(d, ws, j, S_INV_PERM), status,
+                      slot_ptr(d, ws, j, S_LAYOUT_WS), s);
+    if (e != cudaSuccess) return e;
+    return launch_permute(d, x[j], (int32_t *)slot_ptr(d, ws, j, S_PERM),
+                          slot_ptr(d, ws, j, S_X_PERM), status, s);
+  };
+  auto experts = [&](int j, cudaStream_t s) -> cudaError_t {
+    const int32_t *off = (const int32_t *)slot_ptr(d, ws, j, S_OFFSETS);
+    return d.bf16 ? launch_grouped_swiglu_tc(d, slot_ptr(d, ws, j, S_X_PERM), w13, w2, off,
+                                             slot_ptr(d, ws, j, S_H),
+                                             slot_ptr(d, ws, j, S_Y_PERM), two ? sm_reserve : 0,
+                                             status, s)
+                  : launch_grouped_swiglu_simt(d, slot_ptr(d, ws, j, S_X_PERM), w13, w2, off,
+                                               slot_ptr(d, ws, j, S_H),
+                                               slot_ptr(d, ws, j, S_Y_PERM), 0, status, s);
+  };
+  auto back = [&](int j, cudaStream_t s) -> cudaError_t {
+    return launch_combine(d, slot_ptr(d, ws, j, S_Y_PERM),
+                          (const float *)slot_ptr(d, ws, j, S_TOPK_W),
+                          (const int32_t *)slot_ptr(d, ws, j, S_INV_PERM), y[j], status, s);
+  };
+
+  if (!two) {
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), sc);
+    for (int j = 0; j < num_mb && e == cudaSuccess; ++j) {
+      e = front(j, sc);
+      if (e == cudaSuccess) e = experts(j, sc);
+      if (e == cudaSuccess) e = back(j, sc);
+    }
+    return cuda_status(e);
+  }
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  EventPool &pool = g_pools[dev];
+  if (!pool.ready) {
+    for (int i = 0; i < 2 * kMaxMB + 2; ++i)
+      if (cudaEventCreateWithFlags(&pool.ev[i], cudaEventDisableTiming) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    pool.ready = true;
+  }
+  cudaEvent_t ev_start = pool.ev[2 * kMaxMB], ev_done = pool.ev[2 * kMaxMB + 1];
+  cudaEvent_t *ev_front = pool.ev, *ev_gemm = pool.ev + kMaxMB;
+
+  // the dispatch stream starts after whatever the caller queued on `compute`
+  cudaError_t e = cudaEventRecord(ev_start, sc);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_start, 0);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), sd);
+  for (int j = 0; j < num_mb && e == cudaSuccess; ++j) {
+    e = front(j, sd);                                            // dispatch of j
+    if (e == cudaSuccess) e = cudaEventRecord(ev_front[j], sd);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, ev_front[j], 0);
+    if (e == cudaSuccess) e = experts(j, sc);                    // experts of j
+    if (e == cudaSuccess) e = cudaEventRecord(ev_gemm[j], sc);
+    if (j > 0) {                                                 // combine of j-1
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_gemm[j - 1], 0);
+      if (e == cudaSuccess) e = back(j - 1, sd);
+    }
+  }
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_gemm[num_mb - 1], 0);
+  if (e == cudaSuccess) e = back(num_mb - 1, sd);
+  if (e == cudaSuccess) e = cudaEventRecord(ev_done, sd);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, ev_done, 0);
+  return cuda_status(e);
+}
+
+moe_status_t moe_check_status(const int32_t *status_word, moe_stream_t stream) {
+  if (!status_word) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, status_word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (v & MOE_DEV_BAD_ROUTING) return MOE_ERR_BAD_ROUTING;
+  if (v & MOE_DEV_BAD_LAYOUT) return MOE_ERR_BAD_LAYOUT;
+  if (v & MOE_DEV_TIMEOUT) return MOE_ERR_TIMEOUT;
+  return MOE_OK;
+}
+
+}  // extern "C"

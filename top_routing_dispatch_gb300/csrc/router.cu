@@ -1,0 +1,312 @@
+// Router: logits = x·W_gate (+ bias), softmax over experts, TopK, optional
+// renormalisation.  "MoE 分布式推理基础（基于 vLLM）" §1.2, Algorithm 2 steps
+// 1-3 and the router's norm_topk_prob branch.
+//
+// Two kernels:
+//  1. router_logits_kernel: SIMT tiled GEMM (n x H)·(H x E) with float32
+//     accumulation in per-tile partial sums (32 products per partial, then
+//     added to the running sum), bias added last.  Products of bf16 inputs are
+//     exact in float32, so only the additions round.
+//  2. router_topk_kernel: one warp per token.  Max, sum of exp and K+1 rounds
+//     of a warp argmax (ties to the lower expert id) over the float32 logits.
+//     If two of the top K+1 logits lie closer than a margin tau (far above the
+//     float32 error of kernel 1), the experts that can still be in the top K
+//     are rescored in double-float arithmetic (exact products, error-free
+//     sums) and the K best are chosen on those values.  The choice therefore
+//     matches an exact evaluation except for gaps near double-float rounding.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int RBM = 32, RBN = 64, RBK = 32, RTHREADS = 128;
+
+template <bool BF16>
+__device__ __forceinline__ float ld_in(const void *p, size_t i) {
+  if constexpr (BF16)
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
+  else
+    return reinterpret_cast<const float *>(p)[i];
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(RTHREADS) router_logits_kernel(
+    const void *__restrict__ x, const void *__restrict__ wg, const float *__restrict__ bias,
+    float *__restrict__ logits, int n, int H, int E) {
+  __shared__ float As[RBK][RBM + 4];  // k-major
+  __shared__ float Bs[RBK][RBN + 4];
+  const int tid = threadIdx.x;
+  const int m0 = blockIdx.x * RBM, n0 = blockIdx.y * RBN;
+  const int tx = tid % 16, ty = tid / 16;  // 16 x 8 threads, 4x4 outputs each
+  float total[4][4] = {};
+  for (int k0 = 0; k0 < H; k0 += RBK) {
+    // A tile: 32 rows x 32 k; thread loads 8 consecutive k of one row
+    {
+      const int r = tid / 4, kk = (tid % 4) * 8;
+      const int gm = m0 + r;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int gk = k0 + kk + j;
+        As[kk + j][r] = (gm < n && gk < H) ? ld_in<BF16>(x, (size_t)gm * H + gk) : 0.f;
+      }
+    }
+    // B tile: 32 k x 64 experts
+#pragma unroll
+    for (int j = 0; j < (RBK * RBN) / RTHREADS; ++j) {
+      const int idx = tid + j * RTHREADS;
+      const int kk = idx / RBN, c = idx % RBN;
+      const int gk = k0 + kk, gn = n0 + c;
+      Bs[kk][c] = (gk < H && gn < E) ? ld_in<BF16>(wg, (size_t)gk * E + gn) : 0.f;
+    }
+    __syncthreads();
+    float part[4][4] = {};
+#pragma unroll 8
+    for (int kk = 0; kk < RBK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) part[i][j] = fmaf(a[i], b[j], part[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) total[i][j] += part[i][j];
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int gm = m0 + ty * 4 + i;
+    if (gm >= n) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int gn = n0 + tx * 4 + j;
+      if (gn < E) logits[(size_t)gm * E + gn] = total[i][j] + (bias ? bias[gn] : 0.f);
+    }
+  }
+}
+
+// ---- double-float helpers (error-free transformations, no FMA contraction)
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  const float bb = __fsub_rn(s, a.hi);
+  float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+  err = __fadd_rn(err, __fadd_rn(a.lo, b.lo));
+  const float hi = __fadd_rn(s, err);
+  return DF{hi, __fsub_rn(err, __fsub_rn(hi, s))};
+}
+
+__device__ __forceinline__ DF two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return DF{p, fmaf(a, b, -p)};
+}
+
+__device__ __forceinline__ bool df_greater(DF a, int ea, DF b, int eb) {
+  if (a.hi != b.hi) return a.hi > b.hi;
+  if (a.lo != b.lo) return a.lo > b.lo;
+  return ea < eb;
+}
+
+// (value, expert) argmax across the warp; ties to the lower expert id.
+__device__ __forceinline__ void warp_argmax(float &v, int &e) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oe = __shfl_xor_sync(0xffffffffu, e, o);
+    if (ov > v || (ov == v && oe < e)) {
+      v = ov;
+      e = oe;
+    }
+  }
+}
+
+constexpr int TOPK_WARPS = 8;
+
+template <int EPL, bool BF16>
+__global__ void __launch_bounds__(TOPK_WARPS * 32) router_topk_kernel(
+    const float *__restrict__ logits, const void *__restrict__ x, const void *__restrict__ wg,
+    const float *__restrict__ bias, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+    int n, int H, int E, int K, int norm) {
+  __shared__ float s_hi[TOPK_WARPS][kMaxK];
+  __shared__ float s_lo[TOPK_WARPS][kMaxK];
+  __shared__ int s_e[TOPK_WARPS][kMaxK];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int t = blockIdx.x * TOPK_WARPS + wib;
+  if (t >= n) return;
+  const float NEG = -INFINITY;
+  float v[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? logits[(size_t)t * E + e] : NEG;
+  }
+  float m = NEG;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) m = fmaxf(m, v[j]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j)
+    if (lane + 32 * j < E) s += expf(v[j] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+
+  // K+1 rounds of argmax over the unselected experts
+  const int R = K + 1 < E ? K + 1 : E;
+  unsigned taken = 0;
+  float top_v[kMaxK + 1];
+  int top_e[kMaxK + 1];
+#pragma unroll
+  for (int r = 0; r < kMaxK + 1; ++r) {
+    if (r >= R) break;
+    float bv = NEG;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !(taken >> j & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
+        bv = v[j];
+        be = e;
+      }
+    }
+    warp_argmax(bv, be);
+    top_v[r] = bv;
+    top_e[r] = be;
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+  }
+
+  // near-tie check among the top K+1 (finite values only)
+  const float tau = 1e-3f * fmaxf(1.f, fabsf(top_v[0]));
+  bool amb = false;
+#pragma unroll
+  for (int r = 0; r + 1 < kMaxK + 1; ++r) {
+    if (r + 1 >= R) break;
+    if (isfinite(top_v[r]) && isfinite(top_v[r + 1]) && top_v[r] - top_v[r + 1] < tau) amb = true;
+  }
+
+  if (amb) {  // warp-uniform: every lane holds the same top_v
+    float vK = top_v[0];
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r)
+      if (r == K - 1) vK = top_v[r];
+    const float thr = vK - tau;
+    int cnt = 0;  // entries in the per-warp sorted list (uniform)
+    for (int j = 0; j < EPL; ++j) {
+      const int e_l = lane + 32 * j;
+      unsigned ball = __ballot_sync(0xffffffffu, e_l < E && v[j] >= thr);
+      while (ball) {
+        const int b = __ffs(ball) - 1;
+        ball &= ball - 1;
+        const int e = b + 32 * j;
+        DF acc{0.f, 0.f};
+        for (int hh = lane; hh < H; hh += 32)
+          acc = df_add(acc, two_prod(ld_in<BF16>(x, (size_t)t * H + hh),
+                                     ld_in<BF16>(wg, (size_t)hh * E + e)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          DF other{__shfl_xor_sync(0xffffffffu, acc.hi, o), __shfl_xor_sync(0xffffffffu, acc.lo, o)};
+          acc = df_add(acc, other);
+        }
+        if (bias) {
+          const float bb = bias[e];
+          if (isinf(bb))
+            acc = DF{bb, 0.f};
+          else
+            acc = df_add(acc, DF{bb, 0.f});
+        }
+        // insert (acc, e) into the warp's sorted list of at most K entries
+        if (lane == 0) {
+          int pos = cnt < K ? cnt : K;
+          while (pos > 0 && df_greater(acc, e, DF{s_hi[wib][pos - 1], s_lo[wib][pos - 1]},
+                                       s_e[wib][pos - 1]))
+            --pos;
+          if (pos < K) {
+            const int last = (cnt < K ? cnt : K - 1);
+            for (int q = last; q > pos; --q) {
+              s_hi[wib][q] = s_hi[wib][q - 1];
+              s_lo[wib][q] = s_lo[wib][q - 1];
+              s_e[wib][q] = s_e[wib][q - 1];
+            }
+            s_hi[wib][pos] = acc.hi;
+            s_lo[wib][pos] = acc.lo;
+            s_e[wib][pos] = e;
+          }
+        }
+        cnt = cnt < K ? cnt + 1 : K;
+        __syncwarp();
+      }
+    }
+    // cnt >= K always: the K experts of largest float32 logit are candidates
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r)
+      if (r < K) top_e[r] = s_e[wib][r];
+    __syncwarp();
+  }
+
+  // weights: p at the chosen experts (float32 softmax), optional renormalisation
+  float w = 0.f;
+  int e_mine = 0;
+  if (lane < K) {
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r)
+      if (r == lane) e_mine = top_e[r];
+    w = expf(logits[(size_t)t * E + e_mine] - m) / s;
+  }
+  if (norm) {
+    float tot = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r) {
+      const float wr = __shfl_sync(0xffffffffu, w, r);
+      if (r < K) tot += wr;
+    }
+    w = w / tot;
+  }
+  if (lane < K) {
+    topk_idx[(size_t)t * K + lane] = e_mine;
+    topk_w[(size_t)t * K + lane] = w;
+  }
+}
+
+template <int EPL>
+cudaError_t launch_topk(const Desc &d, const float *logits, const void *x, const void *wg,
+                        const float *bias, int32_t *idx, float *w, cudaStream_t s) {
+  dim3 grid((d.n + TOPK_WARPS - 1) / TOPK_WARPS);
+  if (d.bf16)
+    router_topk_kernel<EPL, true><<<grid, TOPK_WARPS * 32, 0, s>>>(logits, x, wg, bias, idx, w,
+                                                                    d.n, d.H, d.E, d.K, d.norm);
+  else
+    router_topk_kernel<EPL, false><<<grid, TOPK_WARPS * 32, 0, s>>>(logits, x, wg, bias, idx, w,
+                                                                     d.n, d.H, d.E, d.K, d.norm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, const float *bias,
+                          int32_t *topk_idx, float *topk_w, float *logits, cudaStream_t s) {
+  if (d.n == 0) return cudaSuccess;
+  dim3 grid((d.n + RBM - 1) / RBM, (d.E + RBN - 1) / RBN);
+  if (d.bf16)
+    router_logits_kernel<true><<<grid, RTHREADS, 0, s>>>(x, w_gate, bias, logits, d.n, d.H, d.E);
+  else
+    router_logits_kernel<false><<<grid, RTHREADS, 0, s>>>(x, w_gate, bias, logits, d.n, d.H, d.E);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (d.E <= 32) return launch_topk<1>(d, logits, x, w_gate, bias, topk_idx, topk_w, s);
+  if (d.E <= 64) return launch_topk<2>(d, logits, x, w_gate, bias, topk_idx, topk_w, s);
+  if (d.E <= 128) return launch_topk<4>(d, logits, x, w_gate, bias, topk_idx, topk_w, s);
+  return launch_topk<8>(d, logits, x, w_gate, bias, topk_idx, topk_w, s);
+}
+
+}  // namespace moe
