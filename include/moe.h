@@ -154,6 +154,18 @@ moe_status_t moe_grouped_swiglu(const moe_layer_desc_t *desc, const void *x_perm
                                 int sm_reserve, int32_t *status_word, moe_stream_t stream);
 
 /*
+ * The two halves of moe_grouped_swiglu as separate calls (same kernels, same
+ * results): GEMM1 with the SwiGLU epilogue writes h; GEMM2 reads h and writes
+ * y_perm.  Arguments as for moe_grouped_swiglu.
+ */
+moe_status_t moe_expert_gemm1_swiglu(const moe_layer_desc_t *desc, const void *x_perm,
+                                     const void *w13, const int32_t *offsets, void *h,
+                                     int sm_reserve, int32_t *status_word, moe_stream_t stream);
+moe_status_t moe_expert_gemm2(const moe_layer_desc_t *desc, const void *h, const void *w2,
+                              const int32_t *offsets, void *y_perm, int sm_reserve,
+                              int32_t *status_word, moe_stream_t stream);
+
+/*
  * Combine (Algorithm 2 steps 10-11, as a gather per token instead of a
  * scatter-add): y[t] = sum_{k=0..K-1} topk_w[t,k] * y_perm[inv_perm[t*K+k]],
  * accumulated in float32 in slot order k = 0..K-1 and rounded once.  No

@@ -26,7 +26,7 @@ def lib():
 def header_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return re.findall(r"\b(moe_[a-z_]+)\s*\(", src)
+    return re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)
 
 
 def test_header_matches_binding_list():
@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 @needs_nvcc
 def test_exported_dynamic_symbols(lib):
     out = os.popen(f"nm -D --defined-only {lib._name}").read()
-    exported = set(re.findall(r"\bT (moe_[a-z_]+)\b", out))
+    exported = set(re.findall(r"\bT (moe_[a-z0-9_]+)\b", out))
     assert set(header_functions()) <= exported
 
 

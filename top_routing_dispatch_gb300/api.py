@@ -93,6 +93,20 @@ def moe_grouped_swiglu(desc, x_perm, w13, w2, offsets, h, y_perm, sm_reserve=0, 
            "moe_grouped_swiglu")
 
 
+def moe_expert_gemm1_swiglu(desc, x_perm, w13, offsets, h, sm_reserve=0, status_word=None,
+                            stream=None):
+    _check(_lib.load().moe_expert_gemm1_swiglu(ctypes.byref(desc), _p(x_perm), _p(w13),
+                                               _p(offsets), _p(h), int(sm_reserve),
+                                               _p(status_word), _stream(stream)),
+           "moe_expert_gemm1_swiglu")
+
+
+def moe_expert_gemm2(desc, h, w2, offsets, y_perm, sm_reserve=0, status_word=None, stream=None):
+    _check(_lib.load().moe_expert_gemm2(ctypes.byref(desc), _p(h), _p(w2), _p(offsets),
+                                        _p(y_perm), int(sm_reserve), _p(status_word),
+                                        _stream(stream)), "moe_expert_gemm2")
+
+
 def moe_combine(desc, y_perm, topk_w, inv_perm, y, status_word=None, stream=None):
     _check(_lib.load().moe_combine(ctypes.byref(desc), _p(y_perm), _p(topk_w), _p(inv_perm),
                                    _p(y), _p(status_word), _stream(stream)), "moe_combine")

@@ -38,14 +38,27 @@ cudaError_t launch_combine(const Desc &d, const void *y_perm, const float *topk_
                            const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s);
 
 // ---- gemm_tc.cu (bf16, tcgen05) and gemm_simt.cu (float32)
-cudaError_t launch_grouped_swiglu_tc(const Desc &d, const void *x_perm, const void *w13,
-                                     const void *w2, const int32_t *offsets, void *h,
-                                     void *y_perm, int sm_reserve, int32_t *status,
-                                     cudaStream_t s);
-cudaError_t launch_grouped_swiglu_simt(const Desc &d, const void *x_perm, const void *w13,
-                                       const void *w2, const int32_t *offsets, void *h,
-                                       void *y_perm, int sm_reserve, int32_t *status,
-                                       cudaStream_t s);
+cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
+                            const int32_t *offsets, void *h, int sm_reserve, int32_t *status,
+                            cudaStream_t s);
+cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const int32_t *offsets,
+                            void *y_perm, int sm_reserve, int32_t *status, cudaStream_t s);
+cudaError_t launch_gemm1_simt(const Desc &d, const void *x_perm, const void *w13,
+                              const int32_t *offsets, void *h, int32_t *status, cudaStream_t s);
+cudaError_t launch_gemm2_simt(const Desc &d, const void *h, const void *w2,
+                              const int32_t *offsets, void *y_perm, int32_t *status,
+                              cudaStream_t s);
+
+// GEMM1 (+SwiGLU) then GEMM2 for the layer's dtype.
+inline cudaError_t launch_experts(const Desc &d, const void *x_perm, const void *w13,
+                                  const void *w2, const int32_t *offsets, void *h, void *y_perm,
+                                  int sm_reserve, int32_t *status, cudaStream_t s) {
+  cudaError_t e = d.bf16 ? launch_gemm1_tc(d, x_perm, w13, offsets, h, sm_reserve, status, s)
+                         : launch_gemm1_simt(d, x_perm, w13, offsets, h, status, s);
+  if (e != cudaSuccess) return e;
+  return d.bf16 ? launch_gemm2_tc(d, h, w2, offsets, y_perm, sm_reserve, status, s)
+                : launch_gemm2_simt(d, h, w2, offsets, y_perm, status, s);
+}
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

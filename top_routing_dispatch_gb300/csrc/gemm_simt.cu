@@ -175,23 +175,32 @@ __global__ void __launch_bounds__(256) simt_gemm2(const float *__restrict__ h,
 
 }  // namespace
 
-cudaError_t launch_grouped_swiglu_simt(const Desc &d, const void *x_perm, const void *w13,
-                                       const void *w2, const int32_t *offsets, void *h,
-                                       void *y_perm, int sm_reserve, int32_t *status,
-                                       cudaStream_t s) {
-  (void)sm_reserve;  // small grids; every block exits early once past the tile count
+namespace {
+inline int simt_max_mtiles(const Desc &d) {
+  return (int)((d.nK() + SBM - 1) / SBM) + d.E;  // >= sum_e ceil(n_e / SBM)
+}
+}  // namespace
+
+cudaError_t launch_gemm1_simt(const Desc &d, const void *x_perm, const void *w13,
+                              const int32_t *offsets, void *h, int32_t *status, cudaStream_t s) {
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
-  const int max_mtiles = (int)((nK + SBM - 1) / SBM) + d.E;  // >= sum_e ceil(n_e / SBM)
-  dim3 g1(max_mtiles, (d.I + SBN - 1) / SBN), g2(max_mtiles, (d.H + SBN - 1) / SBN);
-  simt_gemm1<<<g1, 256, 0, s>>>(reinterpret_cast<const float *>(x_perm),
-                                reinterpret_cast<const float *>(w13), offsets, d.E, (int)nK, d.H,
-                                d.I, reinterpret_cast<float *>(h), status);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  simt_gemm2<<<g2, 256, 0, s>>>(reinterpret_cast<const float *>(h),
-                                reinterpret_cast<const float *>(w2), offsets, d.E, (int)nK, d.H,
-                                d.I, reinterpret_cast<float *>(y_perm), status);
+  dim3 g(simt_max_mtiles(d), (d.I + SBN - 1) / SBN);
+  simt_gemm1<<<g, 256, 0, s>>>(reinterpret_cast<const float *>(x_perm),
+                               reinterpret_cast<const float *>(w13), offsets, d.E, (int)nK, d.H,
+                               d.I, reinterpret_cast<float *>(h), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm2_simt(const Desc &d, const void *h, const void *w2,
+                              const int32_t *offsets, void *y_perm, int32_t *status,
+                              cudaStream_t s) {
+  const long long nK = d.nK();
+  if (nK == 0) return cudaSuccess;
+  dim3 g(simt_max_mtiles(d), (d.H + SBN - 1) / SBN);
+  simt_gemm2<<<g, 256, 0, s>>>(reinterpret_cast<const float *>(h),
+                               reinterpret_cast<const float *>(w2), offsets, d.E, (int)nK, d.H,
+                               d.I, reinterpret_cast<float *>(y_perm), status);
   return cudaGetLastError();
 }
 

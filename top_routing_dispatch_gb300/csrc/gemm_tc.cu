@@ -387,33 +387,41 @@ cudaError_t set_smem_attr() {
   return e;
 }
 
+int gemm_grid(int sm_reserve) {
+  const int g = device_sm_count() - (sm_reserve > 0 ? sm_reserve : 0);
+  return g < 1 ? 1 : g;
+}
+
 }  // namespace
 
-cudaError_t launch_grouped_swiglu_tc(const Desc &d, const void *x_perm, const void *w13,
-                                     const void *w2, const int32_t *offsets, void *h,
-                                     void *y_perm, int sm_reserve, int32_t *status,
-                                     cudaStream_t s) {
+cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
+                            const int32_t *offsets, void *h, int sm_reserve, int32_t *status,
+                            cudaStream_t s) {
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
-  CUtensorMap mA1, mB1, mA2, mB2;
-  if (!make_map_2d(&mA1, x_perm, d.H, nK, BK, BM) ||
-      !make_map_3d(&mB1, w13, 2ull * d.I, d.H, d.E, 64, BK) ||
-      !make_map_2d(&mA2, h, d.I, nK, BK, BM) ||
-      !make_map_3d(&mB2, w2, d.H, d.I, d.E, 64, BK))
+  CUtensorMap mA, mB;
+  if (!make_map_2d(&mA, x_perm, d.H, nK, BK, BM) ||
+      !make_map_3d(&mB, w13, 2ull * d.I, d.H, d.E, 64, BK))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_attr<1>();
   if (e != cudaSuccess) return e;
-  e = set_smem_attr<2>();
-  if (e != cudaSuccess) return e;
-  int grid = device_sm_count() - (sm_reserve > 0 ? sm_reserve : 0);
-  if (grid < 1) grid = 1;
-  grouped_gemm_tc_kernel<1><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(
-      mA1, mB1, offsets, d.E, (int)nK, d.H, d.I, d.I, reinterpret_cast<__nv_bfloat16 *>(h),
+  grouped_gemm_tc_kernel<1><<<gemm_grid(sm_reserve), NUM_THREADS, SMEM_BYTES, s>>>(
+      mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I, reinterpret_cast<__nv_bfloat16 *>(h),
       status);
-  e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const int32_t *offsets,
+                            void *y_perm, int sm_reserve, int32_t *status, cudaStream_t s) {
+  const long long nK = d.nK();
+  if (nK == 0) return cudaSuccess;
+  CUtensorMap mA, mB;
+  if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !make_map_3d(&mB, w2, d.H, d.I, d.E, 64, BK))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr<2>();
   if (e != cudaSuccess) return e;
-  grouped_gemm_tc_kernel<2><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(
-      mA2, mB2, offsets, d.E, (int)nK, d.I, d.I, d.H, reinterpret_cast<__nv_bfloat16 *>(y_perm),
+  grouped_gemm_tc_kernel<2><<<gemm_grid(sm_reserve), NUM_THREADS, SMEM_BYTES, s>>>(
+      mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H, reinterpret_cast<__nv_bfloat16 *>(y_perm),
       status);
   return cudaGetLastError();
 }

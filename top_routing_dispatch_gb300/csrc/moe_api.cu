@@ -186,11 +186,40 @@ moe_status_t moe_grouped_swiglu(const moe_layer_desc_t *desc, const void *x_perm
       !aligned16(y_perm))
     return MOE_ERR_INVALID_ARG;
   if (sm_reserve < 0) return MOE_ERR_INVALID_ARG;
-  cudaError_t e = d.bf16 ? launch_grouped_swiglu_tc(d, x_perm, w13, w2, offsets, h, y_perm,
-                                                    sm_reserve, status_word, stream)
-                         : launch_grouped_swiglu_simt(d, x_perm, w13, w2, offsets, h, y_perm,
-                                                      sm_reserve, status_word, stream);
-  return cuda_status(e);
+  return cuda_status(
+      launch_experts(d, x_perm, w13, w2, offsets, h, y_perm, sm_reserve, status_word, stream));
+}
+
+moe_status_t moe_expert_gemm1_swiglu(const moe_layer_desc_t *desc, const void *x_perm,
+                                     const void *w13, const int32_t *offsets, void *h,
+                                     int sm_reserve, int32_t *status_word, moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  st = check_gemm_shape(d);
+  if (st != MOE_OK) return st;
+  if (d.nK() == 0) return MOE_OK;
+  if (!x_perm || !w13 || !offsets || !h || sm_reserve < 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w13) || !aligned16(h)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(d.bf16 ? launch_gemm1_tc(d, x_perm, w13, offsets, h, sm_reserve,
+                                              status_word, stream)
+                            : launch_gemm1_simt(d, x_perm, w13, offsets, h, status_word, stream));
+}
+
+moe_status_t moe_expert_gemm2(const moe_layer_desc_t *desc, const void *h, const void *w2,
+                              const int32_t *offsets, void *y_perm, int sm_reserve,
+                              int32_t *status_word, moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  st = check_gemm_shape(d);
+  if (st != MOE_OK) return st;
+  if (d.nK() == 0) return MOE_OK;
+  if (!h || !w2 || !offsets || !y_perm || sm_reserve < 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w2) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(d.bf16 ? launch_gemm2_tc(d, h, w2, offsets, y_perm, sm_reserve, status_word,
+                                              stream)
+                            : launch_gemm2_simt(d, h, w2, offsets, y_perm, status_word, stream));
 }
 
 moe_status_t moe_combine(const moe_layer_desc_t *desc, const void *y_perm, const float *topk_w,
@@ -259,14 +288,9 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
                           slot_ptr(d, ws, j, S_X_PERM), status, s);
   };
   auto experts = [&](int j, cudaStream_t s) -> cudaError_t {
-    const int32_t *off = (const int32_t *)slot_ptr(d, ws, j, S_OFFSETS);
-    return d.bf16 ? launch_grouped_swiglu_tc(d, slot_ptr(d, ws, j, S_X_PERM), w13, w2, off,
-                                             slot_ptr(d, ws, j, S_H),
-                                             slot_ptr(d, ws, j, S_Y_PERM), two ? sm_reserve : 0,
-                                             status, s)
-                  : launch_grouped_swiglu_simt(d, slot_ptr(d, ws, j, S_X_PERM), w13, w2, off,
-                                               slot_ptr(d, ws, j, S_H),
-                                               slot_ptr(d, ws, j, S_Y_PERM), 0, status, s);
+    return launch_experts(d, slot_ptr(d, ws, j, S_X_PERM), w13, w2,
+                          (const int32_t *)slot_ptr(d, ws, j, S_OFFSETS), slot_ptr(d, ws, j, S_H),
+                          slot_ptr(d, ws, j, S_Y_PERM), two ? sm_reserve : 0, status, s);
   };
   auto back = [&](int j, cudaStream_t s) -> cudaError_t {
     return launch_combine(d, slot_ptr(d, ws, j, S_Y_PERM),
