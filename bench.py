@@ -1,0 +1,510 @@
+#!/usr/bin/env python
+"""Benchmark of the single-GPU MoE expert layer (router, TopK, dispatch layout,
+permute, grouped SwiGLU GEMMs, combine) on the OLMoE-shaped workload
+(n=4096 tokens, H=2048, I=1024, E=64, K=8, bf16), plus the two-micro-batch
+two-stream schedule.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  A step is one pass of the whole layer over
+one batch of synthetic tokens resident in HBM; `value` is tokens/s over all
+ranks (each rank runs its own batch: weak scaling, no collective on the data
+path).  L2 is flushed (a 256 MiB write) before every timed step, outside the
+timed events.  --impl reference times the fp64 CPU oracle on a bounded token
+sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s and grouped-GEMM TFLOP/s (% BF16 peak), permute/combine GB/s"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 256 << 20          # > 129 MB L2
+# kernels of the library launched by one layer step (single stream):
+# router 2 (logits GEMM, softmax/TopK) + layout 3 (count, scan, scatter)
+# + permute 1 + GEMM1 1 + GEMM2 1 + combine 1
+KERNELS_PER_STEP = 9
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="olmoe_bf16")
+    ap.add_argument("--cpu-sample", type=int, default=512,
+                    help="tokens of the workload the CPU oracle runs per measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-domino", action="store_true")
+    a = ap.parse_args()
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), util=float(parts[4]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        load = [r for r in rows if r["util"] > 0] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(load)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------ CPU oracle arm
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def time_oracle(cfg, x_rows, w_gate, bias, w13, w2, reps=1):
+    """Wall seconds of the fp64 oracle on the given token rows (host arrays;
+    weights as float32 host arrays, upcast per expert inside the oracle)."""
+    from oracle import moe_oracle as O
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        O.moe_forward(x_rows, w_gate, bias, lambda e: w13[e], lambda e: w2[e], cfg.K,
+                      cfg.norm_topk_prob)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def host_inputs_from_device(L, x, rows):
+    import torch
+    ri = torch.as_tensor(rows, device=x.device)
+    f32 = lambda t: None if t is None else t.detach().to("cpu", torch.float32).numpy()
+    return (f32(x[ri]), f32(L["w_gate"]), f32(L["bias"]), f32(L["w13"]), f32(L["w2"]))
+
+
+def cpu_baseline(cfg, L, x, sample):
+    rows = list(range(min(sample, cfg.n)))
+    xs, wg, b, w13, w2 = host_inputs_from_device(L, x, rows)
+    t = time_oracle(cfg, xs, wg, b, w13, w2, reps=1)[0]
+    return {"value": len(rows) / t, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "sample": f"first {len(rows)} of the {cfg.n} tokens of the {cfg.name} workload "
+                      f"(all {cfg.E} experts' weights), fp64 numpy, {t:.2f} s wall"}
+
+
+def run_reference(args, cfg):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    from workloads import synth
+    L = synth.make_layer(cfg, "cpu")
+    x = synth.make_x(cfg, "cpu")
+    rows = list(range(min(args.cpu_sample, cfg.n)))
+    xs, wg, b, w13, w2 = host_inputs_from_device(L, x, rows)
+    del L, x
+    for _ in range(args.warmup):
+        time_oracle(cfg, xs, wg, b, w13, w2)
+    times = time_oracle(cfg, xs, wg, b, w13, w2, reps=args.steps)
+    tot = sum(times)
+    value = len(rows) * args.steps / tot
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * tot / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(cfg, sample=len(rows)),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": f"each step: the first {len(rows)} tokens of the "
+                                   f"{cfg.name} workload, fp64 numpy oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def workload_config(cfg, **extra):
+    d = {"workload": f"{cfg.name}: MoE expert layer n={cfg.n} H={cfg.H} I={cfg.I} E={cfg.E} "
+                     f"K={cfg.K} {cfg.dtype} norm_topk_prob={cfg.norm_topk_prob}",
+         "n": cfg.n, "H": cfg.H, "I": cfg.I, "E": cfg.E, "K": cfg.K,
+         "l2": "flushed (256 MiB write) before every timed step"}
+    d.update(extra)
+    return d
+
+
+# ------------------------------------------------------------ GPU arm
+def algorithmic(cfg, counts=None):
+    """Algorithmic FLOPs and bytes per phase for one micro-batch (the figures
+    the design notes define; weights of empty experts are not counted)."""
+    n, H, I, E, K = cfg.n, cfg.H, cfg.I, cfg.E, cfg.K
+    nK, b = n * K, (2 if cfg.dtype == "bf16" else 4)
+    used = E if counts is None else int(sum(1 for c in counts if c > 0))
+    return {
+        "router": {"flop": 2 * n * H * E, "bytes": n * H * b + H * E * b + 2 * n * E * 4 + 2 * nK * 4},
+        "layout": {"flop": 0, "bytes": 2 * nK * 4 + 2 * nK * 4 + (2 * E + 1) * 4},
+        "permute": {"flop": 0, "bytes": n * H * b + nK * H * b + nK * 4},
+        "gemm1": {"flop": 4 * nK * H * I, "bytes": nK * H * b + used * H * 2 * I * b + nK * I * b},
+        "gemm2": {"flop": 2 * nK * I * H, "bytes": nK * I * b + used * I * H * b + nK * H * b},
+        "combine": {"flop": 2 * nK * H, "bytes": nK * H * b + n * H * b + 2 * nK * 4},
+    }
+
+
+def source_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["top_routing_dispatch_gb300/csrc/gemm_tc.cu",
+                "top_routing_dispatch_gb300/csrc/ptx.cuh"]
+
+
+def recorded_traffic(profile, sources):
+    """DRAM bytes per launch recorded in a profiles/ summary, if it was taken
+    on the current source of the kernel; else None."""
+    p = os.path.join(ROOT, "profiles", profile)
+    try:
+        txt = open(p).read()
+    except OSError:
+        return None
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+    if not m or not s or s.group(1) != source_sha(sources):
+        return None
+    return float(m.group(1))
+
+
+class Timer:
+    """CUDA-event timing on one stream, with an L2 flush and a short device
+    sleep before every measured call so the host enqueues the whole call
+    before the device reaches it (no host gaps inside the measurement)."""
+
+    def __init__(self, torch, stream, dev):
+        self.torch = torch
+        self.stream = stream
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def prep(self):
+        with self.torch.cuda.stream(self.stream):
+            self.flush.zero_()
+            self.torch.cuda._sleep(300_000)
+
+    def event(self):
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record(self.stream)
+        return e
+
+    def measure(self, fn, reps):
+        ts = []
+        for _ in range(reps):
+            self.prep()
+            e0 = self.event()
+            fn()
+            e1 = self.event()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return ts
+
+
+def run_ours(args, cfg):
+    import torch
+    import top_routing_dispatch_gb300 as M
+    from workloads import DOMINO, synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    peaks, peak_src = load_peaks()
+
+    L = synth.make_layer(cfg, dev)
+    x = synth.make_x(cfg, dev, seed=cfg.seed if rank == 0 else cfg.seed + 1000 * rank)
+    desc = M.desc_for(cfg)
+    layer = M.MoELayer(desc, L["w_gate"], L["bias"], L["w13"], L["w2"])
+    v = {k: layer.view(k) for k in ("logits", "topk_idx", "topk_w", "counts", "offsets", "perm",
+                                    "inv_perm", "x_perm", "h", "y_perm")}
+    lws = torch.empty(max(M.moe_layout_workspace_size(desc), 1), dtype=torch.uint8, device=dev)
+    st = layer.status
+    y = torch.empty_like(x)
+    stream = torch.cuda.Stream(device=dev)
+    phases = [
+        ("router", lambda: M.moe_route_topk(desc, x, L["w_gate"], L["bias"], v["topk_idx"],
+                                            v["topk_w"], v["logits"], stream)),
+        ("layout", lambda: M.moe_dispatch_layout(desc, v["topk_idx"], v["counts"], v["offsets"],
+                                                 v["perm"], v["inv_perm"], st, lws, stream)),
+        ("permute", lambda: M.moe_permute(desc, x, v["perm"], v["x_perm"], st, stream)),
+        ("gemm1", lambda: M.moe_expert_gemm1_swiglu(desc, v["x_perm"], L["w13"], v["offsets"],
+                                                    v["h"], 0, st, stream)),
+        ("gemm2", lambda: M.moe_expert_gemm2(desc, v["h"], L["w2"], v["offsets"], v["y_perm"], 0,
+                                             st, stream)),
+        ("combine", lambda: M.moe_combine(desc, v["y_perm"], v["topk_w"], v["inv_perm"], y, st,
+                                          stream)),
+    ]
+    T = Timer(torch, stream, dev)
+
+    def phased_step():
+        T.prep()
+        evs = [T.event()]
+        for _, fn in phases:
+            fn()
+            evs.append(T.event())
+        return evs
+
+    for _ in range(args.warmup):
+        phased_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    steps = [phased_step() for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    per_phase = {name: [s[i].elapsed_time(s[i + 1]) for s in steps]
+                 for i, (name, _) in enumerate(phases)}
+    step_ms = [s[0].elapsed_time(s[-1]) for s in steps]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = M.moe_check_status(st, stream)
+
+    # the same layer through the single forward call (cross-check of the step)
+    api_ms = T.measure(lambda: layer.forward([x], [y], compute=stream), max(3, args.steps // 2))
+
+    # end to end through the public API with host buffers (pinned)
+    x_h = x.cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    x_d = torch.empty_like(x)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            x_d.copy_(x_h, non_blocking=True)
+            layer.forward([x_d], [y], compute=stream)
+            y_h.copy_(y, non_blocking=True)
+    for _ in range(2):
+        T.measure(e2e_step, 1)
+    e2e_ms = T.measure(e2e_step, args.steps)
+    if dist:
+        t = torch.tensor([sum(e2e_ms)], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    else:
+        e2e_total = sum(e2e_ms)
+
+    counts = v["counts"].cpu().tolist()
+    alg = algorithmic(cfg, counts)
+    kernels = {}
+    for name, ts in per_phase.items():
+        ms = statistics.mean(ts)
+        a = alg[name]
+        k = {"ms": ms, "gbs": a["bytes"] / (ms * 1e-3) / 1e9}
+        k["frac_hbm"] = k["gbs"] / peaks["hbm_gbs"]
+        if a["flop"]:
+            k["tflops"] = a["flop"] / (ms * 1e-3) / 1e12
+        if name.startswith("gemm"):
+            k["frac_bf16"] = k["tflops"] / peaks["bf16_tflops"]
+        kernels[name] = k
+    g1 = kernels["gemm1"]
+    roofline = {"bound": "tensor", "kernel": "grouped_gemm_tc_kernel<1> (GEMM1 + SwiGLU)",
+                "achieved": g1["tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": g1["tflops"] / peaks["bf16_tflops"],
+                "peak_source": f"{peak_src} bf16 burst" + (" (of measured)" if peak_src ==
+                                                            "measured" else " (of fallback)"),
+                "traffic": recorded_traffic("gemm1_olmoe_bf16.md", GEMM_SOURCES),
+                "algorithmic_flop_per_launch": alg["gemm1"]["flop"],
+                "algorithmic_bytes_per_launch": alg["gemm1"]["bytes"]}
+
+    out = {
+        "metric": METRIC, "value": world * cfg.n * args.steps / (total_ms * 1e-3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded Gaussian inputs and weights, random init)",
+        "config": workload_config(cfg, parallelism=f"replicas x{world} (one batch per GPU)",
+                                  step="router -> layout -> permute -> GEMM1+SwiGLU -> GEMM2 -> "
+                                       "combine, one C-ABI call each, one stream"),
+        "roofline": roofline,
+        "kernels": kernels,
+        "api_forward_ms_per_step": statistics.median(api_ms),
+        "e2e": {"value": world * cfg.n * args.steps / (e2e_total * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
+                "d2h_bytes_per_step": y_h.numel() * y_h.element_size()},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+        "device_status": status,
+        "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,
+    }
+    if not args.no_domino:
+        out["domino"] = domino(args, torch, M, synth, DOMINO, dev, peaks)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg, L, x, args.cpu_sample)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def domino(args, torch, M, synth, cfg, dev, peaks):
+    """Two micro-batches on two streams: the four controls of the overlap
+    check (compute only, dispatch+combine only, serial, overlapped) and the
+    hide ratio, strict and over the overlap-eligible phases."""
+    L = synth.make_layer(cfg, dev)
+    xs = synth.make_micro_batches(cfg, dev)
+    desc = M.desc_for(cfg)
+    layer = M.MoELayer(desc, L["w_gate"], L["bias"], L["w13"], L["w2"], num_mb=2)
+    ys = [torch.empty_like(x) for x in xs]
+    sc, sd = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    T = Timer(torch, sc, dev)
+    st = layer.status
+    V = [{k: layer.view(k, j) for k in ("logits", "topk_idx", "topk_w", "counts", "offsets",
+                                         "perm", "inv_perm", "x_perm", "h", "y_perm")}
+         for j in range(2)]
+    lws = [torch.empty(max(M.moe_layout_workspace_size(desc), 1), dtype=torch.uint8,
+                       device=dev) for _ in range(2)]
+
+    def front(j):
+        v = V[j]
+        M.moe_route_topk(desc, xs[j], L["w_gate"], L["bias"], v["topk_idx"], v["topk_w"],
+                         v["logits"], sc)
+        M.moe_dispatch_layout(desc, v["topk_idx"], v["counts"], v["offsets"], v["perm"],
+                              v["inv_perm"], st, lws[j], sc)
+        M.moe_permute(desc, xs[j], v["perm"], v["x_perm"], st, sc)
+
+    def gemms(j):
+        v = V[j]
+        M.moe_expert_gemm1_swiglu(desc, v["x_perm"], L["w13"], v["offsets"], v["h"], 0, st, sc)
+        M.moe_expert_gemm2(desc, v["h"], L["w2"], v["offsets"], v["y_perm"], 0, st, sc)
+
+    def back(j):
+        v = V[j]
+        M.moe_combine(desc, v["y_perm"], v["topk_w"], v["inv_perm"], ys[j], st, sc)
+
+    R = max(5, args.steps)
+    med = lambda fn: statistics.median(T.measure(fn, R))
+    layer.forward(xs, ys, compute=sc)
+    torch.cuda.synchronize()
+    ref = [y.clone() for y in ys]
+    t_a = med(lambda: (gemms(0), gemms(1)))
+    t_b = med(lambda: (front(0), front(1), back(0), back(1)))
+    t_edge = med(lambda: (front(0), back(1)))
+    t_elig = med(lambda: (front(1), back(0)))
+    t_c = med(lambda: layer.forward(xs, ys, compute=sc))
+    sweep = {}
+    for s in (0, 8, 16, 24, 32):
+        sweep[s] = med(lambda: layer.forward(xs, ys, sm_reserve=s, compute=sc, dispatch=sd))
+    best = min(sweep, key=sweep.get)
+    t_d = sweep[best]
+    layer.forward(xs, ys, sm_reserve=best, compute=sc, dispatch=sd)
+    torch.cuda.synchronize()
+    bitwise = all(torch.equal(a, b) for a, b in zip(ys, ref))
+    return {
+        "workload": f"{cfg.name}: 2 x n={cfg.n}, seeds {list(cfg.mb_seeds)}",
+        "ms_compute_only_A": t_a, "ms_dispatch_combine_only_B": t_b,
+        "ms_serial_C": t_c, "ms_overlapped_D": t_d, "sm_reserve_best": best,
+        "ms_overlapped_by_sm_reserve": sweep,
+        "ms_edge_phases": t_edge, "ms_eligible_phases": t_elig,
+        "hide_ratio_strict": 1.0 - (t_d - t_a) / t_b,
+        "hide_ratio_eligible": 1.0 - (t_d - t_a - t_edge) / t_elig,
+        "speedup_D_vs_C": t_c / t_d,
+        "tokens_per_s_overlapped": 2 * cfg.n / (t_d * 1e-3),
+        "bitwise_equal_to_single_stream": bitwise,
+    }
+
+
+def main():
+    args = parse_args()
+    from workloads import BY_NAME
+    cfg = BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
