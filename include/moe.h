@@ -129,6 +129,31 @@ moe_status_t moe_dispatch_layout(const moe_layer_desc_t *desc, const int32_t *to
                                  size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_dispatch_layout without a workspace argument: the same layout, computed
+ * by the same kernels, for callers that cannot allocate device memory when
+ * they run (a pre-planned memory pool with nothing left over, or a context in
+ * which a cudaMalloc would stall the device or is not allowed).  There is no
+ * counterpart of this call in the pages; it exists only for such callers.
+ *   - Scratch: a fixed device array owned by the library (512 KiB + 4 KiB per
+ *     GPU that loads the library, kept until the process exits).  The call
+ *     itself allocates nothing.
+ *   - Limit: n*K <= MOE_NOALLOC_MAX_PAIRS (and E <= 256 as everywhere);
+ *     larger layouts return MOE_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (a
+ *     cudaGetSymbolAddress, with that device current); make that first call
+ *     before capturing a stream.
+ *   - All calls on a device share the array.  Calls must not overlap on the
+ *     GPU: two of them running at once (e.g. on unordered streams) race on the
+ *     scratch and give wrong layouts.  Calls ordered on one stream are safe.
+ * Other arguments, results and errors are those of moe_dispatch_layout.
+ */
+#define MOE_NOALLOC_MAX_PAIRS 524288
+moe_status_t moe_dispatch_layout_noalloc(const moe_layer_desc_t *desc, const int32_t *topk_idx,
+                                         int32_t *counts, int32_t *offsets, int32_t *perm,
+                                         int32_t *inv_perm, int32_t *status_word,
+                                         moe_stream_t stream);
+
+/*
  * Permute (the gather of Algorithm 2 step 7 for all experts at once):
  * x_perm[r] = x[perm[r] / K].  x (n,H), x_perm (n*K,H), perm (n*K).
  * A perm entry outside [0, n*K) gives a zero row and sets MOE_DEV_BAD_LAYOUT

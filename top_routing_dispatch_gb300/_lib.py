@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
 # C ABI symbols, in header order (tests check the library exports each one).
 SYMBOLS = (
     "moe_version", "moe_status_string", "moe_route_topk", "moe_layout_workspace_size",
-    "moe_dispatch_layout", "moe_permute", "moe_grouped_swiglu", "moe_expert_gemm1_swiglu",
+    "moe_dispatch_layout", "moe_dispatch_layout_noalloc", "moe_permute", "moe_grouped_swiglu", "moe_expert_gemm1_swiglu",
     "moe_expert_gemm2", "moe_combine",
     "moe_workspace_size", "moe_forward_microbatches", "moe_workspace_slot", "moe_check_status",
 )
@@ -24,6 +24,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
           4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT",
           7: "MOE_ERR_BAD_LAYOUT"}
 DEV_BAD_ROUTING, DEV_BAD_LAYOUT, DEV_TIMEOUT = 0x1, 0x2, 0x4
+NOALLOC_MAX_PAIRS = 524288  # MOE_NOALLOC_MAX_PAIRS
 
 # workspace slots of moe_workspace_slot
 SLOT = dict(logits=0, topk_idx=1, topk_w=2, counts=3, offsets=4, perm=5, inv_perm=6,
@@ -49,6 +50,7 @@ def _declare(lib):
         "moe_layout_workspace_size": (ctypes.c_size_t, [_desc_p]),
         "moe_dispatch_layout": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                       ctypes.c_size_t, _vp]),
+        "moe_dispatch_layout_noalloc": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
         "moe_permute": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp]),
         "moe_grouped_swiglu": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                      _vp, _vp]),

@@ -80,6 +80,16 @@ def moe_dispatch_layout(desc, topk_idx, counts, offsets, perm, inv_perm, status_
            "moe_dispatch_layout")
 
 
+def moe_dispatch_layout_noalloc(desc, topk_idx, counts, offsets, perm, inv_perm, status_word,
+                                stream=None):
+    """moe_dispatch_layout using the library's own fixed scratch array (for
+    callers that cannot allocate device memory when they run)."""
+    _check(_lib.load().moe_dispatch_layout_noalloc(ctypes.byref(desc), _p(topk_idx), _p(counts),
+                                                   _p(offsets), _p(perm), _p(inv_perm),
+                                                   _p(status_word), _stream(stream)),
+           "moe_dispatch_layout_noalloc")
+
+
 def moe_permute(desc, x, perm, x_perm, status_word=None, stream=None):
     _check(_lib.load().moe_permute(ctypes.byref(desc), _p(x), _p(perm), _p(x_perm),
                                    _p(status_word), _stream(stream)), "moe_permute")

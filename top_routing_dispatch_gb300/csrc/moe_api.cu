@@ -356,3 +356,68 @@ moe_status_t moe_check_status(const int32_t *status_word, moe_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Dispatch layout without caller-provided scratch.
+//
+// For callers that cannot allocate device memory at call time -- for example
+// a runtime whose memory is fully pre-planned, or code running where a
+// cudaMalloc would synchronise the device or is simply not permitted -- the
+// layout's scratch (per-chunk histograms and chunk start positions) lives in a
+// fixed array that belongs to the library.  The array is a device global of
+// this file: every GPU that loads the library holds it (512 KiB + 4 KiB) until
+// the process exits.  It is shared by every call on a device and keeps what
+// the previous call left in it; the layout kernels overwrite every entry they
+// read, so nothing needs clearing.  Two calls whose work overlaps on the GPU
+// (on different streams without ordering) would use the same array at the same
+// time and produce wrong results: order such calls on one stream.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+constexpr int kNoAllocMaxChunks = 256;  // chunks of 2048 (token, slot) pairs
+constexpr size_t kNoAllocScratchInts = 2ull * kNoAllocMaxChunks * (kMaxE + 1);
+
+static __device__ __align__(256) int32_t g_layout_scratch[kNoAllocScratchInts];
+
+// Device address of g_layout_scratch per device, looked up once per device.
+void *g_scratch_addr[64] = {nullptr};
+std::mutex g_scratch_mu;
+
+cudaError_t layout_scratch_address(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_layout_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_dispatch_layout_noalloc(const moe_layer_desc_t *desc,
+                                                    const int32_t *topk_idx, int32_t *counts,
+                                                    int32_t *offsets, int32_t *perm,
+                                                    int32_t *inv_perm, int32_t *status_word,
+                                                    moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  if (!counts || !offsets || !status_word) return MOE_ERR_INVALID_ARG;
+  if (d.nK() > 0 && (!topk_idx || !perm || !inv_perm)) return MOE_ERR_INVALID_ARG;
+  if (d.nK() > (long long)MOE_NOALLOC_MAX_PAIRS ||
+      layout_ws_bytes(d) > kNoAllocScratchInts * sizeof(int32_t))
+    return MOE_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  if (layout_scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(
+      launch_layout(d, topk_idx, counts, offsets, perm, inv_perm, status_word, scratch, stream));
+}
