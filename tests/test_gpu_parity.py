@@ -27,6 +27,11 @@ SMALL = [
               norm_topk_prob=True, seed=24),
     MoEConfig("one_token_bf16", n=1, H=128, I=128, E=8, K=2, dtype="bf16",
               norm_topk_prob=True, seed=25),
+    # tensor-core router path (E % 64 == 0): ragged tail tile, bias with -inf experts
+    MoEConfig("ragged_e64_skew_bf16", n=333, H=256, I=128, E=64, K=6, dtype="bf16",
+              norm_topk_prob=True, seed=26, skew=True),
+    MoEConfig("e128_k3_bf16", n=700, H=320, I=256, E=128, K=3, dtype="bf16",
+              norm_topk_prob=False, seed=27),
 ]
 FULL = [OLMOE, SKEW, DSV3]
 
@@ -43,12 +48,15 @@ def check_router(run, rows=None):
     assert np.array_equal(gi[ok], oe[ok]), "TopK indices differ on non-near-tie tokens"
     for t in np.where(near)[0]:
         assert valid_near_tie_choice(lo[t], gi[t], cfg.K), f"token {t}: invalid near-tie choice"
-    rel = np.abs(gw[ok] - ow[ok]) / np.maximum(np.abs(ow[ok]), 1e-30)
-    assert rel.max(initial=0) <= 1e-5, rel.max()
     fin = np.isfinite(lo)
     err = np.abs(lg[fin] - lo[fin]).max(initial=0)
-    # float32 logits: far inside the near-tie rescoring margin (1e-3 * max(1, |l|))
+    # float32 logits: well inside half the near-tie rescoring margin
+    # (tau = 1e-3 * max(1, |l|)), so every non-near-tie choice is decided right
     assert err < 2.5e-4, err
+    # softmax weights move by at most ~2x the largest logit error (relative),
+    # plus float32 rounding of exp and the divisions
+    rel = np.abs(gw[ok] - ow[ok]) / np.maximum(np.abs(ow[ok]), 1e-30)
+    assert rel.max(initial=0) <= 2.0 * err + 2e-6, (rel.max(), err)
     return err, int(near.sum())
 
 
@@ -165,3 +173,48 @@ def test_skew_workload_is_skewed():
     cv = O.count_cv(counts)
     assert 1.35 <= cv <= 1.65, cv
     assert int((counts == 0).sum()) == 4
+
+
+@pytest.mark.parametrize("E,K", [(64, 8), (256, 8), (16, 4)])
+def test_router_constructed_ties(E, K):
+    """Exact ties (duplicated W_gate columns) and near ties (columns one bf16
+    step apart) on large-scored experts: the GPU must order them as the exact
+    evaluation does, except where the oracle itself sees a gap below 1e-6."""
+    import top_routing_dispatch_gb300 as M
+    dev = torch.device("cuda:0")
+    n, H = 1000, 256
+    g = torch.Generator(device="cpu")
+    g.manual_seed(E * 7 + K)
+    x = torch.randn(n, H, generator=g).to(torch.bfloat16)
+    wg = (torch.randn(H, E, generator=g) * 0.02)
+    wg[:, [3, 5, 7, 9, 11]] *= 6.0                 # these experts score high
+    wg[:, 5] = wg[:, 3]                            # exact tie 3 / 5
+    wg = wg.to(torch.bfloat16)
+    col = wg[:, 7].clone()
+    col[::7] = torch.nextafter(col[::7].float(), torch.tensor(10.0)).to(torch.bfloat16)
+    wg[:, 9] = col                                 # near tie 7 / 9 (one step apart in a few k)
+    x, wg = x.to(dev), wg.to(dev)
+    desc = M.make_desc(n, H, 128, E, K, "bf16", True)
+    idx = torch.empty(n, K, dtype=torch.int32, device=dev)
+    w = torch.empty(n, K, dtype=torch.float32, device=dev)
+    logits = torch.empty(n, E, dtype=torch.float32, device=dev)
+    M.moe_route_topk(desc, x, wg, None, idx, w, logits)
+    torch.cuda.synchronize()
+    lo = O.router_logits(f64(x), f64(wg))
+    near = O.near_tie_tokens(lo, K)
+    oe, ow = O.topk(lo, K, True)
+    gi = idx.cpu().numpy()
+    ok = ~near
+    assert ok.sum() > 0
+    assert np.array_equal(gi[ok], oe[ok])
+    for t in np.where(near)[0]:
+        assert valid_near_tie_choice(lo[t], gi[t], K)
+    # exact ties resolve to the lower expert id first, as in the oracle
+    both = np.array([3 in r and 5 in r for r in gi])
+    assert both.any()
+    for r in gi[both]:
+        assert list(r).index(3) < list(r).index(5)
+    err = np.abs(logits.cpu().numpy() - lo).max()
+    assert err < 2.5e-4
+    rel = np.abs(w.cpu().numpy()[ok] - ow[ok]) / ow[ok]
+    assert rel.max() <= 2.0 * err + 2e-6

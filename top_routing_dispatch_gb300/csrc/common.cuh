@@ -21,9 +21,14 @@ struct Desc {
 
 inline size_t elem_bytes(const Desc &d) { return d.bf16 ? 2 : 4; }
 
-// ---- router.cu
+// ---- router.cu (dispatches to router_tc.cu for bf16 layers with E % 64 == 0)
 cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, const float *bias,
-                          int32_t *topk_idx, float *topk_w, float *logits, cudaStream_t s);
+                          int32_t *topk_idx, float *topk_w, float *logits, int32_t *status,
+                          cudaStream_t s);
+bool router_tc_supported(const Desc &d);
+cudaError_t launch_router_tc(const Desc &d, const void *x, const void *w_gate, const float *bias,
+                             int32_t *topk_idx, float *topk_w, float *logits, int32_t *status,
+                             cudaStream_t s);
 
 // ---- layout.cu
 size_t layout_ws_bytes(const Desc &d);

@@ -138,7 +138,9 @@ moe_status_t moe_route_topk(const moe_layer_desc_t *desc, const void *x, const v
   if (st != MOE_OK) return st;
   if (d.n == 0) return MOE_OK;
   if (!x || !w_gate || !topk_idx || !topk_w || !logits) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_router(d, x, w_gate, bias, topk_idx, topk_w, logits, stream));
+  if (!aligned16(x) || !aligned16(w_gate) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_router(d, x, w_gate, bias, topk_idx, topk_w, logits, nullptr, stream));
 }
 
 size_t moe_layout_workspace_size(const moe_layer_desc_t *desc) {
@@ -276,7 +278,7 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
     int32_t *idx = (int32_t *)slot_ptr(d, ws, j, S_TOPK_IDX);
     cudaError_t e = launch_router(d, x[j], w_gate, bias, idx,
                                   (float *)slot_ptr(d, ws, j, S_TOPK_W),
-                                  (float *)slot_ptr(d, ws, j, S_LOGITS), s);
+                                  (float *)slot_ptr(d, ws, j, S_LOGITS), status, s);
     if (e != cudaSuccess) return e;
     e = launch_layout(d, idx, (int32_t *)slot_ptr(d, ws, j, S_COUNTS),
                       (int32_t *)slot_ptr(d, ws, j, S_OFFSETS),

@@ -2,7 +2,9 @@
 // renormalisation.  "MoE 分布式推理基础（基于 vLLM）" §1.2, Algorithm 2 steps
 // 1-3 and the router's norm_topk_prob branch.
 //
-// Two kernels:
+// bf16 layers with E % 64 == 0 use router_tc.cu (tensor-core logits with the
+// softmax/TopK fused into the epilogue) followed by router_topk_kernel in its
+// flagged-only mode.  Other layers use two kernels:
 //  1. router_logits_kernel: SIMT tiled GEMM (n x H)·(H x E) with float32
 //     accumulation in per-tile partial sums (32 products per partial, then
 //     added to the running sum), bias added last.  Products of bf16 inputs are
@@ -132,17 +134,23 @@ __device__ __forceinline__ void warp_argmax(float &v, int &e) {
 
 constexpr int TOPK_WARPS = 8;
 
+constexpr int RG = 8;  // candidates rescored per pass over H
+
+// only_flagged: finish only the tokens the tensor-core router flagged as
+// near ties (topk_idx[t*K] < 0); other tokens are left as they are.
 template <int EPL, bool BF16>
 __global__ void __launch_bounds__(TOPK_WARPS * 32) router_topk_kernel(
     const float *__restrict__ logits, const void *__restrict__ x, const void *__restrict__ wg,
     const float *__restrict__ bias, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
-    int n, int H, int E, int K, int norm) {
+    int n, int H, int E, int K, int norm, int only_flagged) {
   __shared__ float s_hi[TOPK_WARPS][kMaxK];
   __shared__ float s_lo[TOPK_WARPS][kMaxK];
   __shared__ int s_e[TOPK_WARPS][kMaxK];
+  __shared__ int s_cand[TOPK_WARPS][kMaxE];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int t = blockIdx.x * TOPK_WARPS + wib;
   if (t >= n) return;
+  if (only_flagged && topk_idx[(size_t)t * K] >= 0) return;
   const float NEG = -INFINITY;
   float v[EPL];
 #pragma unroll
@@ -201,34 +209,54 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) router_topk_kernel(
     for (int r = 0; r < kMaxK; ++r)
       if (r == K - 1) vK = top_v[r];
     const float thr = vK - tau;
-    int cnt = 0;  // entries in the per-warp sorted list (uniform)
+    // candidates, in ascending expert id: every expert that can still be in
+    // the top K given the float32 error (< tau/2)
+    int C = 0;
+#pragma unroll
     for (int j = 0; j < EPL; ++j) {
-      const int e_l = lane + 32 * j;
-      unsigned ball = __ballot_sync(0xffffffffu, e_l < E && v[j] >= thr);
-      while (ball) {
-        const int b = __ffs(ball) - 1;
-        ball &= ball - 1;
-        const int e = b + 32 * j;
-        DF acc{0.f, 0.f};
-        for (int hh = lane; hh < H; hh += 32)
-          acc = df_add(acc, two_prod(ld_in<BF16>(x, (size_t)t * H + hh),
-                                     ld_in<BF16>(wg, (size_t)hh * E + e)));
+      const unsigned ball = __ballot_sync(0xffffffffu, lane + 32 * j < E && v[j] >= thr);
+      if (ball >> lane & 1u) s_cand[wib][C + __popc(ball & ((1u << lane) - 1u))] = lane + 32 * j;
+      C += __popc(ball);
+    }
+    __syncwarp();
+    int cnt = 0;  // entries in the per-warp sorted list (uniform)
+    for (int g0 = 0; g0 < C; g0 += RG) {
+      int ce[RG];
+#pragma unroll
+      for (int c = 0; c < RG; ++c) ce[c] = g0 + c < C ? s_cand[wib][g0 + c] : -1;
+      DF acc[RG];
+#pragma unroll
+      for (int c = 0; c < RG; ++c) acc[c] = DF{0.f, 0.f};
+      // one pass over H for RG candidates: a lane reads x[h] once and the
+      // candidates' weights from the same row of W_gate
+      for (int hh = lane; hh < H; hh += 32) {
+        const float xv = ld_in<BF16>(x, (size_t)t * H + hh);
+        const size_t row = (size_t)hh * E;
+#pragma unroll
+        for (int c = 0; c < RG; ++c)
+          if (ce[c] >= 0) acc[c] = df_add(acc[c], two_prod(xv, ld_in<BF16>(wg, row + ce[c])));
+      }
+#pragma unroll
+      for (int c = 0; c < RG; ++c) {
+        if (ce[c] < 0) break;  // uniform
+        DF a = acc[c];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-          DF other{__shfl_xor_sync(0xffffffffu, acc.hi, o), __shfl_xor_sync(0xffffffffu, acc.lo, o)};
-          acc = df_add(acc, other);
+          DF other{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+          a = df_add(a, other);
         }
+        const int e = ce[c];
         if (bias) {
           const float bb = bias[e];
           if (isinf(bb))
-            acc = DF{bb, 0.f};
+            a = DF{bb, 0.f};
           else
-            acc = df_add(acc, DF{bb, 0.f});
+            a = df_add(a, DF{bb, 0.f});
         }
-        // insert (acc, e) into the warp's sorted list of at most K entries
+        // insert (a, e) into the warp's sorted list of at most K entries
         if (lane == 0) {
           int pos = cnt < K ? cnt : K;
-          while (pos > 0 && df_greater(acc, e, DF{s_hi[wib][pos - 1], s_lo[wib][pos - 1]},
+          while (pos > 0 && df_greater(a, e, DF{s_hi[wib][pos - 1], s_lo[wib][pos - 1]},
                                        s_e[wib][pos - 1]))
             --pos;
           if (pos < K) {
@@ -238,8 +266,8 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) router_topk_kernel(
               s_lo[wib][q] = s_lo[wib][q - 1];
               s_e[wib][q] = s_e[wib][q - 1];
             }
-            s_hi[wib][pos] = acc.hi;
-            s_lo[wib][pos] = acc.lo;
+            s_hi[wib][pos] = a.hi;
+            s_lo[wib][pos] = a.lo;
             s_e[wib][pos] = e;
           }
         }
@@ -280,22 +308,39 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) router_topk_kernel(
 
 template <int EPL>
 cudaError_t launch_topk(const Desc &d, const float *logits, const void *x, const void *wg,
-                        const float *bias, int32_t *idx, float *w, cudaStream_t s) {
+                        const float *bias, int32_t *idx, float *w, int only_flagged,
+                        cudaStream_t s) {
   dim3 grid((d.n + TOPK_WARPS - 1) / TOPK_WARPS);
   if (d.bf16)
-    router_topk_kernel<EPL, true><<<grid, TOPK_WARPS * 32, 0, s>>>(logits, x, wg, bias, idx, w,
-                                                                    d.n, d.H, d.E, d.K, d.norm);
+    router_topk_kernel<EPL, true><<<grid, TOPK_WARPS * 32, 0, s>>>(
+        logits, x, wg, bias, idx, w, d.n, d.H, d.E, d.K, d.norm, only_flagged);
   else
-    router_topk_kernel<EPL, false><<<grid, TOPK_WARPS * 32, 0, s>>>(logits, x, wg, bias, idx, w,
-                                                                     d.n, d.H, d.E, d.K, d.norm);
+    router_topk_kernel<EPL, false><<<grid, TOPK_WARPS * 32, 0, s>>>(
+        logits, x, wg, bias, idx, w, d.n, d.H, d.E, d.K, d.norm, only_flagged);
   return cudaGetLastError();
+}
+
+cudaError_t launch_topk_any(const Desc &d, const float *logits, const void *x, const void *wg,
+                            const float *bias, int32_t *idx, float *w, int only_flagged,
+                            cudaStream_t s) {
+  if (d.E <= 32) return launch_topk<1>(d, logits, x, wg, bias, idx, w, only_flagged, s);
+  if (d.E <= 64) return launch_topk<2>(d, logits, x, wg, bias, idx, w, only_flagged, s);
+  if (d.E <= 128) return launch_topk<4>(d, logits, x, wg, bias, idx, w, only_flagged, s);
+  return launch_topk<8>(d, logits, x, wg, bias, idx, w, only_flagged, s);
 }
 
 }  // namespace
 
 cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, const float *bias,
-                          int32_t *topk_idx, float *topk_w, float *logits, cudaStream_t s) {
+                          int32_t *topk_idx, float *topk_w, float *logits, int32_t *status,
+                          cudaStream_t s) {
   if (d.n == 0) return cudaSuccess;
+  if (router_tc_supported(d)) {
+    // tensor-core logits with fused softmax/TopK, then the flagged near ties
+    cudaError_t e = launch_router_tc(d, x, w_gate, bias, topk_idx, topk_w, logits, status, s);
+    if (e != cudaSuccess) return e;
+    return launch_topk_any(d, logits, x, w_gate, bias, topk_idx, topk_w, 1, s);
+  }
   dim3 grid((d.n + RBM - 1) / RBM, (d.E + RBN - 1) / RBN);
   if (d.bf16)
     router_logits_kernel<true><<<grid, RTHREADS, 0, s>>>(x, w_gate, bias, logits, d.n, d.H, d.E);
@@ -303,10 +348,7 @@ cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, cons
     router_logits_kernel<false><<<grid, RTHREADS, 0, s>>>(x, w_gate, bias, logits, d.n, d.H, d.E);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  if (d.E <= 32) return launch_topk<1>(d, logits, x, w_gate, bias, topk_idx, topk_w, s);
-  if (d.E <= 64) return launch_topk<2>(d, logits, x, w_gate, bias, topk_idx, topk_w, s);
-  if (d.E <= 128) return launch_topk<4>(d, logits, x, w_gate, bias, topk_idx, topk_w, s);
-  return launch_topk<8>(d, logits, x, w_gate, bias, topk_idx, topk_w, s);
+  return launch_topk_any(d, logits, x, w_gate, bias, topk_idx, topk_w, 0, s);
 }
 
 }  // namespace moe
