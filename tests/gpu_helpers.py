@@ -83,3 +83,26 @@ def valid_near_tie_choice(logits_row, chosen, K, gap=NEAR_TIE_GAP):
     vals = logits_row[np.asarray(chosen)]
     return (len(set(chosen)) == K and np.all(vals >= s[K - 1] - gap)
             and np.all(np.diff(vals) <= gap))
+
+
+def tie_margin(cfg):
+    """The router's relative near-tie margin for this layer: tensor-core
+    logits (bf16, E % 64 == 0, K <= 8, K < E) or FMA-unit logits."""
+    tc = cfg.dtype == "bf16" and cfg.E % 64 == 0 and cfg.H % 64 == 0 and 1 <= cfg.K <= 8 \
+        and cfg.K < cfg.E
+    return 1e-4 * max(1.0, cfg.H / 2048.0) if tc else 1e-3
+
+
+def logit_error_within_margin(gpu_logits, oracle_logits, margin):
+    """Per token: the largest float32 logit error is below half the rescoring
+    margin (margin * max(1, |largest logit|)) -- the condition under which a
+    token that is not rescored cannot be ordered differently from the exact
+    logits.  Returns (ok, worst ratio error / half-margin, max abs error)."""
+    lo = np.asarray(oracle_logits)
+    lg = np.asarray(gpu_logits)
+    fin = np.isfinite(lo)
+    err = np.where(fin, np.abs(lg - np.where(fin, lo, 0.0)), 0.0).max(axis=1)
+    top = np.where(fin, lo, -np.inf).max(axis=1)
+    half = 0.5 * margin * np.maximum(1.0, np.abs(top))
+    ratio = err / half
+    return bool(np.all(ratio < 1.0)), float(ratio.max()), float(err.max())

@@ -7,7 +7,8 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from tests.gpu_helpers import Run, TOL, rel_fro, valid_near_tie_choice, f64
+from tests.gpu_helpers import (Run, TOL, rel_fro, valid_near_tie_choice, f64, tie_margin,
+                               logit_error_within_margin)
 from workloads import TINY, OLMOE, SKEW, DSV3
 from workloads.configs import MoEConfig
 
@@ -48,11 +49,11 @@ def check_router(run, rows=None):
     assert np.array_equal(gi[ok], oe[ok]), "TopK indices differ on non-near-tie tokens"
     for t in np.where(near)[0]:
         assert valid_near_tie_choice(lo[t], gi[t], cfg.K), f"token {t}: invalid near-tie choice"
-    fin = np.isfinite(lo)
-    err = np.abs(lg[fin] - lo[fin]).max(initial=0)
-    # float32 logits: well inside half the near-tie rescoring margin
-    # (tau = 1e-3 * max(1, |l|)), so every non-near-tie choice is decided right
-    assert err < 2.5e-4, err
+    # float32 logits: inside half the near-tie rescoring margin for every
+    # token, so every token the kernel did not rescore is ordered right
+    ok_m, ratio, err = logit_error_within_margin(lg, lo, tie_margin(cfg))
+    print(f"{cfg.name}: max logit error {err:.3e}, worst error / half-margin {ratio:.3f}")
+    assert ok_m, (ratio, err)
     # softmax weights move by at most ~2x the largest logit error (relative),
     # plus float32 rounding of exp and the divisions
     rel = np.abs(gw[ok] - ow[ok]) / np.maximum(np.abs(ow[ok]), 1e-30)
@@ -214,7 +215,8 @@ def test_router_constructed_ties(E, K):
     assert both.any()
     for r in gi[both]:
         assert list(r).index(3) < list(r).index(5)
-    err = np.abs(logits.cpu().numpy() - lo).max()
-    assert err < 2.5e-4
+    ok_m, ratio, err = logit_error_within_margin(
+        logits.cpu().numpy(), lo, 1e-4 * max(1.0, H / 2048.0) if E % 64 == 0 else 1e-3)
+    assert ok_m, (ratio, err)
     rel = np.abs(w.cpu().numpy()[ok] - ow[ok]) / ow[ok]
     assert rel.max() <= 2.0 * err + 2e-6

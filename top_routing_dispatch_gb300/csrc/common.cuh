@@ -12,6 +12,22 @@ namespace moe {
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
 
+// Near-tie margins of the router, relative to max(1, |largest logit|).  A
+// token whose top K+1 float32 logits have an adjacent gap below the margin
+// has its candidate experts rescored in double-float.  The margin must stay
+// above twice the largest float32 logit error: for the FMA-unit logits
+// (float32 chains of 32 products) and for the tensor-core logits (float32
+// accumulation in the tensor cores) that error is measured by the GPU parity
+// tests against the float64 oracle.
+constexpr float kTieMarginSimt = 1e-3f;
+constexpr float kTieMarginTc = 1e-4f;  // scaled by max(1, H / 2048): see tie_margin_tc
+
+// The tensor cores' float32 accumulation error grows about linearly with the
+// length of the sum (measured), so their margin scales with H.
+__host__ __device__ inline float tie_margin_tc(int H) {
+  return kTieMarginTc * (H > 2048 ? (float)H / 2048.f : 1.f);
+}
+
 struct Desc {
   int n, H, I, E, K;
   bool bf16;

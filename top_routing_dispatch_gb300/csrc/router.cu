@@ -2,9 +2,9 @@
 // renormalisation.  "MoE 分布式推理基础（基于 vLLM）" §1.2, Algorithm 2 steps
 // 1-3 and the router's norm_topk_prob branch.
 //
-// bf16 layers with E % 64 == 0 use router_tc.cu (tensor-core logits with the
-// softmax/TopK fused into the epilogue) followed by router_topk_kernel in its
-// flagged-only mode.  Other layers use two kernels:
+// bf16 layers with E % 64 == 0 and K <= 8 use router_tc.cu (one kernel:
+// tensor-core logits, softmax, TopK and near-tie rescoring).  Other layers
+// use two kernels:
 //  1. router_logits_kernel: SIMT tiled GEMM (n x H)·(H x E) with float32
 //     accumulation in per-tile partial sums (32 products per partial, then
 //     added to the running sum), bias added last.  Products of bf16 inputs are
@@ -19,6 +19,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "df.cuh"
 
 namespace moe {
 namespace {
@@ -94,31 +95,6 @@ __global__ void __launch_bounds__(RTHREADS) router_logits_kernel(
   }
 }
 
-// ---- double-float helpers (error-free transformations, no FMA contraction)
-struct DF {
-  float hi, lo;
-};
-
-__device__ __forceinline__ DF df_add(DF a, DF b) {
-  const float s = __fadd_rn(a.hi, b.hi);
-  const float bb = __fsub_rn(s, a.hi);
-  float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
-  err = __fadd_rn(err, __fadd_rn(a.lo, b.lo));
-  const float hi = __fadd_rn(s, err);
-  return DF{hi, __fsub_rn(err, __fsub_rn(hi, s))};
-}
-
-__device__ __forceinline__ DF two_prod(float a, float b) {
-  const float p = __fmul_rn(a, b);
-  return DF{p, fmaf(a, b, -p)};
-}
-
-__device__ __forceinline__ bool df_greater(DF a, int ea, DF b, int eb) {
-  if (a.hi != b.hi) return a.hi > b.hi;
-  if (a.lo != b.lo) return a.lo > b.lo;
-  return ea < eb;
-}
-
 // (value, expert) argmax across the warp; ties to the lower expert id.
 __device__ __forceinline__ void warp_argmax(float &v, int &e) {
 #pragma unroll
@@ -135,6 +111,7 @@ __device__ __forceinline__ void warp_argmax(float &v, int &e) {
 constexpr int TOPK_WARPS = 8;
 
 constexpr int RG = 8;  // candidates rescored per pass over H
+constexpr int RU = 4;  // rows of W_gate per lane per step of that pass
 
 // only_flagged: finish only the tokens the tensor-core router flagged as
 // near ties (topk_idx[t*K] < 0); other tokens are left as they are.
@@ -195,7 +172,7 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) router_topk_kernel(
   }
 
   // near-tie check among the top K+1 (finite values only)
-  const float tau = 1e-3f * fmaxf(1.f, fabsf(top_v[0]));
+  const float tau = kTieMarginSimt * fmaxf(1.f, fabsf(top_v[0]));
   bool amb = false;
 #pragma unroll
   for (int r = 0; r + 1 < kMaxK + 1; ++r) {
@@ -229,12 +206,24 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) router_topk_kernel(
       for (int c = 0; c < RG; ++c) acc[c] = DF{0.f, 0.f};
       // one pass over H for RG candidates: a lane reads x[h] once and the
       // candidates' weights from the same row of W_gate
-      for (int hh = lane; hh < H; hh += 32) {
-        const float xv = ld_in<BF16>(x, (size_t)t * H + hh);
-        const size_t row = (size_t)hh * E;
+      // RU rows per lane per step: all their loads are issued before the
+      // double-float work, so many requests are in flight
+      for (int h0 = lane; h0 < H; h0 += 32 * RU) {
+        float xv[RU], wv[RU][RG];
 #pragma unroll
-        for (int c = 0; c < RG; ++c)
-          if (ce[c] >= 0) acc[c] = df_add(acc[c], two_prod(xv, ld_in<BF16>(wg, row + ce[c])));
+        for (int u = 0; u < RU; ++u) {
+          const int hh = h0 + 32 * u;
+          const bool in = hh < H;
+          xv[u] = in ? ld_in<BF16>(x, (size_t)t * H + hh) : 0.f;
+#pragma unroll
+          for (int c = 0; c < RG; ++c)
+            wv[u][c] = (in && ce[c] >= 0) ? ld_in<BF16>(wg, (size_t)hh * E + ce[c]) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < RU; ++u)
+#pragma unroll
+          for (int c = 0; c < RG; ++c)
+            if (ce[c] >= 0) acc[c] = df_add(acc[c], two_prod(xv[u], wv[u][c]));
       }
 #pragma unroll
       for (int c = 0; c < RG; ++c) {
@@ -336,10 +325,8 @@ cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, cons
                           cudaStream_t s) {
   if (d.n == 0) return cudaSuccess;
   if (router_tc_supported(d)) {
-    // tensor-core logits with fused softmax/TopK, then the flagged near ties
-    cudaError_t e = launch_router_tc(d, x, w_gate, bias, topk_idx, topk_w, logits, status, s);
-    if (e != cudaSuccess) return e;
-    return launch_topk_any(d, logits, x, w_gate, bias, topk_idx, topk_w, 1, s);
+    // tensor-core logits with softmax, TopK and near-tie rescoring fused
+    return launch_router_tc(d, x, w_gate, bias, topk_idx, topk_w, logits, status, s);
   }
   dim3 grid((d.n + RBM - 1) / RBM, (d.E + RBN - 1) / RBN);
   if (d.bf16)

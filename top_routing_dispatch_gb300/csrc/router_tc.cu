@@ -1,36 +1,48 @@
-// Router on the tcgen05 tensor cores with softmax and TopK fused into the
-// epilogue, for bf16 layers with E % 64 == 0.  "MoE 分布式推理基础（基于
-// vLLM）" §1.2, Algorithm 2 steps 1-3 and the router's renormalisation.
+// Router on the tcgen05 tensor cores with softmax, TopK and the near-tie
+// rescoring fused into one kernel, for bf16 layers with E % 64 == 0 and
+// K <= 8.  "MoE 分布式推理基础（基于 vLLM）" §1.2, Algorithm 2 steps 1-3 and
+// the router's renormalisation.
 //
-// One CTA per 128-token tile (persistent over tiles), 6 warps:
-//   warp 0      TMA producer: x tile (128 tokens x 64 k) and E/64 boxes of
-//               W_gate (64 k x 64 experts) per stage.
-//   warp 1      TMEM allocator and MMA issuer: 128 x E x 16 bf16 MMAs into one
-//               of two E-column float32 accumulators.
-//   warps 2..5  epilogue, one thread per token (= TMEM lane): adds the bias,
-//               stores the float32 logits, keeps the K+1 largest logits in
-//               registers (descending, ties to the lower expert id), computes
-//               max and sum of exp, and writes topk_idx / topk_w.  A token
-//               whose top K+1 logits lie closer than the rounding margin tau
-//               is flagged (topk_idx[t*K] = -1) and finished by the TopK kernel
-//               of router.cu, which rescores its candidates in double-float.
+// One CTA per 128-token tile (persistent over tiles), 18 warps:
+//   warp 0       TMA producer: x tile (128 tokens x 64 k) and E/64 boxes of
+//                W_gate (64 k x 64 experts) per stage.
+//   warp 1       TMEM allocator and MMA issuer: 128 x E x 16 bf16 MMAs into one
+//                of two E-column float32 accumulators.
+//   warps 2..17  epilogue: 4 TMEM lane quarters x 4 column slices.  Each
+//                thread owns one token and E/4 experts: it adds the bias,
+//                stores those float32 logits, keeps the K+1 largest in
+//                registers (descending, ties to the lower expert id), and
+//                computes their max and sum of exp.  After a barrier one
+//                thread per token merges the four slices.  Tokens whose top
+//                K+1 logits lie closer than the margin tau are rescored by all
+//                512 epilogue threads in double-float (exact products,
+//                error-free sums) over the experts within tau of the K-th
+//                logit, and chosen on those values.
 #include <cuda.h>
 
 #include <mutex>
 
 #include "common.cuh"
+#include "df.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int RT_BM = 128, RT_BK = 64, RT_STAGES = 4, RT_THREADS = 192;
-constexpr int RT_A_BYTES = RT_BM * RT_BK * 2;   // 16 KB
-constexpr int RT_BOX_BYTES = 64 * RT_BK * 2;    // 8 KB: 64 experts x 64 k
+constexpr int RT_BM = 128, RT_BK = 64, RT_MAX_STAGES = 8;
+constexpr int RT_SLICES = 4;                          // column slices per token
+constexpr int RT_EPI_WARPS = 4 * RT_SLICES;           // 16
+constexpr int RT_EPI_THREADS = 32 * RT_EPI_WARPS;     // 512
+constexpr int RT_THREADS = 64 + RT_EPI_THREADS;       // 576
+constexpr int RT_A_BYTES = RT_BM * RT_BK * 2;         // 16 KB
+constexpr int RT_BOX_BYTES = 64 * RT_BK * 2;          // 8 KB: 64 experts x 64 k
+constexpr int RT_PIPE_BYTES = 168 * 1024;             // operand stages
+constexpr int RS_SLOTS = 256;                         // candidate slots per rescoring sweep
+constexpr int RS_MAXF = 16;                           // flagged tokens per sweep
 
 struct RtTail {
-  uint64_t full[RT_STAGES];
-  uint64_t empty[RT_STAGES];
+  uint64_t full[RT_MAX_STAGES];
+  uint64_t empty[RT_MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -39,8 +51,46 @@ struct RtTail {
   float bias[kMaxE];
 };
 
+template <int KM>
+struct EpiSmem {
+  union {
+    struct {                             // selection: one list per (slice, token)
+      float pv[RT_SLICES][RT_BM][KM + 1];  // per-slice top K+1 values
+      int pi[RT_SLICES][RT_BM][KM + 1];    // ... and expert ids
+    } sel;
+    struct {                             // rescoring of the tile's flagged tokens
+      float phi[RT_EPI_THREADS];           // per-thread partial sums
+      float plo[RT_EPI_THREADS];
+      float chi[RS_SLOTS], clo[RS_SLOTS];  // per slot: summed over row groups + bias
+      int cexp[RS_SLOTS];                  // expert of each slot
+      int ctok[RS_SLOTS];                  // token (index in the sweep) of each slot
+      int tbase[RS_MAXF + 1];              // first slot of each token
+      int S, nb;                           // slots and tokens of the sweep
+    } res;
+  } u;
+  float pm[RT_SLICES][RT_BM];          // per-slice max
+  float ps[RT_SLICES][RT_BM];          // per-slice sum of exp(l - slice max)
+  int stop;                            // set by an epilogue thread whose wait gave up
+  int nflag;                           // flagged tokens of the tile
+  int ftok[RT_BM];
+  float fm[RT_BM], fS[RT_BM], fvK[RT_BM];
+};
+
+__host__ __device__ inline int rt_stages(int E) {
+  const int s = RT_PIPE_BYTES / (RT_A_BYTES + (E / 64) * RT_BOX_BYTES);
+  return s < RT_MAX_STAGES ? s : RT_MAX_STAGES;
+}
+
+// the tail (mbarriers) follows the epilogue area at a 16-byte boundary
+template <int KM>
+__host__ __device__ constexpr size_t epi_bytes() {
+  return (sizeof(EpiSmem<KM>) + 15) & ~size_t(15);
+}
+
+template <int KM>
 inline size_t rt_smem_bytes(int E) {
-  return 1024 + (size_t)RT_STAGES * (RT_A_BYTES + (E / 64) * RT_BOX_BYTES) + sizeof(RtTail);
+  return 1024 + (size_t)rt_stages(E) * (RT_A_BYTES + (E / 64) * RT_BOX_BYTES) + epi_bytes<KM>() +
+         sizeof(RtTail);
 }
 
 __device__ __forceinline__ bool rt_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
@@ -58,26 +108,172 @@ __device__ __forceinline__ bool rt_wait(uint64_t *bar, uint32_t parity, volatile
   }
 }
 
+// barrier among the 512 epilogue threads only
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"r"(RT_EPI_THREADS) : "memory");
+}
+
 // (v, e) ranks above (w, f): larger value, or equal value and lower expert id
 __device__ __forceinline__ bool ranks_above(float v, int e, float w, int f) {
   return v > w || (v == w && e < f);
 }
 
-template <int KM>  // K == KM: every list index is a compile-time constant
+// Rescoring of the tile's flagged tokens by the 512 epilogue threads.  A
+// sweep takes up to 16 flagged tokens and their candidate experts (within tau
+// of the token's K-th float32 logit), one slot per (token, candidate), at most
+// 256 slots.  Thread et serves slot et mod Sp (Sp = slots rounded up to a
+// power of two) over the rows h congruent to et / Sp modulo 512 / Sp,
+// accumulating x[t,h] * W_gate[h,e] in double-float (four interleaved
+// accumulators).  The 32 threads of a warp serve consecutive slots of the same
+// row, so their W_gate loads fall in the few sectors of that row.  The
+// partial sums are added in a fixed order, the bias is added, and one warp per
+// token keeps the K largest.
+template <int KM>
+__device__ __forceinline__ void rescore_tile(EpiSmem<KM> &ep, const float *__restrict__ bias_s,
+                                             const __nv_bfloat16 *__restrict__ x,
+                                             const __nv_bfloat16 *__restrict__ wg,
+                                             const float *__restrict__ logits,
+                                             int32_t *__restrict__ topk_idx,
+                                             float *__restrict__ topk_w, int H, int E, int norm,
+                                             float tau_rel, int ew, int lane, int et) {
+  constexpr int K = KM;
+  auto &rs = ep.u.res;
+  const int nflag = ep.nflag;
+  for (int b0 = 0; b0 < nflag;) {
+    // slots of this sweep (warp 0), in ascending expert order per token
+    if (ew == 0) {
+      int total = 0, nb = 0;
+      for (int g = b0; g < nflag && nb < RS_MAXF; ++g) {
+        const int ft = ep.ftok[g];
+        const float thr = ep.fvK[g] - tau_rel * fmaxf(1.f, fabsf(ep.fm[g]));
+        int C = 0;
+        for (int j = 0; j < E / 32; ++j)
+          C += __popc(__ballot_sync(0xffffffffu, logits[(size_t)ft * E + lane + 32 * j] >= thr));
+        if (nb > 0 && total + C > RS_SLOTS) break;
+        int pos = total;
+        for (int j = 0; j < E / 32; ++j) {
+          const int e = lane + 32 * j;
+          const unsigned ball = __ballot_sync(0xffffffffu, logits[(size_t)ft * E + e] >= thr);
+          if (ball >> lane & 1u) {
+            const int sl = pos + __popc(ball & ((1u << lane) - 1u));
+            rs.cexp[sl] = e;
+            rs.ctok[sl] = nb;
+          }
+          pos += __popc(ball);
+        }
+        if (lane == 0) rs.tbase[nb] = total;
+        total += C;
+        ++nb;
+      }
+      if (lane == 0) {
+        rs.tbase[nb] = total;
+        rs.S = total;
+        rs.nb = nb;
+      }
+    }
+    epi_bar();
+    const int S = rs.S, nb = rs.nb;
+    int Sp = 1;
+    while (Sp < S) Sp <<= 1;
+    const int G = RT_EPI_THREADS / Sp;  // row groups
+    const int s_id = et & (Sp - 1), g_id = et / Sp;
+    const bool active = s_id < S;
+    const int e_s = active ? rs.cexp[s_id] : 0;
+    const int f_s = active ? rs.ctok[s_id] : 0;
+    DF acc{0.f, 0.f};
+    if (active) {
+      const __nv_bfloat16 *xr = x + (size_t)ep.ftok[b0 + f_s] * H;
+      const __nv_bfloat16 *wc = wg + e_s;
+      DF a4[4] = {DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}};
+      int h = g_id;
+      for (; h + 7 * G < H; h += 8 * G) {
+        float xv[8], wv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          xv[u] = __bfloat162float(xr[h + u * G]);
+          wv[u] = __bfloat162float(wc[(size_t)(h + u * G) * E]);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a4[u & 3] = df_add(a4[u & 3], two_prod(xv[u], wv[u]));
+      }
+      for (; h < H; h += G)
+        a4[0] = df_add(a4[0], two_prod(__bfloat162float(xr[h]), __bfloat162float(wc[(size_t)h * E])));
+      acc = df_add(df_add(a4[0], a4[1]), df_add(a4[2], a4[3]));
+    }
+    rs.phi[et] = acc.hi;
+    rs.plo[et] = acc.lo;
+    epi_bar();
+    for (int sl = et; sl < S; sl += RT_EPI_THREADS) {
+      DF sum{0.f, 0.f};
+      for (int g = 0; g < G; ++g) sum = df_add(sum, DF{rs.phi[g * Sp + sl], rs.plo[g * Sp + sl]});
+      const float bb = bias_s[rs.cexp[sl]];
+      sum = isinf(bb) ? DF{bb, 0.f} : df_add(sum, DF{bb, 0.f});
+      rs.chi[sl] = sum.hi;
+      rs.clo[sl] = sum.lo;
+    }
+    epi_bar();
+    // warp f keeps the K best of the sweep's token f
+    if (ew < nb && lane == 0) {
+      const int g = b0 + ew;
+      const int ft = ep.ftok[g];
+      DF lv[K];
+      int li[K];
+#pragma unroll
+      for (int z = 0; z < K; ++z) {
+        lv[z] = DF{-INFINITY, 0.f};
+        li[z] = 0x7fffffff;
+      }
+      for (int sl = rs.tbase[ew]; sl < rs.tbase[ew + 1]; ++sl) {
+        DF cv{rs.chi[sl], rs.clo[sl]};
+        int ci = rs.cexp[sl];
+#pragma unroll
+        for (int z = 0; z < K; ++z) {
+          const bool gt = df_greater(cv, ci, lv[z], li[z]);
+          const DF tv = gt ? lv[z] : cv;
+          const int ti = gt ? li[z] : ci;
+          lv[z] = gt ? cv : lv[z];
+          li[z] = gt ? ci : li[z];
+          cv = tv;
+          ci = ti;
+        }
+      }
+      float w[K];
+      float wsum = 0.f;
+#pragma unroll
+      for (int z = 0; z < K; ++z) {
+        w[z] = expf(logits[(size_t)ft * E + li[z]] - ep.fm[g]) / ep.fS[g];
+        wsum += w[z];
+      }
+#pragma unroll
+      for (int z = 0; z < K; ++z) {
+        topk_idx[(size_t)ft * K + z] = li[z];
+        topk_w[(size_t)ft * K + z] = norm ? w[z] / wsum : w[z];
+      }
+    }
+    epi_bar();  // the slots and staging buffers are reused by the next sweep
+    b0 += nb;
+  }
+}
+
+template <int KM>
 __global__ void __launch_bounds__(RT_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
-                     const __grid_constant__ CUtensorMap tmW, const float *__restrict__ bias,
-                     float *__restrict__ logits, int32_t *__restrict__ topk_idx,
-                     float *__restrict__ topk_w, int n, int H, int E, int K, int norm,
-                     uint32_t idesc, uint32_t tmem_cols, int32_t *status) {
+                     const __grid_constant__ CUtensorMap tmW,
+                     const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ wg,
+                     const float *__restrict__ bias, float *__restrict__ logits,
+                     int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int n, int H,
+                     int E, int norm, uint32_t idesc, uint32_t tmem_cols, int32_t *status) {
+  constexpr int K = KM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int nbox = E / 64;
   const int b_stage = nbox * RT_BOX_BYTES;
+  const int STAGES = rt_stages(E);
   uint8_t *smemA = smem;
-  uint8_t *smemB = smem + RT_STAGES * RT_A_BYTES;
-  RtTail &st = *reinterpret_cast<RtTail *>(smem + RT_STAGES * (RT_A_BYTES + b_stage));
+  uint8_t *smemB = smem + STAGES * RT_A_BYTES;
+  EpiSmem<KM> &ep = *reinterpret_cast<EpiSmem<KM> *>(smem + STAGES * (RT_A_BYTES + b_stage));
+  RtTail &st = *reinterpret_cast<RtTail *>(reinterpret_cast<uint8_t *>(&ep) + epi_bytes<KM>());
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (n + RT_BM - 1) / RT_BM;
@@ -85,16 +281,18 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   if ((int)blockIdx.x >= n_tiles) return;
 
   if (tid == 0) {
-    for (int s = 0; s < RT_STAGES; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&st.full[s], 1);
       ptx::mbar_init(&st.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&st.tfull[a], 1);
-      ptx::mbar_init(&st.tempty[a], 4);
+      ptx::mbar_init(&st.tempty[a], RT_EPI_WARPS);
     }
     ptx::mbar_init(&st.drain, 1);
     st.abort_flag = 0;
+    ep.nflag = 0;
+    ep.stop = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
@@ -132,14 +330,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
                              q * 64, kb * RT_BK);
           used |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == RT_STAGES) {
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (stop) break;
       }
-      for (int s = 0; s < RT_STAGES; ++s)
+      for (int s = 0; s < STAGES; ++s)
         if (used >> s & 1u) ptx::mbar_wait(&st.full[s], last_par >> s & 1u);
     }
   } else if (warp == 1) {
@@ -166,7 +364,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
             ptx::mma_bf16(d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit(&st.empty[stage]);
-          if (++stage == RT_STAGES) {
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
@@ -180,50 +378,60 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       ptx::mbar_wait(&st.drain, 0);
     }
   } else {
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
+    const int ew = warp - 2;              // epilogue warp 0..15
+    const int q = warp & 3;               // TMEM lane quarter this warp may read
+    const int sl = ew >> 2;               // column slice 0..3
+    const int r = q * 32 + lane;          // token row in the tile
+    const int et = ew * 32 + lane;        // 0..511
+    const int cols = E / RT_SLICES;
+    const int c0 = sl * cols;
+    const float tau_rel = tie_margin_tc(H);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      if (!rt_wait(&st.tfull[acc], acc_phase, abort_flag, status)) break;
+      // all 512 threads take every barrier below; a thread whose wait gave up
+      // raises ep.stop before the first one, so all leave together
+      if (!rt_wait(&st.tfull[acc], acc_phase, abort_flag, status)) ep.stop = 1;
+      epi_bar();
+      if (ep.stop) break;
       ptx::tc_fence_after();
-      const uint32_t tbase = tmem + (uint32_t)(acc * E) + ((uint32_t)(q * 32) << 16);
+      const uint32_t tbase = tmem + (uint32_t)(acc * E + c0) + ((uint32_t)(q * 32) << 16);
       const int tok = t * RT_BM + r;
       const bool valid = tok < n;
       float *lrow = logits + (size_t)(valid ? tok : 0) * E;
 
-      // pass 1: logits, running max, top K+1 list
-      float lv[KM + 1];
-      int li[KM + 1];
+      // this slice: logits, max, top K+1 (descending, ties to the lower id)
+      float lv[K + 1];
+      int li[K + 1];
 #pragma unroll
-      for (int j = 0; j <= KM; ++j) {
+      for (int j = 0; j <= K; ++j) {
         lv[j] = -INFINITY;
         li[j] = 0x7fffffff;
       }
-      float last_v = -INFINITY;  // the (K+1)-th entry: the insertion threshold
+      float last_v = -INFINITY;
       int last_i = 0x7fffffff;
       float m = -INFINITY;
-      for (int c = 0; c < E / 8; ++c) {
+      for (int c = 0; c < cols / 8; ++c) {
         uint32_t raw[8];
         ptx::tmem_ld_32x32b_x8(tbase + c * 8, raw);
         ptx::tmem_ld_wait();
         float v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(raw[i]) + st.bias[c * 8 + i];
+        for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(raw[i]) + st.bias[c0 + c * 8 + i];
         if (valid) {
-          float4 *dst = reinterpret_cast<float4 *>(lrow + c * 8);
+          float4 *dst = reinterpret_cast<float4 *>(lrow + c0 + c * 8);
           dst[0] = make_float4(v[0], v[1], v[2], v[3]);
           dst[1] = make_float4(v[4], v[5], v[6], v[7]);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           m = fmaxf(m, v[i]);
-          const int e = c * 8 + i;
+          const int e = c0 + c * 8 + i;
           if (ranks_above(v[i], e, last_v, last_i)) {
             float cv = v[i];
             int ci = e;
 #pragma unroll
-            for (int j = 0; j <= KM; ++j) {
+            for (int j = 0; j <= K; ++j) {
               const bool gt = ranks_above(cv, ci, lv[j], li[j]);
               const float tv = gt ? lv[j] : cv;
               const int ti = gt ? li[j] : ci;
@@ -232,53 +440,102 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
               cv = tv;
               ci = ti;
             }
-            last_v = lv[KM];
-            last_i = li[KM];
+            last_v = lv[K];
+            last_i = li[K];
           }
         }
       }
-      // pass 2: sum of exp(l - max)
       float ssum = 0.f;
-      for (int c = 0; c < E / 32; ++c) {
-        uint32_t raw[32];
-        ptx::tmem_ld_32x32b_x32(tbase + c * 32, raw);
+      for (int c = 0; c < cols / 8; ++c) {
+        uint32_t raw[8];
+        ptx::tmem_ld_32x32b_x8(tbase + c * 8, raw);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          ssum += expf(__uint_as_float(raw[i]) + st.bias[c * 32 + i] - m);
+        for (int i = 0; i < 8; ++i)
+          ssum += expf(__uint_as_float(raw[i]) + st.bias[c0 + c * 8 + i] - m);
       }
-      // the accumulator can be reused by the next tile
+      // the accumulator is free for the next tile
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&st.tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
 
-      if (valid) {
-        const int R = K + 1 < E ? K + 1 : E;
-        const float tau = 1e-3f * fmaxf(1.f, fabsf(lv[0]));
+#pragma unroll
+      for (int j = 0; j <= K; ++j) {
+        ep.u.sel.pv[sl][r][j] = lv[j];
+        ep.u.sel.pi[sl][r][j] = li[j];
+      }
+      ep.pm[sl][r] = m;
+      ep.ps[sl][r] = ssum;
+      __threadfence_block();  // the logits rows are read back below
+      epi_bar();
+
+      // merge the four slices: one thread per token
+      if (sl == 0 && valid) {
+        float fv[K + 1];
+        int fi[K + 1];
+        int h0 = 0, h1 = 0, h2 = 0, h3 = 0;
+#pragma unroll
+        for (int j = 0; j <= K; ++j) {
+          float bv = h0 <= K ? ep.u.sel.pv[0][r][h0] : -INFINITY;
+          int bi = h0 <= K ? ep.u.sel.pi[0][r][h0] : 0x7fffffff;
+          int bw = 0;
+          const float v1 = h1 <= K ? ep.u.sel.pv[1][r][h1] : -INFINITY;
+          const int i1 = h1 <= K ? ep.u.sel.pi[1][r][h1] : 0x7fffffff;
+          if (ranks_above(v1, i1, bv, bi)) { bv = v1; bi = i1; bw = 1; }
+          const float v2 = h2 <= K ? ep.u.sel.pv[2][r][h2] : -INFINITY;
+          const int i2 = h2 <= K ? ep.u.sel.pi[2][r][h2] : 0x7fffffff;
+          if (ranks_above(v2, i2, bv, bi)) { bv = v2; bi = i2; bw = 2; }
+          const float v3 = h3 <= K ? ep.u.sel.pv[3][r][h3] : -INFINITY;
+          const int i3 = h3 <= K ? ep.u.sel.pi[3][r][h3] : 0x7fffffff;
+          if (ranks_above(v3, i3, bv, bi)) { bv = v3; bi = i3; bw = 3; }
+          fv[j] = bv;
+          fi[j] = bi;
+          h0 += bw == 0;
+          h1 += bw == 1;
+          h2 += bw == 2;
+          h3 += bw == 3;
+        }
+        float M = ep.pm[0][r];
+#pragma unroll
+        for (int w = 1; w < RT_SLICES; ++w) M = fmaxf(M, ep.pm[w][r]);
+        float S = 0.f;
+#pragma unroll
+        for (int w = 0; w < RT_SLICES; ++w) S += ep.ps[w][r] * expf(ep.pm[w][r] - M);
+        const float tau = tau_rel * fmaxf(1.f, fabsf(M));
         bool amb = false;
 #pragma unroll
-        for (int j = 0; j < KM; ++j)
-          if (j + 1 < R && isfinite(lv[j]) && isfinite(lv[j + 1]) && lv[j] - lv[j + 1] < tau)
-            amb = true;
-        float w[KM];
-        float wsum = 0.f;
+        for (int j = 0; j < K; ++j)
+          if (isfinite(fv[j]) && isfinite(fv[j + 1]) && fv[j] - fv[j + 1] < tau) amb = true;
+        if (!amb) {
+          float w[K];
+          float wsum = 0.f;
 #pragma unroll
-        for (int j = 0; j < KM; ++j) {
-          w[j] = j < K ? expf(lv[j] - m) / ssum : 0.f;
-          wsum += w[j];
-        }
-        int32_t *irow = topk_idx + (size_t)tok * K;
-        float *wrow = topk_w + (size_t)tok * K;
-#pragma unroll
-        for (int j = 0; j < KM; ++j) {
-          if (j < K) {
-            irow[j] = (j == 0 && amb) ? -1 : li[j];
-            wrow[j] = norm ? w[j] / wsum : w[j];
+          for (int j = 0; j < K; ++j) {
+            w[j] = expf(fv[j] - M) / S;
+            wsum += w[j];
           }
+#pragma unroll
+          for (int j = 0; j < K; ++j) {
+            topk_idx[(size_t)tok * K + j] = fi[j];
+            topk_w[(size_t)tok * K + j] = norm ? w[j] / wsum : w[j];
+          }
+        } else {
+          const int slot = atomicAdd(&ep.nflag, 1);
+          ep.ftok[slot] = tok;
+          ep.fm[slot] = M;
+          ep.fS[slot] = S;
+          ep.fvK[slot] = fv[K - 1];
         }
       }
+      epi_bar();
+
+      // rescoring of the tile's flagged tokens (all 512 epilogue threads)
+      rescore_tile<KM>(ep, st.bias, x, wg, logits, topk_idx, topk_w, H, E, norm, tau_rel, ew, lane,
+                       et);
+      epi_bar();  // the rescoring lists alias the next tile's selection lists
+      if (et == 0) ep.nflag = 0;
     }
   }
 
@@ -343,28 +600,34 @@ cudaError_t launch_router_tc(const Desc &d, const void *x, const void *w_gate, c
   const int sms = device_sm_count();
   const int grid = n_tiles < sms ? n_tiles : sms;
   const uint32_t idesc = ptx::idesc_bf16_f32(RT_BM, d.E, false, true);
-  auto run = [&](auto kernel) -> cudaError_t {
+  const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
+  const __nv_bfloat16 *wb = reinterpret_cast<const __nv_bfloat16 *>(w_gate);
+  auto run = [&](auto kernel, size_t smem_max, size_t smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)rt_smem_bytes(kMaxE));
+                                         (int)smem_max);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, RT_THREADS, rt_smem_bytes(d.E), s>>>(mX, mW, bias, logits, topk_idx, topk_w,
-                                                        d.n, d.H, d.E, d.K, d.norm ? 1 : 0,
-                                                        idesc, cols, status);
-    return cudaSuccess;
+    kernel<<<grid, RT_THREADS, smem, s>>>(mX, mW, xb, wb, bias, logits, topk_idx, topk_w, d.n,
+                                          d.H, d.E, d.norm ? 1 : 0, idesc, cols, status);
+    return cudaGetLastError();
   };
-  cudaError_t e;
+#define MOE_RT_CASE(KK)                                                              \
+  case KK:                                                                           \
+    return run(router_tc_kernel<KK>, rt_smem_bytes<KK>(64) > rt_smem_bytes<KK>(256) \
+                                         ? rt_smem_bytes<KK>(64)                     \
+                                         : rt_smem_bytes<KK>(256),                   \
+               rt_smem_bytes<KK>(d.E));
   switch (d.K) {
-    case 1: e = run(router_tc_kernel<1>); break;
-    case 2: e = run(router_tc_kernel<2>); break;
-    case 3: e = run(router_tc_kernel<3>); break;
-    case 4: e = run(router_tc_kernel<4>); break;
-    case 5: e = run(router_tc_kernel<5>); break;
-    case 6: e = run(router_tc_kernel<6>); break;
-    case 7: e = run(router_tc_kernel<7>); break;
-    default: e = run(router_tc_kernel<8>); break;
+    MOE_RT_CASE(1)
+    MOE_RT_CASE(2)
+    MOE_RT_CASE(3)
+    MOE_RT_CASE(4)
+    MOE_RT_CASE(5)
+    MOE_RT_CASE(6)
+    MOE_RT_CASE(7)
+    MOE_RT_CASE(8)
+    default: return cudaErrorInvalidValue;
   }
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+#undef MOE_RT_CASE
 }
 
 }  // namespace moe
