@@ -125,6 +125,29 @@ class ClockSampler:
                 "samples": len(load)}
 
 
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The largest `value` over all ranks (every rank gets it); the value
+    itself when running alone."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(cfg, rank):
+    """Seed of a rank's token batch: rank 0 runs the workload's own inputs,
+    the other replicas get their own batches (weak scaling)."""
+    return cfg.seed if rank == 0 else cfg.seed + 1000 * rank
+
+
+def aggregate_tokens_per_s(tokens_per_rank_step, steps, world, max_total_ms):
+    """Whole-job throughput: the tokens all ranks processed over the slowest
+    rank's time."""
+    return world * tokens_per_rank_step * steps / (max_total_ms * 1e-3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -307,7 +330,7 @@ def run_ours(args, cfg):
     peaks, peak_src = load_peaks()
 
     L = synth.make_layer(cfg, dev)
-    x = synth.make_x(cfg, dev, seed=cfg.seed if rank == 0 else cfg.seed + 1000 * rank)
+    x = synth.make_x(cfg, dev, seed=rank_seed(cfg, rank))
     desc = M.desc_for(cfg)
     layer = M.MoELayer(desc, L["w_gate"], L["bias"], L["w13"], L["w2"])
     v = {k: layer.view(k) for k in ("logits", "topk_idx", "topk_w", "counts", "offsets", "perm",
@@ -355,11 +378,7 @@ def run_ours(args, cfg):
     per_phase = {name: [s[i].elapsed_time(s[i + 1]) for s in steps]
                  for i, (name, _) in enumerate(phases)}
     step_ms = [s[0].elapsed_time(s[-1]) for s in steps]
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     status = M.moe_check_status(st, stream)
 
     # the same layer through the single forward call (cross-check of the step)
@@ -378,12 +397,7 @@ def run_ours(args, cfg):
     for _ in range(2):
         T.measure(e2e_step, 1)
     e2e_ms = T.measure(e2e_step, args.steps)
-    if dist:
-        t = torch.tensor([sum(e2e_ms)], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    else:
-        e2e_total = sum(e2e_ms)
+    e2e_total = max_over_ranks(sum(e2e_ms), dist, dev)
 
     counts = v["counts"].cpu().tolist()
     alg = algorithmic(cfg, counts)
@@ -409,7 +423,8 @@ def run_ours(args, cfg):
                 "algorithmic_bytes_per_launch": alg["gemm1"]["bytes"]}
 
     out = {
-        "metric": METRIC, "value": world * cfg.n * args.steps / (total_ms * 1e-3), "unit": UNIT,
+        "metric": METRIC, "value": aggregate_tokens_per_s(cfg.n, args.steps, world, total_ms),
+        "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
@@ -420,7 +435,7 @@ def run_ours(args, cfg):
         "roofline": roofline,
         "kernels": kernels,
         "api_forward_ms_per_step": statistics.median(api_ms),
-        "e2e": {"value": world * cfg.n * args.steps / (e2e_total * 1e-3), "unit": UNIT,
+        "e2e": {"value": aggregate_tokens_per_s(cfg.n, args.steps, world, e2e_total), "unit": UNIT,
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
                 "d2h_bytes_per_step": y_h.numel() * y_h.element_size()},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
