@@ -43,6 +43,7 @@ constexpr int B_STAGE_BYTES = 4 * B_BOX_BYTES;      // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;                      // two 256-column accumulators
+constexpr int EPI_ROW_BYTES_ = 80, EPI_WARP_BYTES_ = 32 * EPI_ROW_BYTES_;
 
 struct SmemTail {
   uint64_t full[STAGES];
@@ -56,6 +57,7 @@ struct SmemTail {
   int total_mtiles;
   int off[kMaxE + 1];
   int tp[kMaxE + 1];  // first m-tile of each expert (exclusive prefix)
+  alignas(16) uint8_t epi[4][EPI_WARP_BYTES_];  // per epilogue warp staging
 };
 
 constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES +
@@ -106,7 +108,37 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+// SiLU(g) = g / (1 + exp(-g)) with the fast exponential and divide (h is
+// rounded to bf16 right after); the exponent is clamped so 1 + e stays finite.
+__device__ __forceinline__ float silu(float g) {
+  return __fdividef(g, 1.0f + __expf(fminf(-g, 80.f)));
+}
+
+// Epilogue staging: each epilogue warp puts its 32 rows x 32 columns (64 B per
+// row) in shared memory, then stores them as whole 64-byte row segments, 8
+// rows per store instruction.  Rows are 80 B apart so that both the row-wise
+// writes and the segment-wise reads are (nearly) free of bank conflicts.
+constexpr int EPI_ROW_BYTES = 80;
+constexpr int EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
+
+__device__ __forceinline__ void store_tile_chunk(uint8_t *wbuf, const uint32_t (&pk)[16], int lane,
+                                                 __nv_bfloat16 *out, size_t ld, int row0,
+                                                 int rows, int col0) {
+  uint4 *mine = reinterpret_cast<uint4 *>(wbuf + lane * EPI_ROW_BYTES);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) mine[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int p = lane + 32 * i;
+    const int row = p >> 2, c16 = p & 3;
+    if (row < rows) {
+      const uint4 val = *reinterpret_cast<const uint4 *>(wbuf + row * EPI_ROW_BYTES + c16 * 16);
+      *reinterpret_cast<uint4 *>(out + (size_t)(row0 + row) * ld + col0 + c16 * 8) = val;
+    }
+  }
+  __syncwarp();
+}
 
 // MODE 1: GEMM1 + SwiGLU (B = W13, out = h, n-tile = 128 h columns)
 // MODE 2: GEMM2          (B = W2,  out = y_perm, n-tile = 256 columns)
@@ -266,9 +298,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!wait_or_abort(&st.tfull[acc], acc_phase, abort_flag, status)) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + (uint32_t)(acc * UMMA_N) + ((uint32_t)(q * 32) << 16);
-      const bool valid = r < ti.rows;
+      // rows of this warp's 32-row slice that belong to the tile's expert
+      const int wrows = ti.rows - q * 32;
+      const int wrow0 = ti.row0 + q * 32;
+      uint8_t *wbuf = st.epi[q];
       if (MODE == 1) {
-        __nv_bfloat16 *orow = out + (size_t)(ti.row0 + (valid ? r : 0)) * I + ti.nt * 128;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t g[32], u[32];
@@ -282,15 +316,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
             pk[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
           }
-          if (valid) {
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          }
+          store_tile_chunk(wbuf, pk, lane, out, (size_t)I, wrow0, wrows, ti.nt * 128 + c * 32);
         }
       } else {
-        __nv_bfloat16 *orow = out + (size_t)(ti.row0 + (valid ? r : 0)) * Nout + ti.nt * UMMA_N;
 #pragma unroll 1
         for (int c = 0; c < UMMA_N / 32; ++c) {
           if (ti.nt * UMMA_N + c * 32 >= Nout) break;  // uniform across the warp
@@ -301,12 +329,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
-          if (valid) {
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          }
+          store_tile_chunk(wbuf, pk, lane, out, (size_t)Nout, wrow0, wrows,
+                           ti.nt * UMMA_N + c * 32);
         }
       }
       ptx::tc_fence_before();
