@@ -35,10 +35,10 @@ METRIC = "MoE-layer tokens/s and grouped-GEMM TFLOP/s (% BF16 peak), permute/com
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20          # > 129 MB L2
-# kernels of the library launched by one layer step (single stream):
-# router 2 (logits GEMM, softmax/TopK) + layout 3 (count, scan, scatter)
-# + permute 1 + GEMM1 1 + GEMM2 1 + combine 1
-KERNELS_PER_STEP = 9
+# kernels of the library launched by one layer step (single stream, bf16 with
+# E % 64 == 0): router 1 (tensor-core logits + TopK + near-tie rescoring)
+# + layout 3 (count, scan, scatter) + permute 1 + GEMM1 1 + GEMM2 1 + combine 1
+KERNELS_PER_STEP = 8
 
 
 def parse_args():
@@ -252,6 +252,10 @@ def algorithmic(cfg, counts=None):
         "layout": {"flop": 0, "bytes": 2 * nK * 4 + 2 * nK * 4 + (2 * E + 1) * 4},
         "permute": {"flop": 0, "bytes": n * H * b + nK * H * b + nK * 4},
         "gemm1": {"flop": 4 * nK * H * I, "bytes": nK * H * b + used * H * 2 * I * b + nK * I * b},
+        # GEMM1 with the permute fused: x once (rows are re-read from L2),
+        # perm, the used experts' W13, h
+        "gemm1_gather": {"flop": 4 * nK * H * I,
+                         "bytes": n * H * b + nK * 4 + used * H * 2 * I * b + nK * I * b},
         "gemm2": {"flop": 2 * nK * I * H, "bytes": nK * I * b + used * I * H * b + nK * H * b},
         "combine": {"flop": 2 * nK * H, "bytes": nK * H * b + n * H * b + 2 * nK * 4},
     }
@@ -399,13 +403,22 @@ def run_ours(args, cfg):
     e2e_ms = T.measure(e2e_step, args.steps)
     e2e_total = max_over_ranks(sum(e2e_ms), dist, dev)
 
+    # an entry point the step does not call, timed alone on the same layout:
+    # GEMM1 with the permute fused into its A loads (x_perm never written)
+    h_alt = torch.empty_like(v["h"])
+    fused = lambda: M.moe_expert_gemm1_swiglu_gather(desc, x, v["perm"], L["w13"], v["offsets"],
+                                                     h_alt, 0, st, stream)
+    T.measure(fused, 3)
+    per_phase["gemm1_gather"] = T.measure(fused, max(5, args.steps // 2))
+
     counts = v["counts"].cpu().tolist()
     alg = algorithmic(cfg, counts)
     kernels = {}
     for name, ts in per_phase.items():
         ms = statistics.mean(ts)
         a = alg[name]
-        k = {"ms": ms, "gbs": a["bytes"] / (ms * 1e-3) / 1e9}
+        k = {"ms": ms, "gbs": a["bytes"] / (ms * 1e-3) / 1e9,
+             "in_step": any(name == p for p, _ in phases)}
         k["frac_hbm"] = k["gbs"] / peaks["hbm_gbs"]
         if a["flop"]:
             k["tflops"] = a["flop"] / (ms * 1e-3) / 1e12

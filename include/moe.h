@@ -186,6 +186,28 @@ moe_status_t moe_grouped_swiglu(const moe_layer_desc_t *desc, const void *x_perm
 moe_status_t moe_expert_gemm1_swiglu(const moe_layer_desc_t *desc, const void *x_perm,
                                      const void *w13, const int32_t *offsets, void *h,
                                      int sm_reserve, int32_t *status_word, moe_stream_t stream);
+/*
+ * GEMM1 + SwiGLU with the permute fused into it (bf16 layers only): the A
+ * rows of expert e's segment are read straight from x, row r being token
+ * perm[r] / K, by tensor-memory-accelerator gathers of four rows at a time,
+ * so x_perm is never written.  The gather of Algorithm 2 step 7 and step 8 in
+ * one pass: the permute folded into the expert GEMM, as HybridEP's
+ * dispatch_with_permute (DModel notes "0. goin", §2.4) and FLUX/COMET's
+ * scatter-into-grouped-GEMM ("大模型系统中的通算融合", §4.2.4) do.  Results
+ * are bitwise identical to moe_permute followed by moe_expert_gemm1_swiglu.
+ * A perm entry outside [0, n*K) sets MOE_DEV_BAD_LAYOUT and leaves that row
+ * of h unspecified.  It trades speed for memory: x_perm (n*K*H elements) is
+ * never allocated, but A rows arrive through 16-byte cp.async gathers from
+ * L2, slower than the TMA tile loads of a materialised x_perm, so
+ * moe_forward_microbatches uses moe_permute + moe_expert_gemm1_swiglu.
+ *   x (n,H) bf16; perm (n*K) int32 as from moe_dispatch_layout; other
+ *   arguments as for moe_expert_gemm1_swiglu.  float32 layers:
+ *   MOE_ERR_UNSUPPORTED.
+ */
+moe_status_t moe_expert_gemm1_swiglu_gather(const moe_layer_desc_t *desc, const void *x,
+                                            const int32_t *perm, const void *w13,
+                                            const int32_t *offsets, void *h, int sm_reserve,
+                                            int32_t *status_word, moe_stream_t stream);
 moe_status_t moe_expert_gemm2(const moe_layer_desc_t *desc, const void *h, const void *w2,
                               const int32_t *offsets, void *y_perm, int sm_reserve,
                               int32_t *status_word, moe_stream_t stream);

@@ -71,10 +71,22 @@ def check_layout(run):
     assert np.array_equal(run.np("inv_perm"), inv)
 
 
+def run_permute(run):
+    """x_perm from an explicit moe_permute call on the layer's own layout, into
+    a fresh buffer."""
+    import top_routing_dispatch_gb300 as M
+    xp = torch.empty((run.cfg.nK, run.cfg.H), dtype=run.x.dtype, device=run.dev)
+    st = torch.zeros(1, dtype=torch.int32, device=run.dev)
+    M.moe_permute(run.desc, run.x, run.view("perm"), xp, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return xp
+
+
 def check_permute(run, sample_rows=None):
     """x_perm against the oracle's gather, exactly (bf16/f32 -> f64 is exact)."""
     perm = run.np("perm")
-    xp = run.view("x_perm")
+    xp = run_permute(run)
     if sample_rows is None:
         assert np.array_equal(f64(xp), O.permute(f64(run.x), perm, run.cfg.K))
         return
@@ -85,21 +97,22 @@ def check_permute(run, sample_rows=None):
 
 
 def check_experts(run, sample_rows=None):
-    """GPU h and y_perm against the oracle's SwiGLU of the GPU's own x_perm."""
+    """GPU h and y_perm against the oracle's SwiGLU: GEMM1 on the oracle's
+    gather of x (Algorithm 2 step 7), GEMM2 on the GPU's (rounded) h."""
     cfg = run.cfg
     off = run.np("offsets")
-    xp = run.view("x_perm")
+    perm = run.np("perm")
     h = run.view("h")
     yp = run.view("y_perm")
     nK = cfg.nK
     rows = np.arange(nK) if sample_rows is None else np.asarray(sorted(set(sample_rows)))
     experts = np.searchsorted(off, rows, side="right") - 1
+    x64 = f64(run.x)
     hs, ys, ho, yo = [], [], [], []
     for e in np.unique(experts):
         r = rows[experts == e]
-        ri = torch.as_tensor(r, device=xp.device)
-        # GEMM1+SwiGLU on the GPU's x_perm; GEMM2 on the GPU's (rounded) h
-        ho.append(O.expert_up(f64(xp[ri]), run.w13_get(int(e))))
+        ri = torch.as_tensor(r, device=h.device)
+        ho.append(O.expert_up(O.permute(x64, perm[r], cfg.K), run.w13_get(int(e))))
         yo.append(O.expert_down(f64(h[ri]), run.w2_get(int(e))))
         hs.append(f64(h[ri]))
         ys.append(f64(yp[ri]))
@@ -109,6 +122,29 @@ def check_experts(run, sample_rows=None):
     assert eh <= tol, f"h error {eh:.3e}"
     assert ey <= tol, f"y_perm error {ey:.3e}"
     return eh, ey
+
+
+def check_gather_fusion(run):
+    """bf16: GEMM1 with the gather fused into its A loads gives the same bits
+    as moe_permute followed by the unfused GEMM1 (each h row depends on its
+    own A row only, and both read the same values)."""
+    import top_routing_dispatch_gb300 as M
+    cfg = run.cfg
+    if cfg.dtype != "bf16" or cfg.I % 128 or cfg.H % 64:
+        return
+    xp = run_permute(run)
+    h1 = torch.empty((cfg.nK, cfg.I), dtype=run.x.dtype, device=run.dev)
+    h2 = torch.empty_like(h1)
+    st = torch.zeros(1, dtype=torch.int32, device=run.dev)
+    off = run.view("offsets")
+    M.moe_expert_gemm1_swiglu(run.desc, xp, run.L["w13"], off, h1, status_word=st)
+    M.moe_expert_gemm1_swiglu_gather(run.desc, run.x, run.view("perm"), run.L["w13"], off, h2,
+                                     status_word=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+    # and both equal the h of the forward
+    assert torch.equal(h2.view(torch.int16), run.view("h").view(torch.int16))
 
 
 def check_combine(run):
@@ -137,6 +173,7 @@ def test_small_all_steps(cfg):
     check_layout(run)
     check_permute(run)
     check_experts(run)
+    check_gather_fusion(run)
     check_combine(run)
     check_layer(run)
 
@@ -163,6 +200,7 @@ def test_full_size(cfg):
         rows += list(seg[:3]) + list(seg[-3:]) + list(seg[127:130]) + list(
             rng.choice(seg, size=min(64, len(seg)), replace=False))
     check_experts(run, rows)
+    check_gather_fusion(run)
     check_combine(run)
     toks = sorted(set(rng.choice(cfg.n, size=96, replace=False).tolist() + [0, cfg.n - 1]))
     check_layer(run, toks)

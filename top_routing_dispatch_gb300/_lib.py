@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
 SYMBOLS = (
     "moe_version", "moe_status_string", "moe_route_topk", "moe_layout_workspace_size",
     "moe_dispatch_layout", "moe_dispatch_layout_noalloc", "moe_permute", "moe_grouped_swiglu", "moe_expert_gemm1_swiglu",
-    "moe_expert_gemm2", "moe_combine",
+    "moe_expert_gemm1_swiglu_gather", "moe_expert_gemm2", "moe_combine",
     "moe_workspace_size", "moe_forward_microbatches", "moe_workspace_slot", "moe_check_status",
 )
 
@@ -55,6 +55,8 @@ def _declare(lib):
         "moe_grouped_swiglu": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                      _vp, _vp]),
         "moe_expert_gemm1_swiglu": (_st, [_desc_p, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp]),
+        "moe_expert_gemm1_swiglu_gather": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
+                                                 _vp, _vp]),
         "moe_expert_gemm2": (_st, [_desc_p, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp]),
         "moe_combine": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp]),
         "moe_workspace_size": (ctypes.c_size_t, [_desc_p]),

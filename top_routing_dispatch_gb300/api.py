@@ -111,6 +111,13 @@ def moe_expert_gemm1_swiglu(desc, x_perm, w13, offsets, h, sm_reserve=0, status_
            "moe_expert_gemm1_swiglu")
 
 
+def moe_expert_gemm1_swiglu_gather(desc, x, perm, w13, offsets, h, sm_reserve=0,
+                                   status_word=None, stream=None):
+    _check(_lib.load().moe_expert_gemm1_swiglu_gather(
+        ctypes.byref(desc), _p(x), _p(perm), _p(w13), _p(offsets), _p(h), int(sm_reserve),
+        _p(status_word), _stream(stream)), "moe_expert_gemm1_swiglu_gather")
+
+
 def moe_expert_gemm2(desc, h, w2, offsets, y_perm, sm_reserve=0, status_word=None, stream=None):
     _check(_lib.load().moe_expert_gemm2(ctypes.byref(desc), _p(h), _p(w2), _p(offsets),
                                         _p(y_perm), int(sm_reserve), _p(status_word),

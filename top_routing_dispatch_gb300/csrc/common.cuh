@@ -62,6 +62,9 @@ cudaError_t launch_combine(const Desc &d, const void *y_perm, const float *topk_
 cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
                             const int32_t *offsets, void *h, int sm_reserve, int32_t *status,
                             cudaStream_t s);
+cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *perm,
+                                   const void *w13, const int32_t *offsets, void *h,
+                                   int sm_reserve, int32_t *status, cudaStream_t s);
 cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const int32_t *offsets,
                             void *y_perm, int sm_reserve, int32_t *status, cudaStream_t s);
 cudaError_t launch_gemm1_simt(const Desc &d, const void *x_perm, const void *w13,

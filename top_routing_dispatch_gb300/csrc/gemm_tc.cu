@@ -41,9 +41,17 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;            // 8 KB: 64 n x 64 k
 constexpr int B_STAGE_BYTES = 4 * B_BOX_BYTES;      // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+// warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue; MODE 3 adds
+// warps 6-9, which gather the A rows with cp.async
 constexpr int NUM_THREADS = 192;
+// MODE 3 copies a tile's 128 A rows with 16-byte cp.async from GATHER_WARPS
+// extra warps (warps 6..9).
+constexpr int GATHER_WARPS = BM / 32;
+constexpr int threads_for(int mode) {
+  return mode == 3 ? NUM_THREADS + 32 * GATHER_WARPS : NUM_THREADS;
+}
 constexpr int TMEM_COLS = 512;                      // two 256-column accumulators
-constexpr int EPI_ROW_BYTES_ = 80, EPI_WARP_BYTES_ = 32 * EPI_ROW_BYTES_;
+constexpr int EPI_ROW_BYTES = 80, EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
 
 struct SmemTail {
   uint64_t full[STAGES];
@@ -57,7 +65,7 @@ struct SmemTail {
   int total_mtiles;
   int off[kMaxE + 1];
   int tp[kMaxE + 1];  // first m-tile of each expert (exclusive prefix)
-  alignas(16) uint8_t epi[4][EPI_WARP_BYTES_];  // per epilogue warp staging
+  alignas(16) uint8_t epi[4][EPI_WARP_BYTES];  // per epilogue warp staging
 };
 
 constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES +
@@ -103,6 +111,18 @@ __device__ __forceinline__ TileInfo decode_tile(const SmemTail &s, int t, int n_
   return ti;
 }
 
+// MODE 3: perm entry of tile row rr (0 past the segment: such rows are never
+// stored and read token 0), and the token it names
+__device__ __forceinline__ int tile_perm(const int32_t *__restrict__ perm, const TileInfo &ti,
+                                         int rr) {
+  return rr < ti.rows ? __ldg(perm + ti.row0 + rr) : 0;
+}
+__device__ __forceinline__ int perm_token(int f, int nK, int Kslots, bool &bad) {
+  if ((unsigned)f < (unsigned)nK) return f / Kslots;
+  bad = true;
+  return 0;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&v);
@@ -118,8 +138,6 @@ __device__ __forceinline__ float silu(float g) {
 // row) in shared memory, then stores them as whole 64-byte row segments, 8
 // rows per store instruction.  Rows are 80 B apart so that both the row-wise
 // writes and the segment-wise reads are (nearly) free of bank conflicts.
-constexpr int EPI_ROW_BYTES = 80;
-constexpr int EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
 
 __device__ __forceinline__ void store_tile_chunk(uint8_t *wbuf, const uint32_t (&pk)[16], int lane,
                                                  __nv_bfloat16 *out, size_t ld, int row0,
@@ -140,14 +158,20 @@ __device__ __forceinline__ void store_tile_chunk(uint8_t *wbuf, const uint32_t (
   __syncwarp();
 }
 
-// MODE 1: GEMM1 + SwiGLU (B = W13, out = h, n-tile = 128 h columns)
-// MODE 2: GEMM2          (B = W2,  out = y_perm, n-tile = 256 columns)
+// MODE 1: GEMM1 + SwiGLU (A = x_perm, B = W13, out = h, n-tile = 128 h columns)
+// MODE 2: GEMM2          (A = h,      B = W2,  out = y_perm, n-tile = 256 columns)
+// MODE 3: GEMM1 + SwiGLU with the permute fused into the A loads: the A rows of
+//         a tile are read straight from x (row perm[r] / K) by four gather
+//         warps with 16-byte cp.async, written in the same 128-byte swizzled
+//         layout the TMA produces; no x_perm exists.
 template <int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(threads_for(MODE), 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const int32_t *__restrict__ offsets, int E, int nK, int Kdim, int I,
-                           int Nout, __nv_bfloat16 *__restrict__ out, int32_t *status) {
+                           int Nout, __nv_bfloat16 *__restrict__ out, int32_t *status,
+                           const int32_t *__restrict__ perm, int Kslots,
+                           const __nv_bfloat16 *__restrict__ xg) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -156,12 +180,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   SmemTail &st = *reinterpret_cast<SmemTail *>(smem + STAGES * STAGE_BYTES);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles = MODE == 1 ? I / 128 : (Nout + UMMA_N - 1) / UMMA_N;
+  const int n_tiles = MODE != 2 ? I / 128 : (Nout + UMMA_N - 1) / UMMA_N;
   const int KB = Kdim / BK;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&st.full[s], 1);
+      // MODE 3: the TMA producer's arrive (with the B bytes) + one completion
+      // arrive per cp.async thread
+      ptx::mbar_init(&st.full[s], MODE == 3 ? 1 + 32 * GATHER_WARPS : 1);
       ptx::mbar_init(&st.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -219,13 +245,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             stop = true;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&st.full[stage], STAGE_BYTES);
-          ptx::tma_load_2d(smemA + stage * A_STAGE_BYTES, &tmA, &st.full[stage], kb * BK,
-                           ti.row0);
+          ptx::mbar_arrive_expect_tx(&st.full[stage], MODE == 3 ? B_STAGE_BYTES : STAGE_BYTES);
+          if (MODE != 3)
+            ptx::tma_load_2d(smemA + stage * A_STAGE_BYTES, &tmA, &st.full[stage], kb * BK,
+                             ti.row0);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             int ncol;
-            if (MODE == 1)
+            if (MODE != 2)
               ncol = (q < 2 ? 0 : I) + ti.nt * 128 + (q & 1) * 64;
             else
               ncol = ti.nt * UMMA_N + q * 64;
@@ -261,6 +288,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             stop = true;
             break;
           }
+          // MODE 3: A was written by cp.async (generic proxy); the barrier
+          // made it visible to this thread, the proxy fence makes it visible
+          // to the tensor cores' async-proxy reads issued below
+          if (MODE == 3) ptx::fence_proxy_async_smem();
           ptx::tc_fence_after();
           const uint32_t a0 = ptx::smem_u32(smemA + stage * A_STAGE_BYTES);
           const uint32_t b0 = ptx::smem_u32(smemB + stage * B_STAGE_BYTES);
@@ -287,10 +318,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mma_commit(&st.drain);
       ptx::mbar_wait(&st.drain, 0);
     }
-  } else {
+  } else if (warp < 6) {
     // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
     const int q = warp & 3;
-    const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -302,7 +332,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int wrows = ti.rows - q * 32;
       const int wrow0 = ti.row0 + q * 32;
       uint8_t *wbuf = st.epi[q];
-      if (MODE == 1) {
+      if (MODE != 2) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t g[32], u[32];
@@ -339,6 +369,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+  } else if (MODE == 3) {
+    // cp.async gatherers: warp g fills tile rows [32g, 32g + 32).  Lane =
+    // 8 * sub + chunk moves 16-byte chunk `chunk` of rows 32g + 4i + sub
+    // (i = 0..7), so one warp instruction copies four whole 128-byte row
+    // segments.  The chunk lands where the TMA's 128-byte swizzle puts it:
+    // chunk c of row r at r * 128 + ((c ^ (r % 8)) * 16).  Every thread's
+    // copies of a stage end in a completion arrive on that stage's full
+    // barrier.  Perm entries of the next tile are loaded while the current
+    // tile streams.
+    const int g = warp - 6;
+    const int sub = lane >> 3, chunk = lane & 7;
+    const uint32_t a_base = ptx::smem_u32(smemA);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool bad = false;
+    int fnext[8];
+    {
+      const TileInfo t0 = decode_tile(st, blockIdx.x, n_tiles, E);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) fnext[i] = tile_perm(perm, t0, g * 32 + i * 4 + sub);
+    }
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const __nv_bfloat16 *src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        src[i] = xg + (size_t)perm_token(fnext[i], nK, Kslots, bad) * Kdim + chunk * 8;
+      if (t + (int)gridDim.x < total) {
+        const TileInfo tn = decode_tile(st, t + gridDim.x, n_tiles, E);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) fnext[i] = tile_perm(perm, tn, g * 32 + i * 4 + sub);
+      }
+      bool stop = false;
+      for (int kb = 0; kb < KB; ++kb) {
+        int ok = 1;
+        if (lane == 0) ok = wait_or_abort(&st.empty[stage], phase ^ 1u, abort_flag, status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          stop = true;
+          break;
+        }
+        const uint32_t sb = a_base + stage * A_STAGE_BYTES;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = g * 32 + i * 4 + sub;
+          ptx::cp_async_cg16(sb + rr * 128 + ((chunk ^ (rr & 7)) << 4), src[i] + kb * BK);
+        }
+        ptx::cp_async_arrive_noinc(&st.full[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (stop) break;
+    }
+    ptx::cp_async_wait<0>();  // no copy stays in flight
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(status, MOE_DEV_BAD_LAYOUT);
   }
 
   ptx::tc_fence_before();
@@ -431,7 +517,22 @@ cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
   if (e != cudaSuccess) return e;
   grouped_gemm_tc_kernel<1><<<gemm_grid(sm_reserve), NUM_THREADS, SMEM_BYTES, s>>>(
       mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I, reinterpret_cast<__nv_bfloat16 *>(h),
-      status);
+      status, nullptr, 0, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *perm,
+                                   const void *w13, const int32_t *offsets, void *h,
+                                   int sm_reserve, int32_t *status, cudaStream_t s) {
+  const long long nK = d.nK();
+  if (nK == 0) return cudaSuccess;
+  CUtensorMap mB;  // A is gathered with cp.async: no tensor map for x
+  if (!make_map_3d(&mB, w13, 2ull * d.I, d.H, d.E, 64, BK)) return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr<3>();
+  if (e != cudaSuccess) return e;
+  grouped_gemm_tc_kernel<3><<<gemm_grid(sm_reserve), threads_for(3), SMEM_BYTES, s>>>(
+      mB, mB, offsets, d.E, (int)nK, d.H, d.I, d.I, reinterpret_cast<__nv_bfloat16 *>(h),
+      status, perm, d.K, reinterpret_cast<const __nv_bfloat16 *>(x));
   return cudaGetLastError();
 }
 
@@ -446,7 +547,7 @@ cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const 
   if (e != cudaSuccess) return e;
   grouped_gemm_tc_kernel<2><<<gemm_grid(sm_reserve), NUM_THREADS, SMEM_BYTES, s>>>(
       mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H, reinterpret_cast<__nv_bfloat16 *>(y_perm),
-      status);
+      status, nullptr, 0, nullptr);
   return cudaGetLastError();
 }
 

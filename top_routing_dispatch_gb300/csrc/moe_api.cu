@@ -208,6 +208,23 @@ moe_status_t moe_expert_gemm1_swiglu(const moe_layer_desc_t *desc, const void *x
                             : launch_gemm1_simt(d, x_perm, w13, offsets, h, status_word, stream));
 }
 
+moe_status_t moe_expert_gemm1_swiglu_gather(const moe_layer_desc_t *desc, const void *x,
+                                            const int32_t *perm, const void *w13,
+                                            const int32_t *offsets, void *h, int sm_reserve,
+                                            int32_t *status_word, moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  if (!d.bf16) return MOE_ERR_UNSUPPORTED;
+  st = check_gemm_shape(d);
+  if (st != MOE_OK) return st;
+  if (d.nK() == 0) return MOE_OK;
+  if (!x || !perm || !w13 || !offsets || !h || sm_reserve < 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(h)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_gemm1_tc_gather(d, x, perm, w13, offsets, h, sm_reserve, status_word, stream));
+}
+
 moe_status_t moe_expert_gemm2(const moe_layer_desc_t *desc, const void *h, const void *w2,
                               const int32_t *offsets, void *y_perm, int sm_reserve,
                               int32_t *status_word, moe_stream_t stream) {
