@@ -189,8 +189,8 @@ moe_status_t moe_expert_gemm1_swiglu(const moe_layer_desc_t *desc, const void *x
 /*
  * GEMM1 + SwiGLU with the permute fused into it (bf16 layers only): the A
  * rows of expert e's segment are read straight from x, row r being token
- * perm[r] / K, by tensor-memory-accelerator gathers of four rows at a time,
- * so x_perm is never written.  The gather of Algorithm 2 step 7 and step 8 in
+ * perm[r] / K, by 16-byte cp.async copies from four gathering warps, so
+ * x_perm is never written.  The gather of Algorithm 2 step 7 and step 8 in
  * one pass: the permute folded into the expert GEMM, as HybridEP's
  * dispatch_with_permute (DModel notes "0. goin", §2.4) and FLUX/COMET's
  * scatter-into-grouped-GEMM ("大模型系统中的通算融合", §4.2.4) do.  Results
@@ -260,6 +260,40 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
  * argument.  No device access.
  */
 void *moe_workspace_slot(const moe_layer_desc_t *desc, void *ws, int mb, int which);
+
+/*
+ * Device bytes moe_forward_host needs: one layer workspace and two staging
+ * slots (x and y of one call each).  0 for an invalid descriptor.
+ */
+size_t moe_host_workspace_size(const moe_layer_desc_t *desc);
+
+/*
+ * The whole layer (Algorithm 2, as moe_forward_microbatches with one
+ * micro-batch) on host buffers, with the copies of consecutive calls
+ * overlapped with the layer of their neighbours: the input-copy and
+ * output-copy stages of a serving loop around the layer.
+ *   x_host, y_host: (n,H) dtype in page-locked host memory (cudaHostAlloc or
+ *   cudaHostRegister; pageable memory turns the copies synchronous).
+ *   ws: moe_host_workspace_size(desc) bytes of device memory, 256-byte
+ *   aligned, kept for the whole sequence of calls.
+ *   call: the caller's running call number (>= 0); consecutive calls must
+ *   alternate its parity, which selects the staging slot.
+ *   copy_in / copy_out: streams for the host-to-device and device-to-host
+ *   copies (NULL: `compute` carries them and nothing overlaps).
+ * Per call: copy_in waits until the layer of the previous call on the same
+ * slot has finished, copies x_host into the slot; compute waits for that copy
+ * and for the slot's previous copy-out, runs the layer; copy_out waits for the
+ * layer and copies y back to y_host.  y_host is complete once copy_out has
+ * passed the work this call enqueued (record an event on copy_out after the
+ * call, or synchronise copy_out).  The host never blocks.  Results are
+ * bitwise those of moe_forward_microbatches on the same input.
+ *   status_word: as for moe_forward_microbatches (NULL: a word inside ws).
+ */
+moe_status_t moe_forward_host(const moe_layer_desc_t *desc, const void *x_host,
+                              const void *w_gate, const float *bias, const void *w13,
+                              const void *w2, void *y_host, void *ws, size_t ws_bytes,
+                              long long call, int32_t *status_word, moe_stream_t compute,
+                              moe_stream_t copy_in, moe_stream_t copy_out);
 
 /*
  * Blocks until `stream` is idle, then reads *status_word and maps it to

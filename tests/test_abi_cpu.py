@@ -71,8 +71,11 @@ def test_workspace_sizes(lib):
     assert ws >= nK * 2048 * 2 * 2 + nK * 1024 * 2
     assert ws % 256 == 0
     lw = lib.moe_layout_workspace_size(ctypes.byref(d))
-    assert lw == 2 * ((nK + 2047) // 2048) * 65 * 4
+    assert lw == ((nK + 2047) // 2048) * 65 * 4      # one histogram per 2048-pair chunk
+    hw = lib.moe_host_workspace_size(ctypes.byref(d))
+    assert hw == ws + 4 * 4096 * 2048 * 2             # two staging slots of x and y
     assert lib.moe_workspace_size(ctypes.byref(_desc(E=0))) == 0
+    assert lib.moe_host_workspace_size(ctypes.byref(_desc(E=0))) == 0
     assert lib.moe_workspace_size(None) == 0
 
 
@@ -152,3 +155,28 @@ def test_forward_microbatches_argument_checks(lib):
                                       ctypes.c_void_p(256), ctypes.c_void_p(256), xs,
                                       ctypes.c_void_p(1 << 20), 1 << 30, 0, nullp, nullp, nullp)
     assert st == 1
+
+
+@needs_nvcc
+def test_forward_host_argument_checks(lib):
+    """Checks that return before any CUDA call (no GPU needed)."""
+    d = _desc(n=64, H=256, I=128, E=8, K=2)
+    nullp = ctypes.c_void_p(None)
+    need = lib.moe_host_workspace_size(ctypes.byref(d))
+    assert need > 0 and need % 256 == 0
+    ws = ctypes.c_void_p(1 << 20)
+    fake = ctypes.c_void_p(1 << 12)  # never dereferenced: every call below fails first
+
+    def call(**kw):
+        a = dict(x=fake, wg=fake, w13=fake, w2=fake, y=fake, ws=ws, nbytes=need, call=0, dd=d)
+        a.update(kw)
+        return lib.moe_forward_host(ctypes.byref(a["dd"]), a["x"], a["wg"], nullp, a["w13"],
+                                    a["w2"], a["y"], a["ws"], a["nbytes"], a["call"], nullp,
+                                    nullp, nullp, nullp)
+    assert call(ws=nullp) == 1                                  # MOE_ERR_INVALID_ARG
+    assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == 1        # ws not 256-byte aligned
+    assert call(call=-1) == 1
+    assert call(w13=nullp) == 1
+    assert call(nbytes=need - 1) == 3                           # MOE_ERR_WORKSPACE
+    assert call(dd=_desc(n=64, H=256, I=100, E=8, K=2)) == 2    # bf16 GEMM needs I % 128
+    assert call(dd=_desc(n=64, H=256, I=128, E=8, K=2), x=nullp) == 1

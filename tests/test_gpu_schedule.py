@@ -113,8 +113,11 @@ def test_layout_printed_example():
     assert perm.tolist() == [3, 6, 9, 0, 4, 10, 1, 7, 11, 2, 5, 8]
 
 
+# n*K <= 65536 runs the single-CTA layout, above it the three-kernel layout
 @pytest.mark.parametrize("n,E,K,hot", [(5000, 64, 8, False), (3001, 256, 8, True),
-                                       (4096, 1, 1, False), (1, 7, 3, False)])
+                                       (4096, 1, 1, False), (1, 7, 3, False),
+                                       (8192, 64, 8, False), (8193, 64, 8, False),
+                                       (20000, 256, 8, True)])
 def test_layout_edge_shapes(n, E, K, hot):
     g = torch.Generator(device="cpu")
     g.manual_seed(n * 31 + E)
@@ -139,3 +142,29 @@ def test_layout_bad_ids_flagged_and_perm_stays_a_permutation():
     assert offsets[-1] == 5                       # five valid pairs
     assert counts.tolist() == [1, 1, 2, 1]
     assert np.array_equal(inv[perm], np.arange(8))
+
+
+@pytest.mark.parametrize("n", [3000, 9000])
+def test_layout_bad_ids_both_paths(n):
+    """Invalid ids on the single-CTA (n*K <= 65536) and the multi-block path:
+    flagged, valid pairs laid out as the oracle lays out the valid subset,
+    invalid pairs after them in ascending flat index."""
+    E, K = 16, 8
+    g = torch.Generator(device="cpu")
+    g.manual_seed(n)
+    idx = torch.stack([torch.randperm(E, generator=g)[:K] for _ in range(n)]).to(torch.int32)
+    bad = torch.rand(idx.shape, generator=g) < 0.01
+    idx[bad] = torch.where(torch.rand(idx.shape, generator=g)[bad] < 0.5, -1, E + 3).to(torch.int32)
+    desc = M.make_desc(n, 64, 128, E, K, "bf16", False)
+    st, counts, offsets, perm, inv = _layout(desc, idx.cuda())
+    assert st == 4  # MOE_ERR_BAD_ROUTING
+    flat = idx.numpy().reshape(-1)
+    ok = (flat >= 0) & (flat < E)
+    nv = int(ok.sum())
+    assert offsets[-1] == nv
+    assert counts.tolist() == np.bincount(flat[ok], minlength=E).tolist()
+    valid_f = np.where(ok)[0]
+    order = valid_f[np.argsort(flat[ok], kind="stable")]
+    assert np.array_equal(perm[:nv], order)
+    assert np.array_equal(perm[nv:], np.where(~ok)[0])
+    assert np.array_equal(inv[perm], np.arange(n * K))

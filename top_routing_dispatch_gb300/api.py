@@ -146,6 +146,20 @@ def moe_forward_microbatches(desc, xs, w_gate, bias, w13, w2, ys, ws, sm_reserve
         "moe_forward_microbatches")
 
 
+def moe_host_workspace_size(desc) -> int:
+    return int(_lib.load().moe_host_workspace_size(ctypes.byref(desc)))
+
+
+def moe_forward_host(desc, x_host, w_gate, bias, w13, w2, y_host, ws, call, status_word=None,
+                     compute=None, copy_in=None, copy_out=None):
+    nbytes = ws.numel() * ws.element_size()
+    opt = lambda s: _stream(s) if s is not None else ctypes.c_void_p(None)
+    _check(_lib.load().moe_forward_host(
+        ctypes.byref(desc), _p(x_host), _p(w_gate), _p(bias), _p(w13), _p(w2), _p(y_host),
+        _p(ws), nbytes, int(call), _p(status_word), _stream(compute), opt(copy_in),
+        opt(copy_out)), "moe_forward_host")
+
+
 def moe_workspace_slot(desc, ws, mb, which) -> int:
     if isinstance(which, str):
         which = SLOT[which]
@@ -212,3 +226,30 @@ class MoELayer:
 
     def check(self, stream=None):
         _check(moe_check_status(self.status, stream), "device status")
+
+
+class HostPipeline:
+    """moe_forward_host over one staging workspace: each call enqueues the copy
+    of a pinned host x in, the layer, and the copy of y out, on three streams,
+    so consecutive calls overlap their copies with their neighbours' layers.
+    y_host of a call is final after `synchronize()` (or once an event recorded
+    on `copy_out` after the call has completed)."""
+
+    def __init__(self, layer: MoELayer, compute=None, copy_in=None, copy_out=None):
+        dev = layer.w13.device
+        self.layer = layer
+        self.ws = torch.empty(moe_host_workspace_size(layer.desc), dtype=torch.uint8, device=dev)
+        self.compute = compute if compute is not None else torch.cuda.current_stream(dev)
+        self.copy_in = copy_in if copy_in is not None else torch.cuda.Stream(device=dev)
+        self.copy_out = copy_out if copy_out is not None else torch.cuda.Stream(device=dev)
+        self.calls = 0
+
+    def __call__(self, x_host, y_host):
+        L = self.layer
+        moe_forward_host(L.desc, x_host, L.w_gate, L.bias, L.w13, L.w2, y_host, self.ws,
+                         self.calls, L.status, self.compute, self.copy_in, self.copy_out)
+        self.calls += 1
+        return y_host
+
+    def synchronize(self):
+        self.copy_out.synchronize()

@@ -4,15 +4,13 @@
 // n_e and sets I_e) and §2.3 (moe_align_block_size: pairs sorted by expert,
 // ascending flat index inside an expert, as in its worked example).
 //
-// Three integer-only kernels, so the result is deterministic:
-//  1. layout_count:   each block histograms a chunk of CH pairs (+1 bucket for
-//                     ids outside [0, E)).
-//  2. layout_scan:    one block turns the per-chunk histograms into counts,
-//                     offsets and the first output position of every
-//                     (chunk, expert).
-//  3. layout_scatter: each warp walks its 256-pair slice in order; pairs of
-//                     one expert inside a 32-wide step are ranked with
-//                     __match_any_sync, so order within an expert follows f.
+// Two integer-only kernels, so the result is deterministic:
+//  1. layout_count:        each block histograms a chunk of CH pairs (+1
+//                          bucket for ids outside [0, E)).
+//  2. layout_scan_scatter: each block scans the per-chunk histograms itself
+//                          (counts, offsets, its chunk's first position per
+//                          expert), then each warp walks its 256-pair slice
+//                          in order and scatters it stably.
 #include "common.cuh"
 
 namespace moe {
@@ -43,67 +41,81 @@ __global__ void __launch_bounds__(LT) layout_count(const int32_t *__restrict__ i
   for (int c = threadIdx.x; c <= E; c += LT) cnt[(size_t)blockIdx.x * (E + 1) + c] = hist[c];
 }
 
-__global__ void __launch_bounds__(LT) layout_scan(const int32_t *__restrict__ cnt, int nb, int E,
-                                                  int32_t *__restrict__ counts,
-                                                  int32_t *__restrict__ offsets,
-                                                  int32_t *__restrict__ base) {
+// Scan and scatter.  Every block reads the per-chunk histograms, forms the
+// bucket totals, their exclusive scan and the first position of each bucket
+// inside its own chunk (block 0 also writes counts and offsets).  Each warp
+// then counts its 256-pair slice, takes running positions after the earlier
+// warps of the block, and re-walks the slice in order: inside a 32-pair step
+// the lanes holding one expert find each other through a per-warp bit mask
+// per expert (atomicOr of the lane bit), a pair's rank is the number of lower
+// lanes with its expert, so the order inside an expert follows the flat index.
+__global__ void __launch_bounds__(LT) layout_scan_scatter(const int32_t *__restrict__ idx,
+                                                          long long nK, int E, int nb,
+                                                          const int32_t *__restrict__ cnt,
+                                                          int32_t *__restrict__ counts,
+                                                          int32_t *__restrict__ offsets,
+                                                          int32_t *__restrict__ perm,
+                                                          int32_t *__restrict__ inv_perm) {
   __shared__ int tot[kMaxE + 1];
-  __shared__ int start[kMaxE + 1];
-  for (int c = threadIdx.x; c <= E; c += LT) {
-    int s = 0;
-    for (int b = 0; b < nb; ++b) s += cnt[(size_t)b * (E + 1) + c];
-    tot[c] = s;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int c = 0; c <= E; ++c) {
-      start[c] = run;
-      run += tot[c];
-    }
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c <= E; c += LT) {
-    if (c < E) {
-      counts[c] = tot[c];
-      offsets[c] = start[c];
-    } else {
-      offsets[E] = start[E];  // pairs with a valid id; invalid ones follow
-    }
-    int run = start[c];
-    for (int b = 0; b < nb; ++b) {
-      base[(size_t)b * (E + 1) + c] = run;
-      run += cnt[(size_t)b * (E + 1) + c];
-    }
-  }
-}
-
-__global__ void __launch_bounds__(LT) layout_scatter(const int32_t *__restrict__ idx, long long nK,
-                                                     int E, const int32_t *__restrict__ base,
-                                                     int32_t *__restrict__ perm,
-                                                     int32_t *__restrict__ inv_perm) {
+  __shared__ int pre[kMaxE + 1];
   __shared__ int run[LW][kMaxE + 1];
+  __shared__ unsigned mask[LW][kMaxE + 1];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const long long slice0 = (long long)blockIdx.x * CH + (long long)w * SLICE;
-  for (int c = lane; c <= E; c += 32) run[w][c] = 0;
-  __syncwarp();
-  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int c = threadIdx.x; c <= E; c += LT) {
+    int t = 0, p = 0;
+    for (int b = 0; b < nb; ++b) {
+      const int v = cnt[(size_t)b * (E + 1) + c];
+      t += v;
+      p += b < (int)blockIdx.x ? v : 0;
+    }
+    tot[c] = t;
+    pre[c] = p;
+  }
+  for (int c = lane; c <= E; c += 32) {
+    run[w][c] = 0;
+    mask[w][c] = 0u;
+  }
+  __syncthreads();
+  // exclusive scan of the bucket totals (warp 0, 32 buckets per step)
+  if (w == 0) {
+    int carry = 0;
+    for (int c0 = 0; c0 <= E; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c <= E ? tot[c] : 0;
+      int inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (c <= E) {
+        const int start = carry + inc - v;
+        if (blockIdx.x == 0) {
+          if (c < E) {
+            counts[c] = v;
+            offsets[c] = start;
+          } else {
+            offsets[E] = start;  // pairs with a valid id; invalid ones follow
+          }
+        }
+        pre[c] += start;  // first position of bucket c in this block's chunk
+      }
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+  }
   // pass 1: this warp's histogram
   for (int s = 0; s < SLICE; s += 32) {
     const long long f = slice0 + s + lane;
-    int key = -1;
     if (f < nK) {
       const int e = idx[f];
-      key = (unsigned)e < (unsigned)E ? e : E;
+      atomicAdd(&run[w][(unsigned)e < (unsigned)E ? e : E], 1);
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    if (key >= 0 && (peers & lt_mask) == 0) run[w][key] += __popc(peers);
-    __syncwarp();
   }
   __syncthreads();
   // running positions: chunk base + counts of the earlier warps of this block
   for (int c = threadIdx.x; c <= E; c += LT) {
-    int r = base[(size_t)blockIdx.x * (E + 1) + c];
+    int r = pre[c];
     for (int ww = 0; ww < LW; ++ww) {
       const int h = run[ww][c];
       run[ww][c] = r;
@@ -112,6 +124,7 @@ __global__ void __launch_bounds__(LT) layout_scatter(const int32_t *__restrict__
   }
   __syncthreads();
   // pass 2: stable scatter
+  const unsigned lt_mask = (1u << lane) - 1u;
   for (int s = 0; s < SLICE; s += 32) {
     const long long f = slice0 + s + lane;
     int key = -1;
@@ -119,14 +132,20 @@ __global__ void __launch_bounds__(LT) layout_scatter(const int32_t *__restrict__
       const int e = idx[f];
       key = (unsigned)e < (unsigned)E ? e : E;
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (key >= 0) atomicOr(&mask[w][key], 1u << lane);
+    __syncwarp();
+    const unsigned peers = key >= 0 ? mask[w][key] : 0u;
+    __syncwarp();
     if (key >= 0) {
       const int pos = run[w][key] + __popc(peers & lt_mask);
       perm[pos] = (int32_t)f;
       inv_perm[f] = pos;
     }
     __syncwarp();
-    if (key >= 0 && (peers & lt_mask) == 0) run[w][key] += __popc(peers);
+    if (key >= 0 && (peers & lt_mask) == 0) {  // the lowest lane of the expert
+      run[w][key] += __popc(peers);
+      mask[w][key] = 0u;
+    }
     __syncwarp();
   }
 }
@@ -137,7 +156,7 @@ inline int num_chunks(long long nK) { return (int)((nK + CH - 1) / CH); }
 
 size_t layout_ws_bytes(const Desc &d) {
   const int nb = num_chunks(d.nK()) > 0 ? num_chunks(d.nK()) : 1;
-  return 2 * (size_t)nb * (d.E + 1) * sizeof(int32_t);
+  return (size_t)nb * (d.E + 1) * sizeof(int32_t);
 }
 
 cudaError_t launch_layout(const Desc &d, const int32_t *topk_idx, int32_t *counts,
@@ -151,10 +170,9 @@ cudaError_t launch_layout(const Desc &d, const int32_t *topk_idx, int32_t *count
     return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d.E + 1), s);
   }
   int32_t *cnt = reinterpret_cast<int32_t *>(ws);
-  int32_t *base = cnt + (size_t)nb * (d.E + 1);
   layout_count<<<nb, LT, 0, s>>>(topk_idx, nK, d.E, cnt, status);
-  layout_scan<<<1, LT, 0, s>>>(cnt, nb, d.E, counts, offsets, base);
-  layout_scatter<<<nb, LT, 0, s>>>(topk_idx, nK, d.E, base, perm, inv_perm);
+  layout_scan_scatter<<<nb, LT, 0, s>>>(topk_idx, nK, d.E, nb, cnt, counts, offsets, perm,
+                                        inv_perm);
   return cudaGetLastError();
 }
 

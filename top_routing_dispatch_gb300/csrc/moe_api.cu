@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -106,6 +107,14 @@ struct EventPool {
 };
 EventPool g_pools[64];
 std::mutex g_pool_mu;
+
+// events of one host pipeline (one workspace): per staging slot, x copied in,
+// layer finished (x read, y written), y copied out
+struct HostEvents {
+  cudaEvent_t in[2], layer[2], out[2];
+};
+std::map<std::pair<int, const void *>, HostEvents> g_host_events;
+std::mutex g_host_mu;
 
 }  // namespace
 }  // namespace moe
@@ -359,6 +368,73 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
   if (e == cudaSuccess) e = back(num_mb - 1, sd);
   if (e == cudaSuccess) e = cudaEventRecord(ev_done, sd);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, ev_done, 0);
+  return cuda_status(e);
+}
+
+size_t moe_host_workspace_size(const moe_layer_desc_t *desc) {
+  Desc d;
+  if (check_desc(desc, &d) != MOE_OK) return 0;
+  const size_t io = up((size_t)d.n * d.H * elem_bytes(d));
+  return mb_bytes(d) + 4 * io;
+}
+
+moe_status_t moe_forward_host(const moe_layer_desc_t *desc, const void *x_host,
+                              const void *w_gate, const float *bias, const void *w13,
+                              const void *w2, void *y_host, void *ws, size_t ws_bytes,
+                              long long call, int32_t *status_word, moe_stream_t compute,
+                              moe_stream_t copy_in, moe_stream_t copy_out) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  st = check_gemm_shape(d);
+  if (st != MOE_OK) return st;
+  if (!ws || !w_gate || !w13 || !w2 || call < 0) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_host_workspace_size(desc)) return MOE_ERR_WORKSPACE;
+  if (d.n == 0) return MOE_OK;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)d.n * d.H * elem_bytes(d);
+  const size_t io = up(bytes);
+  const int slot = (int)(call & 1);
+  uint8_t *stage = reinterpret_cast<uint8_t *>(ws) + mb_bytes(d) + (size_t)slot * 2 * io;
+  void *xs = stage, *ys = stage + io;
+  cudaStream_t sc = compute;
+  cudaStream_t si = copy_in ? copy_in : sc;
+  cudaStream_t so = copy_out ? copy_out : sc;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  auto it = g_host_events.find({dev, ws});
+  if (it == g_host_events.end()) {
+    HostEvents h;
+    for (int k = 0; k < 2; ++k) {
+      if (cudaEventCreateWithFlags(&h.in[k], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&h.layer[k], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&h.out[k], cudaEventDisableTiming) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
+    it = g_host_events.emplace(std::make_pair(dev, (const void *)ws), h).first;
+  }
+  HostEvents &ev = it->second;
+  // copy in once the slot's previous layer has read its x
+  cudaError_t e = cudaStreamWaitEvent(si, ev.layer[slot], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, si);
+  if (e == cudaSuccess) e = cudaEventRecord(ev.in[slot], si);
+  // the layer, once x is in and the slot's previous y has been copied out
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, ev.in[slot], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, ev.out[slot], 0);
+  if (e != cudaSuccess) return cuda_status(e);
+  const void *xv[1] = {xs};
+  void *yv[1] = {ys};
+  st = moe_forward_microbatches(desc, 1, xv, w_gate, bias, w13, w2, yv, ws, mb_bytes(d), 0,
+                                status_word, sc, nullptr);
+  if (st != MOE_OK) return st;
+  e = cudaEventRecord(ev.layer[slot], sc);
+  // copy out once the layer is done
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(so, ev.layer[slot], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, so);
+  if (e == cudaSuccess) e = cudaEventRecord(ev.out[slot], so);
   return cuda_status(e);
 }
 

@@ -37,8 +37,7 @@ constexpr int RT_THREADS = 64 + RT_EPI_THREADS;       // 576
 constexpr int RT_A_BYTES = RT_BM * RT_BK * 2;         // 16 KB
 constexpr int RT_BOX_BYTES = 64 * RT_BK * 2;          // 8 KB: 64 experts x 64 k
 constexpr int RT_PIPE_BYTES = 168 * 1024;             // operand stages
-constexpr int RS_SLOTS = 256;                         // candidate slots per rescoring sweep
-constexpr int RS_MAXF = 16;                           // flagged tokens per sweep
+constexpr int RR_THREADS = 256;                       // rescoring kernel: threads per CTA
 
 struct RtTail {
   uint64_t full[RT_MAX_STAGES];
@@ -53,27 +52,11 @@ struct RtTail {
 
 template <int KM>
 struct EpiSmem {
-  union {
-    struct {                             // selection: one list per (slice, token)
-      float pv[RT_SLICES][RT_BM][KM + 1];  // per-slice top K+1 values
-      int pi[RT_SLICES][RT_BM][KM + 1];    // ... and expert ids
-    } sel;
-    struct {                             // rescoring of the tile's flagged tokens
-      float phi[RT_EPI_THREADS];           // per-thread partial sums
-      float plo[RT_EPI_THREADS];
-      float chi[RS_SLOTS], clo[RS_SLOTS];  // per slot: summed over row groups + bias
-      int cexp[RS_SLOTS];                  // expert of each slot
-      int ctok[RS_SLOTS];                  // token (index in the sweep) of each slot
-      int tbase[RS_MAXF + 1];              // first slot of each token
-      int S, nb;                           // slots and tokens of the sweep
-    } res;
-  } u;
+  float pv[RT_SLICES][RT_BM][KM + 1];  // per-slice top K+1 values
+  int pi[RT_SLICES][RT_BM][KM + 1];    // ... and expert ids
   float pm[RT_SLICES][RT_BM];          // per-slice max
   float ps[RT_SLICES][RT_BM];          // per-slice sum of exp(l - slice max)
   int stop;                            // set by an epilogue thread whose wait gave up
-  int nflag;                           // flagged tokens of the tile
-  int ftok[RT_BM];
-  float fm[RT_BM], fS[RT_BM], fvK[RT_BM];
 };
 
 __host__ __device__ inline int rt_stages(int E) {
@@ -118,140 +101,221 @@ __device__ __forceinline__ bool ranks_above(float v, int e, float w, int f) {
   return v > w || (v == w && e < f);
 }
 
-// Rescoring of the tile's flagged tokens by the 512 epilogue threads.  A
-// sweep takes up to 16 flagged tokens and their candidate experts (within tau
-// of the token's K-th float32 logit), one slot per (token, candidate), at most
-// 256 slots.  Thread et serves slot et mod Sp (Sp = slots rounded up to a
-// power of two) over the rows h congruent to et / Sp modulo 512 / Sp,
-// accumulating x[t,h] * W_gate[h,e] in double-float (four interleaved
-// accumulators).  The 32 threads of a warp serve consecutive slots of the same
-// row, so their W_gate loads fall in the few sectors of that row.  The
-// partial sums are added in a fixed order, the bias is added, and one warp per
-// token keeps the K largest.
+// Exact TopK of the tokens the tile kernel flagged (topk_idx[t][0] == -1).
+// One CTA per flagged token (grid-stride over the tokens; each CTA first
+// collects its flagged tokens with one parallel pass over the markers).
+// Thread e ranks expert e among all E by float32 logit (larger first, ties to
+// the lower id); the rank K-1 expert gives the threshold, and the experts
+// within tau of it form the candidate list L (a prefix of that order), which
+// holds every expert that can be in the exact top K since the logits' error
+// is below tau / 2.  A position of L whose gap to a neighbour is below tau is
+// uncertain; every other position already holds the expert the exact order
+// puts there (neighbours tau apart cannot swap).  Only the uncertain experts
+// are rescored: x[t,:] . W_gate[:,e] in double-float (exact products,
+// error-free sums), thread j serving expert j mod Sp over the rows h congruent
+// to j / Sp modulo G = 256 / Sp; the G partial sums of an expert are added by
+// a butterfly inside each warp and then over the warps in order, and the bias
+// is added.  Each run of consecutive uncertain positions is re-sorted by those
+// values (larger first, ties to the lower id) and the first K of L are the
+// token's experts.  Weights: softmax of the float32 logits.
 template <int KM>
-__device__ __forceinline__ void rescore_tile(EpiSmem<KM> &ep, const float *__restrict__ bias_s,
-                                             const __nv_bfloat16 *__restrict__ x,
-                                             const __nv_bfloat16 *__restrict__ wg,
-                                             const float *__restrict__ logits,
-                                             int32_t *__restrict__ topk_idx,
-                                             float *__restrict__ topk_w, int H, int E, int norm,
-                                             float tau_rel, int ew, int lane, int et) {
+__global__ void __launch_bounds__(RR_THREADS)
+    router_rescore_kernel(const __nv_bfloat16 *__restrict__ x,
+                          const __nv_bfloat16 *__restrict__ wg, const float *__restrict__ bias,
+                          const float *__restrict__ logits, int32_t *__restrict__ topk_idx,
+                          float *__restrict__ topk_w, int n, int H, int E, int norm,
+                          float tau_rel) {
+  static_assert(RR_THREADS >= kMaxE, "one thread per expert");
   constexpr int K = KM;
-  auto &rs = ep.u.res;
-  const int nflag = ep.nflag;
-  for (int b0 = 0; b0 < nflag;) {
-    // slots of this sweep (warp 0), in ascending expert order per token
-    if (ew == 0) {
-      int total = 0, nb = 0;
-      for (int g = b0; g < nflag && nb < RS_MAXF; ++g) {
-        const int ft = ep.ftok[g];
-        const float thr = ep.fvK[g] - tau_rel * fmaxf(1.f, fabsf(ep.fm[g]));
-        int C = 0;
-        for (int j = 0; j < E / 32; ++j)
-          C += __popc(__ballot_sync(0xffffffffu, logits[(size_t)ft * E + lane + 32 * j] >= thr));
-        if (nb > 0 && total + C > RS_SLOTS) break;
-        int pos = total;
-        for (int j = 0; j < E / 32; ++j) {
-          const int e = lane + 32 * j;
-          const unsigned ball = __ballot_sync(0xffffffffu, logits[(size_t)ft * E + e] >= thr);
-          if (ball >> lane & 1u) {
-            const int sl = pos + __popc(ball & ((1u << lane) - 1u));
-            rs.cexp[sl] = e;
-            rs.ctok[sl] = nb;
-          }
-          pos += __popc(ball);
-        }
-        if (lane == 0) rs.tbase[nb] = total;
-        total += C;
-        ++nb;
-      }
-      if (lane == 0) {
-        rs.tbase[nb] = total;
-        rs.S = total;
-        rs.nb = nb;
-      }
+  constexpr int MAXT = 64;  // tokens one CTA inspects per pass
+  __shared__ float lg[kMaxE];
+  __shared__ float cv[kMaxE];   // L's float values, in rank order
+  __shared__ int ce[kMaxE];     // L's experts, in rank order
+  __shared__ int unc[kMaxE];    // position of L is uncertain
+  __shared__ int uslot[kMaxE];  // slot of an uncertain position
+  __shared__ int ue[kMaxE];     // expert of each slot
+  __shared__ float phi[RR_THREADS], plo[RR_THREADS];
+  __shared__ float fhi[kMaxE], flo[kMaxE];  // exact value of each slot
+  __shared__ int flagged[MAXT];
+  __shared__ int nfl, shU;
+  __shared__ float shM, shS, shThr, shTau;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  for (int t0 = blockIdx.x; t0 < n; t0 += gridDim.x * MAXT) {
+    // this pass's tokens t0 + i * gridDim.x, i < MAXT: collect the flagged ones
+    if (tid == 0) nfl = 0;
+    __syncthreads();
+    if (tid < MAXT) {
+      const long long t = (long long)t0 + (long long)tid * gridDim.x;
+      if (t < n && topk_idx[t * K] < 0) flagged[atomicAdd(&nfl, 1)] = (int)t;
     }
-    epi_bar();
-    const int S = rs.S, nb = rs.nb;
-    int Sp = 1;
-    while (Sp < S) Sp <<= 1;
-    const int G = RT_EPI_THREADS / Sp;  // row groups
-    const int s_id = et & (Sp - 1), g_id = et / Sp;
-    const bool active = s_id < S;
-    const int e_s = active ? rs.cexp[s_id] : 0;
-    const int f_s = active ? rs.ctok[s_id] : 0;
-    DF acc{0.f, 0.f};
-    if (active) {
-      const __nv_bfloat16 *xr = x + (size_t)ep.ftok[b0 + f_s] * H;
-      const __nv_bfloat16 *wc = wg + e_s;
-      DF a4[4] = {DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}};
-      int h = g_id;
-      for (; h + 7 * G < H; h += 8 * G) {
+    __syncthreads();
+    const int nf = nfl;
+    for (int q = 0; q < nf; ++q) {
+      const int t = flagged[q];
+      const bool ex = tid < E;  // this thread's expert e = tid
+      const float v = ex ? logits[(size_t)t * E + tid] : -INFINITY;
+      if (ex) lg[tid] = v;
+      __syncthreads();
+      int rk = 0;
+      if (ex) {
+#pragma unroll 4
+        for (int f = 0; f < E; ++f) rk += ranks_above(lg[f], f, v, tid);
+      }
+      if (warp == 0) {  // softmax statistics
+        float m = -INFINITY;
+        for (int e = lane; e < E; e += 32) m = fmaxf(m, lg[e]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float sm = 0.f;
+        for (int e = lane; e < E; e += 32) sm += expf(lg[e] - m);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+        if (lane == 0) {
+          shM = m;
+          shS = sm;
+          shTau = tau_rel * fmaxf(1.f, fabsf(m));
+        }
+      }
+      __syncthreads();
+      if (ex && rk == K - 1) shThr = v - shTau;
+      __syncthreads();
+      const float thr = shThr, tau = shTau;
+      const bool inL = ex && v >= thr;  // L = ranks 0 .. C-1
+      if (inL) {
+        cv[rk] = v;
+        ce[rk] = tid;
+      }
+      const int C = __syncthreads_count(inL);
+      if (tid < C)
+        unc[tid] = (tid > 0 && cv[tid - 1] - cv[tid] < tau) ||
+                   (tid + 1 < C && cv[tid] - cv[tid + 1] < tau);
+      __syncthreads();
+      if (warp == 0) {  // slots of the uncertain positions, in position order
+        int base = 0;
+        for (int p0 = 0; p0 < C; p0 += 32) {
+          const int p = p0 + lane;
+          const bool u = p < C && unc[p];
+          const unsigned b = __ballot_sync(0xffffffffu, u);
+          if (u) {
+            const int sl = base + __popc(b & ((1u << lane) - 1u));
+            uslot[p] = sl;
+            ue[sl] = ce[p];
+          }
+          base += __popc(b);
+        }
+        if (lane == 0) shU = base;
+      }
+      __syncthreads();
+      const int U = shU;
+      // double-float dot products of the uncertain experts
+      int Sp = 1;
+      while (Sp < U) Sp <<= 1;
+      const int G = RR_THREADS / Sp;
+      const int s_id = tid & (Sp - 1), g_id = tid / Sp;
+      DF acc{0.f, 0.f};
+      if (s_id < U) {
+        const __nv_bfloat16 *xr = x + (size_t)t * H;
+        const __nv_bfloat16 *wc = wg + ue[s_id];
+        const int nrows = (H - g_id + G - 1) / G;  // rows g_id + i * G, i < nrows
+        DF a4[4] = {DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}};
         float xv[8], wv[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          xv[u] = __bfloat162float(xr[h + u * G]);
-          wv[u] = __bfloat162float(wc[(size_t)(h + u * G) * E]);
+          const bool in = u < nrows;
+          const int h = g_id + u * G;
+          xv[u] = in ? __bfloat162float(xr[h]) : 0.f;
+          wv[u] = in ? __bfloat162float(wc[(size_t)h * E]) : 0.f;
         }
+        for (int i0 = 0; i0 < nrows; i0 += 8) {
+          float xn[8], wn[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) a4[u & 3] = df_add(a4[u & 3], two_prod(xv[u], wv[u]));
-      }
-      for (; h < H; h += G)
-        a4[0] = df_add(a4[0], two_prod(__bfloat162float(xr[h]), __bfloat162float(wc[(size_t)h * E])));
-      acc = df_add(df_add(a4[0], a4[1]), df_add(a4[2], a4[3]));
-    }
-    rs.phi[et] = acc.hi;
-    rs.plo[et] = acc.lo;
-    epi_bar();
-    for (int sl = et; sl < S; sl += RT_EPI_THREADS) {
-      DF sum{0.f, 0.f};
-      for (int g = 0; g < G; ++g) sum = df_add(sum, DF{rs.phi[g * Sp + sl], rs.plo[g * Sp + sl]});
-      const float bb = bias_s[rs.cexp[sl]];
-      sum = isinf(bb) ? DF{bb, 0.f} : df_add(sum, DF{bb, 0.f});
-      rs.chi[sl] = sum.hi;
-      rs.clo[sl] = sum.lo;
-    }
-    epi_bar();
-    // warp f keeps the K best of the sweep's token f
-    if (ew < nb && lane == 0) {
-      const int g = b0 + ew;
-      const int ft = ep.ftok[g];
-      DF lv[K];
-      int li[K];
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + 8 + u;
+            const bool in = i < nrows;
+            const int h = g_id + i * G;
+            xn[u] = in ? __bfloat162float(xr[h]) : 0.f;
+            wn[u] = in ? __bfloat162float(wc[(size_t)h * E]) : 0.f;
+          }
 #pragma unroll
-      for (int z = 0; z < K; ++z) {
-        lv[z] = DF{-INFINITY, 0.f};
-        li[z] = 0x7fffffff;
+          for (int u = 0; u < 8; ++u) a4[u & 3] = df_add(a4[u & 3], two_prod(xv[u], wv[u]));
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            xv[u] = xn[u];
+            wv[u] = wn[u];
+          }
+        }
+        acc = df_add(df_add(a4[0], a4[1]), df_add(a4[2], a4[3]));
       }
-      for (int sl = rs.tbase[ew]; sl < rs.tbase[ew + 1]; ++sl) {
-        DF cv{rs.chi[sl], rs.clo[sl]};
-        int ci = rs.cexp[sl];
+      // the G partial sums of each slot: butterfly over the lanes of a warp
+      // that serve the slot, then the warps in order
+      int ng = G;
+      if (Sp < 32) {
+        for (int o = Sp; o < 32; o <<= 1) {
+          const DF other{__shfl_xor_sync(0xffffffffu, acc.hi, o),
+                         __shfl_xor_sync(0xffffffffu, acc.lo, o)};
+          acc = df_add(acc, other);
+        }
+        if (lane < Sp) {
+          phi[warp * Sp + lane] = acc.hi;
+          plo[warp * Sp + lane] = acc.lo;
+        }
+        ng = RR_THREADS / 32;
+      } else {
+        phi[tid] = acc.hi;
+        plo[tid] = acc.lo;
+      }
+      __syncthreads();
+      if (tid < U) {
+        DF sum{0.f, 0.f};
+        for (int g = 0; g < ng; ++g) sum = df_add(sum, DF{phi[g * Sp + tid], plo[g * Sp + tid]});
+        const float bb = bias ? bias[ue[tid]] : 0.f;
+        sum = isinf(bb) ? DF{bb, 0.f} : df_add(sum, DF{bb, 0.f});
+        fhi[tid] = sum.hi;
+        flo[tid] = sum.lo;
+      }
+      __syncthreads();
+      // runs of uncertain positions re-sorted by the exact values; first K out
+      if (tid == 0) {
+        int out[K];
+        int k = 0;
+        for (int p = 0; p < C && k < K;) {
+          if (!unc[p]) {
+            out[k++] = ce[p++];
+            continue;
+          }
+          int r = p;
+          while (r < C && unc[r]) ++r;
+          for (int a = p + 1; a < r; ++a) {  // insertion sort of [p, r)
+            const int ea = ce[a], sa = uslot[a];
+            const DF va{fhi[sa], flo[sa]};
+            int b = a - 1;
+            while (b >= p && df_greater(va, ea, DF{fhi[uslot[b]], flo[uslot[b]]}, ce[b])) {
+              ce[b + 1] = ce[b];
+              uslot[b + 1] = uslot[b];
+              --b;
+            }
+            ce[b + 1] = ea;
+            uslot[b + 1] = sa;
+          }
+          for (int a = p; a < r && k < K; ++a) out[k++] = ce[a];
+          p = r;
+        }
+        float w[K];
+        float wsum = 0.f;
 #pragma unroll
         for (int z = 0; z < K; ++z) {
-          const bool gt = df_greater(cv, ci, lv[z], li[z]);
-          const DF tv = gt ? lv[z] : cv;
-          const int ti = gt ? li[z] : ci;
-          lv[z] = gt ? cv : lv[z];
-          li[z] = gt ? ci : li[z];
-          cv = tv;
-          ci = ti;
+          w[z] = expf(lg[out[z]] - shM) / shS;
+          wsum += w[z];
+        }
+#pragma unroll
+        for (int z = 0; z < K; ++z) {
+          topk_idx[(size_t)t * K + z] = out[z];
+          topk_w[(size_t)t * K + z] = norm ? w[z] / wsum : w[z];
         }
       }
-      float w[K];
-      float wsum = 0.f;
-#pragma unroll
-      for (int z = 0; z < K; ++z) {
-        w[z] = expf(logits[(size_t)ft * E + li[z]] - ep.fm[g]) / ep.fS[g];
-        wsum += w[z];
-      }
-#pragma unroll
-      for (int z = 0; z < K; ++z) {
-        topk_idx[(size_t)ft * K + z] = li[z];
-        topk_w[(size_t)ft * K + z] = norm ? w[z] / wsum : w[z];
-      }
+      __syncthreads();
     }
-    epi_bar();  // the slots and staging buffers are reused by the next sweep
-    b0 += nb;
   }
 }
 
@@ -259,7 +323,6 @@ template <int KM>
 __global__ void __launch_bounds__(RT_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW,
-                     const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ wg,
                      const float *__restrict__ bias, float *__restrict__ logits,
                      int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int n, int H,
                      int E, int norm, uint32_t idesc, uint32_t tmem_cols, int32_t *status) {
@@ -291,7 +354,6 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     }
     ptx::mbar_init(&st.drain, 1);
     st.abort_flag = 0;
-    ep.nflag = 0;
     ep.stop = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -382,7 +444,6 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     const int q = warp & 3;               // TMEM lane quarter this warp may read
     const int sl = ew >> 2;               // column slice 0..3
     const int r = q * 32 + lane;          // token row in the tile
-    const int et = ew * 32 + lane;        // 0..511
     const int cols = E / RT_SLICES;
     const int c0 = sl * cols;
     const float tau_rel = tie_margin_tc(H);
@@ -463,12 +524,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 
 #pragma unroll
       for (int j = 0; j <= K; ++j) {
-        ep.u.sel.pv[sl][r][j] = lv[j];
-        ep.u.sel.pi[sl][r][j] = li[j];
+        ep.pv[sl][r][j] = lv[j];
+        ep.pi[sl][r][j] = li[j];
       }
       ep.pm[sl][r] = m;
       ep.ps[sl][r] = ssum;
-      __threadfence_block();  // the logits rows are read back below
       epi_bar();
 
       // merge the four slices: one thread per token
@@ -478,17 +538,17 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         int h0 = 0, h1 = 0, h2 = 0, h3 = 0;
 #pragma unroll
         for (int j = 0; j <= K; ++j) {
-          float bv = h0 <= K ? ep.u.sel.pv[0][r][h0] : -INFINITY;
-          int bi = h0 <= K ? ep.u.sel.pi[0][r][h0] : 0x7fffffff;
+          float bv = h0 <= K ? ep.pv[0][r][h0] : -INFINITY;
+          int bi = h0 <= K ? ep.pi[0][r][h0] : 0x7fffffff;
           int bw = 0;
-          const float v1 = h1 <= K ? ep.u.sel.pv[1][r][h1] : -INFINITY;
-          const int i1 = h1 <= K ? ep.u.sel.pi[1][r][h1] : 0x7fffffff;
+          const float v1 = h1 <= K ? ep.pv[1][r][h1] : -INFINITY;
+          const int i1 = h1 <= K ? ep.pi[1][r][h1] : 0x7fffffff;
           if (ranks_above(v1, i1, bv, bi)) { bv = v1; bi = i1; bw = 1; }
-          const float v2 = h2 <= K ? ep.u.sel.pv[2][r][h2] : -INFINITY;
-          const int i2 = h2 <= K ? ep.u.sel.pi[2][r][h2] : 0x7fffffff;
+          const float v2 = h2 <= K ? ep.pv[2][r][h2] : -INFINITY;
+          const int i2 = h2 <= K ? ep.pi[2][r][h2] : 0x7fffffff;
           if (ranks_above(v2, i2, bv, bi)) { bv = v2; bi = i2; bw = 2; }
-          const float v3 = h3 <= K ? ep.u.sel.pv[3][r][h3] : -INFINITY;
-          const int i3 = h3 <= K ? ep.u.sel.pi[3][r][h3] : 0x7fffffff;
+          const float v3 = h3 <= K ? ep.pv[3][r][h3] : -INFINITY;
+          const int i3 = h3 <= K ? ep.pi[3][r][h3] : 0x7fffffff;
           if (ranks_above(v3, i3, bv, bi)) { bv = v3; bi = i3; bw = 3; }
           fv[j] = bv;
           fi[j] = bi;
@@ -522,20 +582,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
             topk_w[(size_t)tok * K + j] = norm ? w[j] / wsum : w[j];
           }
         } else {
-          const int slot = atomicAdd(&ep.nflag, 1);
-          ep.ftok[slot] = tok;
-          ep.fm[slot] = M;
-          ep.fS[slot] = S;
-          ep.fvK[slot] = fv[K - 1];
+          topk_idx[(size_t)tok * K] = -1;  // flagged: router_rescore_kernel decides
         }
       }
-      epi_bar();
-
-      // rescoring of the tile's flagged tokens (all 512 epilogue threads)
-      rescore_tile<KM>(ep, st.bias, x, wg, logits, topk_idx, topk_w, H, E, norm, tau_rel, ew, lane,
-                       et);
-      epi_bar();  // the rescoring lists alias the next tile's selection lists
-      if (et == 0) ep.nflag = 0;
+      epi_bar();  // the selection lists are reused by the next tile
     }
   }
 
@@ -602,19 +652,26 @@ cudaError_t launch_router_tc(const Desc &d, const void *x, const void *w_gate, c
   const uint32_t idesc = ptx::idesc_bf16_f32(RT_BM, d.E, false, true);
   const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
   const __nv_bfloat16 *wb = reinterpret_cast<const __nv_bfloat16 *>(w_gate);
-  auto run = [&](auto kernel, size_t smem_max, size_t smem) -> cudaError_t {
+  const int rgrid = d.n < 2 * sms ? d.n : 2 * sms;
+  const float tau_rel = tie_margin_tc(d.H);
+  // the tile kernel, then the exact rescoring of the tokens it flagged
+  auto run = [&](auto kernel, auto rescore, size_t smem_max, size_t smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem_max);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, RT_THREADS, smem, s>>>(mX, mW, xb, wb, bias, logits, topk_idx, topk_w, d.n,
-                                          d.H, d.E, d.norm ? 1 : 0, idesc, cols, status);
+    kernel<<<grid, RT_THREADS, smem, s>>>(mX, mW, bias, logits, topk_idx, topk_w, d.n, d.H, d.E,
+                                          d.norm ? 1 : 0, idesc, cols, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    rescore<<<rgrid, RR_THREADS, 0, s>>>(xb, wb, bias, logits, topk_idx, topk_w, d.n, d.H, d.E,
+                                         d.norm ? 1 : 0, tau_rel);
     return cudaGetLastError();
   };
-#define MOE_RT_CASE(KK)                                                              \
-  case KK:                                                                           \
-    return run(router_tc_kernel<KK>, rt_smem_bytes<KK>(64) > rt_smem_bytes<KK>(256) \
-                                         ? rt_smem_bytes<KK>(64)                     \
-                                         : rt_smem_bytes<KK>(256),                   \
+#define MOE_RT_CASE(KK)                                                                    \
+  case KK:                                                                                 \
+    return run(router_tc_kernel<KK>, router_rescore_kernel<KK>,                            \
+               rt_smem_bytes<KK>(64) > rt_smem_bytes<KK>(256) ? rt_smem_bytes<KK>(64)      \
+                                                              : rt_smem_bytes<KK>(256),    \
                rt_smem_bytes<KK>(d.E));
   switch (d.K) {
     MOE_RT_CASE(1)
