@@ -134,7 +134,7 @@ moe_status_t moe_dispatch_layout(const moe_layer_desc_t *desc, const int32_t *to
  * they run (a pre-planned memory pool with nothing left over, or a context in
  * which a cudaMalloc would stall the device or is not allowed).  There is no
  * counterpart of this call in the pages; it exists only for such callers.
- *   - Scratch: a fixed device array owned by the library (512 KiB + 4 KiB per
+ *   - Scratch: a fixed device array owned by the library (257 KiB per
  *     GPU that loads the library, kept until the process exits).  The call
  *     itself allocates nothing.
  *   - Limit: n*K <= MOE_NOALLOC_MAX_PAIRS (and E <= 256 as everywhere);

@@ -458,9 +458,9 @@ moe_status_t moe_check_status(const int32_t *status_word, moe_stream_t stream) {
 // For callers that cannot allocate device memory at call time -- for example
 // a runtime whose memory is fully pre-planned, or code running where a
 // cudaMalloc would synchronise the device or is simply not permitted -- the
-// layout's scratch (per-chunk histograms and chunk start positions) lives in a
+// layout's scratch (the per-chunk histograms) lives in a
 // fixed array that belongs to the library.  The array is a device global of
-// this file: every GPU that loads the library holds it (512 KiB + 4 KiB) until
+// this file: every GPU that loads the library holds it (257 KiB) until
 // the process exits.  It is shared by every call on a device and keeps what
 // the previous call left in it; the layout kernels overwrite every entry they
 // read, so nothing needs clearing.  Two calls whose work overlaps on the GPU
@@ -471,7 +471,7 @@ namespace moe {
 namespace {
 
 constexpr int kNoAllocMaxChunks = 256;  // chunks of 2048 (token, slot) pairs
-constexpr size_t kNoAllocScratchInts = 2ull * kNoAllocMaxChunks * (kMaxE + 1);
+constexpr size_t kNoAllocScratchInts = (size_t)kNoAllocMaxChunks * (kMaxE + 1);
 
 static __device__ __align__(256) int32_t g_layout_scratch[kNoAllocScratchInts];
 
