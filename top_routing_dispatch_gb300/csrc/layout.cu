@@ -29,13 +29,18 @@ __global__ void __launch_bounds__(LT) layout_count(const int32_t *__restrict__ i
   __syncthreads();
   const long long base = (long long)blockIdx.x * CH;
   bool bad = false;
-  for (int i = threadIdx.x; i < CH; i += LT) {
-    const long long f = base + i;
-    if (f >= nK) break;
-    const int e = idx[f];
-    const bool ok = (unsigned)e < (unsigned)E;
+  int ev[CH / LT];  // all loads first, then the counting
+#pragma unroll
+  for (int j = 0; j < CH / LT; ++j) {
+    const long long f = base + j * LT + threadIdx.x;
+    ev[j] = f < nK ? __ldg(idx + f) : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < CH / LT; ++j) {
+    if (base + j * LT + threadIdx.x >= nK) break;
+    const bool ok = (unsigned)ev[j] < (unsigned)E;
     bad |= !ok;
-    atomicAdd(&hist[ok ? e : E], 1);
+    atomicAdd(&hist[ok ? ev[j] : E], 1);
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(status, MOE_DEV_BAD_ROUTING);
   for (int c = threadIdx.x; c <= E; c += LT) cnt[(size_t)blockIdx.x * (E + 1) + c] = hist[c];
@@ -104,14 +109,19 @@ __global__ void __launch_bounds__(LT) layout_scan_scatter(const int32_t *__restr
       carry += __shfl_sync(0xffffffffu, inc, 31);
     }
   }
-  // pass 1: this warp's histogram
-  for (int s = 0; s < SLICE; s += 32) {
-    const long long f = slice0 + s + lane;
-    if (f < nK) {
-      const int e = idx[f];
-      atomicAdd(&run[w][(unsigned)e < (unsigned)E ? e : E], 1);
-    }
+  // pass 1: the slice's buckets (kept in registers for pass 2) and this
+  // warp's histogram
+  constexpr int NS = SLICE / 32;
+  int key[NS];
+#pragma unroll
+  for (int j = 0; j < NS; ++j) {  // -1 past the end; E for an id outside [0, E)
+    const long long f = slice0 + 32 * j + lane;
+    const int e = f < nK ? __ldg(idx + f) : 0;
+    key[j] = f < nK ? ((unsigned)e < (unsigned)E ? e : E) : -1;
   }
+#pragma unroll
+  for (int j = 0; j < NS; ++j)
+    if (key[j] >= 0) atomicAdd(&run[w][key[j]], 1);
   __syncthreads();
   // running positions: chunk base + counts of the earlier warps of this block
   for (int c = threadIdx.x; c <= E; c += LT) {
@@ -125,26 +135,23 @@ __global__ void __launch_bounds__(LT) layout_scan_scatter(const int32_t *__restr
   __syncthreads();
   // pass 2: stable scatter
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int s = 0; s < SLICE; s += 32) {
-    const long long f = slice0 + s + lane;
-    int key = -1;
-    if (f < nK) {
-      const int e = idx[f];
-      key = (unsigned)e < (unsigned)E ? e : E;
-    }
-    if (key >= 0) atomicOr(&mask[w][key], 1u << lane);
+#pragma unroll
+  for (int j = 0; j < NS; ++j) {
+    const long long f = slice0 + 32 * j + lane;
+    const int k = key[j];
+    if (k >= 0) atomicOr(&mask[w][k], 1u << lane);
     __syncwarp();
-    const unsigned peers = key >= 0 ? mask[w][key] : 0u;
+    const unsigned peers = k >= 0 ? mask[w][k] : 0u;
     __syncwarp();
-    if (key >= 0) {
-      const int pos = run[w][key] + __popc(peers & lt_mask);
+    if (k >= 0) {
+      const int pos = run[w][k] + __popc(peers & lt_mask);
       perm[pos] = (int32_t)f;
       inv_perm[f] = pos;
     }
     __syncwarp();
-    if (key >= 0 && (peers & lt_mask) == 0) {  // the lowest lane of the expert
-      run[w][key] += __popc(peers);
-      mask[w][key] = 0u;
+    if (k >= 0 && (peers & lt_mask) == 0) {  // the lowest lane of the expert
+      run[w][k] += __popc(peers);
+      mask[w][k] = 0u;
     }
     __syncwarp();
   }

@@ -17,33 +17,46 @@ namespace {
 constexpr int PT = 256;   // threads per block
 constexpr int PU = 8;     // 16-byte vectors in flight per lane
 
+// Permute: warp w copies the contiguous row range [w*nK/W, (w+1)*nK/W) of
+// x_perm (its writes are one contiguous block), two rows per step with every
+// load of both rows issued before their stores.
 __global__ void __launch_bounds__(PT) permute_kernel(const uint4 *__restrict__ x,
                                                      const int32_t *__restrict__ perm,
                                                      uint4 *__restrict__ xp, long long nK, int K,
                                                      int V, int32_t *status) {
   const int lane = threadIdx.x & 31;
-  const long long w0 = ((long long)blockIdx.x * PT + threadIdx.x) >> 5;
-  const long long nw = ((long long)gridDim.x * PT) >> 5;
-  for (long long r = w0; r < nK; r += nw) {
-    const int f = __ldg(perm + r);
-    uint4 *dst = xp + (size_t)r * V;
-    if ((unsigned long long)(unsigned)f >= (unsigned long long)nK || f < 0) {
-      if (lane == 0) flag_status(status, MOE_DEV_BAD_LAYOUT);
-      for (int v = lane; v < V; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    const uint4 *src = x + (size_t)(f / K) * V;
-    for (int v0 = 0; v0 < V; v0 += 32 * PU) {
-      uint4 buf[PU];
+  const long long W = ((long long)gridDim.x * PT) >> 5;
+  const long long wid = ((long long)blockIdx.x * PT + threadIdx.x) >> 5;
+  const long long r0 = wid * nK / W, r1 = (wid + 1) * nK / W;
+  for (long long r = r0; r < r1; r += 2) {
+    const bool two = r + 1 < r1;
+    int f[2] = {__ldg(perm + r), two ? __ldg(perm + r + 1) : 0};
+    bool ok[2];
 #pragma unroll
-      for (int u = 0; u < PU; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < V) buf[u] = __ldg(src + v);
+    for (int q = 0; q < 2; ++q) {
+      ok[q] = (q == 0 || two) && f[q] >= 0 && (long long)f[q] < nK;
+      if ((q == 0 || two) && !ok[q] && lane == 0) flag_status(status, MOE_DEV_BAD_LAYOUT);
+    }
+    for (int v0 = 0; v0 < V; v0 += 32 * PU) {
+      uint4 buf[2][PU];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint4 *src = x + (size_t)(ok[q] ? f[q] / K : 0) * V;
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < V) buf[q][u] = ok[q] ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        }
       }
 #pragma unroll
-      for (int u = 0; u < PU; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < V) dst[v] = buf[u];
+      for (int q = 0; q < 2; ++q) {
+        if (q == 1 && !two) break;
+        uint4 *dst = xp + (size_t)(r + q) * V;
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < V) dst[v] = buf[q][u];
+        }
       }
     }
   }
@@ -65,6 +78,12 @@ __device__ __forceinline__ void acc_vec(float (&a)[8], uint4 v, float w, bool bf
   }
 }
 
+// Combine work item: one token's 64-vector chunk of a row (two 16-byte vectors
+// per lane).  Warp w takes the contiguous item range [w*T/W, (w+1)*T/W), so
+// the warps' loads differ by at most one item, and all K rows' vectors of an
+// item are loaded before they are accumulated.
+constexpr int CV = 64;  // vectors per combine item
+
 template <bool BF16, int KM>
 __global__ void __launch_bounds__(PT) combine_kernel(const uint4 *__restrict__ yp,
                                                      const float *__restrict__ tw,
@@ -72,62 +91,95 @@ __global__ void __launch_bounds__(PT) combine_kernel(const uint4 *__restrict__ y
                                                      uint4 *__restrict__ y, int n, int K, int V,
                                                      long long nK, int32_t *status) {
   const int lane = threadIdx.x & 31;
-  const long long w0 = ((long long)blockIdx.x * PT + threadIdx.x) >> 5;
-  const long long nw = ((long long)gridDim.x * PT) >> 5;
-  for (long long t = w0; t < n; t += nw) {
-    int my_row = 0;
-    float my_w = 0.f;
-    bool my_ok = true;
-    if (lane < K) {
-      my_row = __ldg(inv + t * K + lane);
-      my_w = __ldg(tw + t * K + lane);
-      my_ok = my_row >= 0 && (long long)my_row < nK;
+  const int nseg = (V + CV - 1) / CV;
+  const long long T = (long long)n * nseg;
+  const long long W = ((long long)gridDim.x * PT) >> 5;
+  const long long wid = ((long long)blockIdx.x * PT + threadIdx.x) >> 5;
+  const long long i0 = wid * T / W, i1 = (wid + 1) * T / W;
+  int cur = -1;
+  int rows[KM];
+  float ws[KM];
+  unsigned okmask = 0u;
+  for (long long i = i0; i < i1; ++i) {
+    const int t = (int)(i / nseg);
+    const int v0 = (int)(i - (long long)t * nseg) * CV + lane;
+    if (t != cur) {  // the token's K rows and weights
+      cur = t;
+      int my_row = 0;
+      float my_w = 0.f;
+      bool my_ok = true;
+      if (lane < K) {
+        my_row = __ldg(inv + (size_t)t * K + lane);
+        my_w = __ldg(tw + (size_t)t * K + lane);
+        my_ok = my_row >= 0 && (long long)my_row < nK;
+      }
+      okmask = __ballot_sync(0xffffffffu, my_ok);
+      if (okmask != 0xffffffffu && lane == 0 && v0 == lane) flag_status(status, MOE_DEV_BAD_LAYOUT);
+#pragma unroll
+      for (int k = 0; k < KM; ++k) {
+        rows[k] = __shfl_sync(0xffffffffu, my_row, k);
+        ws[k] = __shfl_sync(0xffffffffu, my_w, k);
+      }
     }
-    const unsigned okmask = __ballot_sync(0xffffffffu, my_ok);
-    if (okmask != 0xffffffffu && lane == 0) flag_status(status, MOE_DEV_BAD_LAYOUT);
-    int rows[KM];
-    float ws[KM];
+    const bool in0 = v0 < V, in1 = v0 + 32 < V;
+    uint4 b0[KM], b1[KM];
 #pragma unroll
     for (int k = 0; k < KM; ++k) {
-      rows[k] = __shfl_sync(0xffffffffu, my_row, k);
-      ws[k] = __shfl_sync(0xffffffffu, my_w, k);
+      if (k < K && (okmask >> k & 1u)) {
+        const uint4 *r = yp + (size_t)rows[k] * V;
+        if (in0) b0[k] = __ldg(r + v0);
+        if (in1) b1[k] = __ldg(r + v0 + 32);
+      }
     }
     uint4 *dst = y + (size_t)t * V;
-    for (int v = lane; v < V; v += 32) {
-      uint4 buf[KM];
 #pragma unroll
-      for (int k = 0; k < KM; ++k)
-        if (k < K && (okmask >> k & 1u)) buf[k] = __ldg(yp + (size_t)rows[k] * V + v);
+    for (int h = 0; h < 2; ++h) {
+      if (!(h ? in1 : in0)) continue;
       float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < KM; ++k)
-        if (k < K && (okmask >> k & 1u)) acc_vec(a, buf[k], ws[k], BF16);
+        if (k < K && (okmask >> k & 1u)) acc_vec(a, h ? b1[k] : b0[k], ws[k], BF16);
       uint4 o;
       if (BF16) {
         __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&o);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
+        for (int q = 0; q < 4; ++q) p[q] = __floats2bfloat162_rn(a[2 * q], a[2 * q + 1]);
       } else {
         float *p = reinterpret_cast<float *>(&o);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) p[i] = a[i];
+        for (int q = 0; q < 4; ++q) p[q] = a[q];
       }
-      dst[v] = o;
+      dst[v0 + 32 * h] = o;
     }
   }
 }
 
-inline int grid_for_rows(long long rows) {
-  const long long want = (rows + (PT / 32) - 1) / (PT / 32);
-  const long long cap = (long long)device_sm_count() * 8;
-  return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+// blocks of the kernel that fit on the device at once (all CTAs in one wave)
+template <auto Kernel>
+int resident_grid() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int &c = cache[dev >= 0 && dev < 64 ? dev : 0];
+  if (c == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, Kernel, PT, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    c = per_sm * device_sm_count();
+  }
+  return c;
 }
 
 template <bool BF16, int KM>
 cudaError_t combine_k(const Desc &d, const void *y_perm, const float *topk_w,
                       const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s) {
   const int V = (int)((size_t)d.H * elem_bytes(d) / 16);
-  combine_kernel<BF16, KM><<<grid_for_rows(d.n), PT, 0, s>>>(
+  const long long items = (long long)d.n * ((V + CV - 1) / CV);
+  const long long res = resident_grid<combine_kernel<BF16, KM>>();
+  const long long want = (items + (PT / 32) - 1) / (PT / 32);
+  const int grid = (int)(want < res ? want : res);
+  combine_kernel<BF16, KM><<<grid, PT, 0, s>>>(
       reinterpret_cast<const uint4 *>(y_perm), topk_w, inv_perm, reinterpret_cast<uint4 *>(y),
       d.n, d.K, V, d.nK(), status);
   return cudaGetLastError();
@@ -150,7 +202,9 @@ cudaError_t launch_permute(const Desc &d, const void *x, const int32_t *perm, vo
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
   const int V = (int)((size_t)d.H * elem_bytes(d) / 16);
-  permute_kernel<<<grid_for_rows(nK), PT, 0, s>>>(reinterpret_cast<const uint4 *>(x), perm,
+  const long long res = resident_grid<permute_kernel>();
+  const long long want = (nK + (PT / 32) - 1) / (PT / 32);
+  permute_kernel<<<(int)(want < res ? want : res), PT, 0, s>>>(reinterpret_cast<const uint4 *>(x), perm,
                                                   reinterpret_cast<uint4 *>(x_perm), nK, d.K, V,
                                                   status);
   return cudaGetLastError();
