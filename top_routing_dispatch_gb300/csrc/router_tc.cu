@@ -3,21 +3,17 @@
 // K <= 8.  "MoE 分布式推理基础（基于 vLLM）" §1.2, Algorithm 2 steps 1-3 and
 // the router's renormalisation.
 //
-// One CTA per 128-token tile (persistent over tiles), 18 warps:
-//   warp 0       TMA producer: x tile (128 tokens x 64 k) and E/64 boxes of
-//                W_gate (64 k x 64 experts) per stage.
-//   warp 1       TMEM allocator and MMA issuer: 128 x E x 16 bf16 MMAs into one
-//                of two E-column float32 accumulators.
-//   warps 2..17  epilogue: 4 TMEM lane quarters x 4 column slices.  Each
-//                thread owns one token and E/4 experts: it adds the bias,
-//                stores those float32 logits, keeps the K+1 largest in
-//                registers (descending, ties to the lower expert id), and
-//                computes their max and sum of exp.  After a barrier one
-//                thread per token merges the four slices.  Tokens whose top
-//                K+1 logits lie closer than the margin tau are rescored by all
-//                512 epilogue threads in double-float (exact products,
-//                error-free sums) over the experts within tau of the K-th
-//                logit, and chosen on those values.
+// A cluster of 4 CTAs per 128-token tile (6 warps each):
+//   warp 0      TMA producer: x tile (128 tokens x 64 k) and E/64 boxes of
+//               W_gate (64 k x 64 experts) per stage, for this CTA's quarter
+//               of the k-blocks.
+//   warp 1      TMEM allocator and MMA issuer: 128 x E x 16 bf16 MMAs into
+//               one E-column float32 accumulator.
+//   warps 2..5  exchange of the partial logits through distributed shared
+//               memory, then the TopK epilogue of this CTA's 32 tokens.
+// Tokens whose top K+1 logits lie closer than the margin tau are rescored by
+// router_rescore_kernel in double-float (exact products, error-free sums) over
+// the experts whose order the float32 logits leave open.
 #include <cuda.h>
 
 #include <mutex>
@@ -30,10 +26,11 @@ namespace moe {
 namespace {
 
 constexpr int RT_BM = 128, RT_BK = 64, RT_MAX_STAGES = 8;
-constexpr int RT_SLICES = 4;                          // column slices per token
-constexpr int RT_EPI_WARPS = 4 * RT_SLICES;           // 16
-constexpr int RT_EPI_THREADS = 32 * RT_EPI_WARPS;     // 512
-constexpr int RT_THREADS = 64 + RT_EPI_THREADS;       // 576
+constexpr int RC = 4;                                 // CTAs per tile (cluster): K split 4 ways
+constexpr int RT_ROWS = RT_BM / RC;                   // tokens a CTA finalises (32)
+constexpr int RT_SLICES = 4;                          // column slices per token (= epilogue warps)
+constexpr int RT_EPI_THREADS = 32 * RT_SLICES;        // 128
+constexpr int RT_THREADS = 64 + RT_EPI_THREADS;       // 192
 constexpr int RT_A_BYTES = RT_BM * RT_BK * 2;         // 16 KB
 constexpr int RT_BOX_BYTES = 64 * RT_BK * 2;          // 8 KB: 64 experts x 64 k
 constexpr int RT_PIPE_BYTES = 168 * 1024;             // operand stages
@@ -42,8 +39,7 @@ constexpr int RR_THREADS = 256;                       // rescoring kernel: threa
 struct RtTail {
   uint64_t full[RT_MAX_STAGES];
   uint64_t empty[RT_MAX_STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull;
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -52,16 +48,22 @@ struct RtTail {
 
 template <int KM>
 struct EpiSmem {
-  float pv[RT_SLICES][RT_BM][KM + 1];  // per-slice top K+1 values
-  int pi[RT_SLICES][RT_BM][KM + 1];    // ... and expert ids
-  float pm[RT_SLICES][RT_BM];          // per-slice max
-  float ps[RT_SLICES][RT_BM];          // per-slice sum of exp(l - slice max)
-  int stop;                            // set by an epilogue thread whose wait gave up
+  float pv[RT_SLICES][RT_ROWS][KM + 1];  // per-slice top K+1 values
+  int pi[RT_SLICES][RT_ROWS][KM + 1];    // ... and expert ids
+  float pm[RT_SLICES][RT_ROWS];          // per-slice max
+  float ps[RT_SLICES][RT_ROWS];          // per-slice sum of exp(l - slice max)
 };
 
 __host__ __device__ inline int rt_stages(int E) {
   const int s = RT_PIPE_BYTES / (RT_A_BYTES + (E / 64) * RT_BOX_BYTES);
   return s < RT_MAX_STAGES ? s : RT_MAX_STAGES;
+}
+
+// float32 partial logits received from the cluster: [RC][RT_ROWS][E + 4]
+// (rows padded by 16 bytes against bank conflicts); aliases the operand
+// stages, which are idle once every MMA of the cluster has finished
+__host__ __device__ inline size_t red_bytes(int E) {
+  return (size_t)RC * RT_ROWS * (E + 4) * sizeof(float);
 }
 
 // the tail (mbarriers) follows the epilogue area at a 16-byte boundary
@@ -91,7 +93,7 @@ __device__ __forceinline__ bool rt_wait(uint64_t *bar, uint32_t parity, volatile
   }
 }
 
-// barrier among the 512 epilogue threads only
+// barrier among the epilogue threads only
 __device__ __forceinline__ void epi_bar() {
   asm volatile("bar.sync 1, %0;" ::"r"(RT_EPI_THREADS) : "memory");
 }
@@ -319,6 +321,21 @@ __global__ void __launch_bounds__(RR_THREADS)
   }
 }
 
+// Tile kernel.  A cluster of RC = 4 CTAs takes one 128-token tile; CTA c of
+// the cluster runs the k-blocks [c*KB/4, (c+1)*KB/4) of the 128 x E router
+// GEMM into its own TMEM accumulator, so the four CTAs stream disjoint
+// quarters of x and W_gate.  After a cluster barrier (every MMA of the cluster
+// done, so the operand stages are idle) each CTA's epilogue warps send row
+// quarter q of their partial logits to CTA q's shared memory; after a second
+// barrier CTA c adds the four partials of its 32 tokens in k order, adds the
+// bias, and runs the TopK epilogue on them: 4 warps = 4 column slices of E/4
+// experts, one token per lane; each thread stores its float32 logits, keeps
+// their K+1 largest (descending, ties to the lower id), their max and sum of
+// exp; one thread per token merges the four slices.  A token whose top K+1
+// logits lie closer than the margin tau gets topk_idx[t][0] = -1 and is
+// decided by router_rescore_kernel.  Every thread passes both cluster
+// barriers on every path (also after a timed-out wait), so no CTA waits on a
+// peer that left.
 template <int KM>
 __global__ void __launch_bounds__(RT_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
@@ -335,26 +352,26 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   const int STAGES = rt_stages(E);
   uint8_t *smemA = smem;
   uint8_t *smemB = smem + STAGES * RT_A_BYTES;
+  float *red = reinterpret_cast<float *>(smem);  // after the first cluster barrier
   EpiSmem<KM> &ep = *reinterpret_cast<EpiSmem<KM> *>(smem + STAGES * (RT_A_BYTES + b_stage));
   RtTail &st = *reinterpret_cast<RtTail *>(reinterpret_cast<uint8_t *>(&ep) + epi_bytes<KM>());
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles = (n + RT_BM - 1) / RT_BM;
+  const int rank = (int)ptx::cluster_ctarank();
+  const int tile = blockIdx.x / RC;
   const int KB = H / RT_BK;
-  if ((int)blockIdx.x >= n_tiles) return;
+  const int kb0 = rank * KB / RC, kb1 = (rank + 1) * KB / RC;
+  const bool has_k = kb1 > kb0;
+  const int RS = E + 4;  // row stride of red (floats)
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&st.full[s], 1);
       ptx::mbar_init(&st.empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(&st.tfull[a], 1);
-      ptx::mbar_init(&st.tempty[a], RT_EPI_WARPS);
-    }
+    ptx::mbar_init(&st.tfull, 1);
     ptx::mbar_init(&st.drain, 1);
     st.abort_flag = 0;
-    ep.stop = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
@@ -369,223 +386,222 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = st.tmem_base;
   volatile int *abort_flag = &st.abort_flag;
+  bool acc_ok = has_k;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && has_k) {
       ptx::prefetch_tmap(&tmX);
       ptx::prefetch_tmap(&tmW);
       int stage = 0;
       uint32_t phase = 0, used = 0, last_par = 0;
       const uint32_t tx_bytes = RT_A_BYTES + b_stage;
-      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-        bool stop = false;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!rt_wait(&st.empty[stage], phase ^ 1u, abort_flag, status)) {
-            stop = true;
-            break;
-          }
-          ptx::mbar_arrive_expect_tx(&st.full[stage], tx_bytes);
-          ptx::tma_load_2d(smemA + stage * RT_A_BYTES, &tmX, &st.full[stage], kb * RT_BK,
-                           t * RT_BM);
-          for (int q = 0; q < nbox; ++q)
-            ptx::tma_load_2d(smemB + stage * b_stage + q * RT_BOX_BYTES, &tmW, &st.full[stage],
-                             q * 64, kb * RT_BK);
-          used |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!rt_wait(&st.empty[stage], phase ^ 1u, abort_flag, status)) break;
+        ptx::mbar_arrive_expect_tx(&st.full[stage], tx_bytes);
+        ptx::tma_load_2d(smemA + stage * RT_A_BYTES, &tmX, &st.full[stage], kb * RT_BK,
+                         tile * RT_BM);
+        for (int q = 0; q < nbox; ++q)
+          ptx::tma_load_2d(smemB + stage * b_stage + q * RT_BOX_BYTES, &tmW, &st.full[stage],
+                           q * 64, kb * RT_BK);
+        used |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
-        if (stop) break;
       }
+      // never leave a TMA copy in flight
       for (int s = 0; s < STAGES; ++s)
         if (used >> s & 1u) ptx::mbar_wait(&st.full[s], last_par >> s & 1u);
     }
+    __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-        if (!rt_wait(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status)) break;
-        ptx::tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(acc * E);
-        bool stop = false;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!rt_wait(&st.full[stage], phase, abort_flag, status)) {
-            stop = true;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_u32(smemA + stage * RT_A_BYTES);
-          const uint32_t b0 = ptx::smem_u32(smemB + stage * b_stage);
-#pragma unroll
-          for (int kk = 0; kk < RT_BK / 16; ++kk) {
-            const uint64_t adesc = ptx::smem_desc(a0 + kk * 32, 16, 1024);
-            const uint64_t bdesc = ptx::smem_desc(b0 + kk * 2048, RT_BOX_BYTES, 1024);
-            ptx::mma_bf16(d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
-          ptx::mma_commit(&st.empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+    if (lane == 0 && has_k) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!rt_wait(&st.full[stage], phase, abort_flag, status)) {
+          ok = false;
+          break;
         }
-        if (stop) break;
-        ptx::mma_commit(&st.tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        ptx::tc_fence_after();
+        const uint32_t a0 = ptx::smem_u32(smemA + stage * RT_A_BYTES);
+        const uint32_t b0 = ptx::smem_u32(smemB + stage * b_stage);
+#pragma unroll
+        for (int kk = 0; kk < RT_BK / 16; ++kk) {
+          const uint64_t adesc = ptx::smem_desc(a0 + kk * 32, 16, 1024);
+          const uint64_t bdesc = ptx::smem_desc(b0 + kk * 2048, RT_BOX_BYTES, 1024);
+          ptx::mma_bf16(tmem, adesc, bdesc, idesc, (kb > kb0 || kk) ? 1u : 0u);
+        }
+        ptx::mma_commit(&st.empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
+      (void)ok;
+      // the accumulator (complete, or abandoned after a timeout) and the end
+      // of every MMA this thread issued
+      ptx::mma_commit(&st.tfull);
       ptx::mma_commit(&st.drain);
       ptx::mbar_wait(&st.drain, 0);
     }
+    __syncwarp();
   } else {
-    const int ew = warp - 2;              // epilogue warp 0..15
-    const int q = warp & 3;               // TMEM lane quarter this warp may read
-    const int sl = ew >> 2;               // column slice 0..3
-    const int r = q * 32 + lane;          // token row in the tile
+    if (has_k) acc_ok = rt_wait(&st.tfull, 0, abort_flag, status) && !*abort_flag;
+    acc_ok = __all_sync(0xffffffffu, acc_ok);  // tcgen05.ld below is warp-wide
+  }
+
+  // #1: every MMA of the cluster has finished, the operand stages are idle
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  if (warp >= 2) {
+    // row quarter q of this CTA's partial -> CTA q, slot `rank`
+    const int q = warp & 3;
+    const uint32_t dst = ptx::mapa_shared(
+        ptx::smem_u32(red + ((size_t)rank * RT_ROWS + lane) * RS), (uint32_t)q);
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    for (int c = 0; c < E; c += 8) {
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (acc_ok) {  // warp-uniform
+        uint32_t raw[8];
+        ptx::tmem_ld_32x32b_x8(tq + c, raw);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(raw[i]);
+      }
+      ptx::st_cluster_v4(dst + c * 4, v[0], v[1], v[2], v[3]);
+      ptx::st_cluster_v4(dst + c * 4 + 16, v[4], v[5], v[6], v[7]);
+    }
+  }
+  // #2: this CTA's 32 rows hold the four partials
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+
+  if (warp >= 2) {
+    const int sl = warp - 2;             // column slice 0..3
+    const int r = lane;                  // token row among this CTA's 32
     const int cols = E / RT_SLICES;
     const int c0 = sl * cols;
     const float tau_rel = tie_margin_tc(H);
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      // all 512 threads take every barrier below; a thread whose wait gave up
-      // raises ep.stop before the first one, so all leave together
-      if (!rt_wait(&st.tfull[acc], acc_phase, abort_flag, status)) ep.stop = 1;
-      epi_bar();
-      if (ep.stop) break;
-      ptx::tc_fence_after();
-      const uint32_t tbase = tmem + (uint32_t)(acc * E + c0) + ((uint32_t)(q * 32) << 16);
-      const int tok = t * RT_BM + r;
-      const bool valid = tok < n;
-      float *lrow = logits + (size_t)(valid ? tok : 0) * E;
+    const int tok = tile * RT_BM + rank * RT_ROWS + r;
+    const bool valid = tok < n;
+    float *lrow = logits + (size_t)(valid ? tok : 0) * E;
 
-      // this slice: logits, max, top K+1 (descending, ties to the lower id)
-      float lv[K + 1];
-      int li[K + 1];
+    float lv[K + 1];
+    int li[K + 1];
+#pragma unroll
+    for (int j = 0; j <= K; ++j) {
+      lv[j] = -INFINITY;
+      li[j] = 0x7fffffff;
+    }
+    float last_v = -INFINITY;
+    int last_i = 0x7fffffff;
+    float m = -INFINITY;
+    for (int c = 0; c < cols; c += 4) {
+      float4 sum = *reinterpret_cast<const float4 *>(red + (size_t)r * RS + c0 + c);
+#pragma unroll
+      for (int p = 1; p < RC; ++p) {  // k order
+        const float4 pv = *reinterpret_cast<const float4 *>(red + ((size_t)p * RT_ROWS + r) * RS + c0 + c);
+        sum.x += pv.x;
+        sum.y += pv.y;
+        sum.z += pv.z;
+        sum.w += pv.w;
+      }
+      const float v[4] = {sum.x + st.bias[c0 + c], sum.y + st.bias[c0 + c + 1],
+                          sum.z + st.bias[c0 + c + 2], sum.w + st.bias[c0 + c + 3]};
+      if (valid) *reinterpret_cast<float4 *>(lrow + c0 + c) = make_float4(v[0], v[1], v[2], v[3]);
+      // keep the logits for the sum of exp (same smem row, partial 0's slot)
+      *reinterpret_cast<float4 *>(red + (size_t)r * RS + c0 + c) = make_float4(v[0], v[1], v[2], v[3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, v[i]);
+        const int e = c0 + c + i;
+        if (ranks_above(v[i], e, last_v, last_i)) {
+          float cv = v[i];
+          int ci = e;
+#pragma unroll
+          for (int j = 0; j <= K; ++j) {
+            const bool gt = ranks_above(cv, ci, lv[j], li[j]);
+            const float tv = gt ? lv[j] : cv;
+            const int ti = gt ? li[j] : ci;
+            lv[j] = gt ? cv : lv[j];
+            li[j] = gt ? ci : li[j];
+            cv = tv;
+            ci = ti;
+          }
+          last_v = lv[K];
+          last_i = li[K];
+        }
+      }
+    }
+    float ssum = 0.f;
+    for (int c = 0; c < cols; ++c) ssum += expf(red[(size_t)r * RS + c0 + c] - m);
+#pragma unroll
+    for (int j = 0; j <= K; ++j) {
+      ep.pv[sl][r][j] = lv[j];
+      ep.pi[sl][r][j] = li[j];
+    }
+    ep.pm[sl][r] = m;
+    ep.ps[sl][r] = ssum;
+    epi_bar();
+
+    // merge the four slices: one thread per token
+    if (sl == 0 && valid) {
+      float fv[K + 1];
+      int fi[K + 1];
+      int h0 = 0, h1 = 0, h2 = 0, h3 = 0;
 #pragma unroll
       for (int j = 0; j <= K; ++j) {
-        lv[j] = -INFINITY;
-        li[j] = 0x7fffffff;
+        float bv = h0 <= K ? ep.pv[0][r][h0] : -INFINITY;
+        int bi = h0 <= K ? ep.pi[0][r][h0] : 0x7fffffff;
+        int bw = 0;
+        const float v1 = h1 <= K ? ep.pv[1][r][h1] : -INFINITY;
+        const int i1 = h1 <= K ? ep.pi[1][r][h1] : 0x7fffffff;
+        if (ranks_above(v1, i1, bv, bi)) { bv = v1; bi = i1; bw = 1; }
+        const float v2 = h2 <= K ? ep.pv[2][r][h2] : -INFINITY;
+        const int i2 = h2 <= K ? ep.pi[2][r][h2] : 0x7fffffff;
+        if (ranks_above(v2, i2, bv, bi)) { bv = v2; bi = i2; bw = 2; }
+        const float v3 = h3 <= K ? ep.pv[3][r][h3] : -INFINITY;
+        const int i3 = h3 <= K ? ep.pi[3][r][h3] : 0x7fffffff;
+        if (ranks_above(v3, i3, bv, bi)) { bv = v3; bi = i3; bw = 3; }
+        fv[j] = bv;
+        fi[j] = bi;
+        h0 += bw == 0;
+        h1 += bw == 1;
+        h2 += bw == 2;
+        h3 += bw == 3;
       }
-      float last_v = -INFINITY;
-      int last_i = 0x7fffffff;
-      float m = -INFINITY;
-      for (int c = 0; c < cols / 8; ++c) {
-        uint32_t raw[8];
-        ptx::tmem_ld_32x32b_x8(tbase + c * 8, raw);
-        ptx::tmem_ld_wait();
-        float v[8];
+      float M = ep.pm[0][r];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(raw[i]) + st.bias[c0 + c * 8 + i];
-        if (valid) {
-          float4 *dst = reinterpret_cast<float4 *>(lrow + c0 + c * 8);
-          dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-          dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+      for (int w = 1; w < RT_SLICES; ++w) M = fmaxf(M, ep.pm[w][r]);
+      float S = 0.f;
+#pragma unroll
+      for (int w = 0; w < RT_SLICES; ++w) S += ep.ps[w][r] * expf(ep.pm[w][r] - M);
+      const float tau = tau_rel * fmaxf(1.f, fabsf(M));
+      bool amb = false;
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+        if (isfinite(fv[j]) && isfinite(fv[j + 1]) && fv[j] - fv[j + 1] < tau) amb = true;
+      if (!amb) {
+        float w[K];
+        float wsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          w[j] = expf(fv[j] - M) / S;
+          wsum += w[j];
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          m = fmaxf(m, v[i]);
-          const int e = c0 + c * 8 + i;
-          if (ranks_above(v[i], e, last_v, last_i)) {
-            float cv = v[i];
-            int ci = e;
-#pragma unroll
-            for (int j = 0; j <= K; ++j) {
-              const bool gt = ranks_above(cv, ci, lv[j], li[j]);
-              const float tv = gt ? lv[j] : cv;
-              const int ti = gt ? li[j] : ci;
-              lv[j] = gt ? cv : lv[j];
-              li[j] = gt ? ci : li[j];
-              cv = tv;
-              ci = ti;
-            }
-            last_v = lv[K];
-            last_i = li[K];
-          }
+        for (int j = 0; j < K; ++j) {
+          topk_idx[(size_t)tok * K + j] = fi[j];
+          topk_w[(size_t)tok * K + j] = norm ? w[j] / wsum : w[j];
         }
+      } else {
+        topk_idx[(size_t)tok * K] = -1;  // flagged: router_rescore_kernel decides
       }
-      float ssum = 0.f;
-      for (int c = 0; c < cols / 8; ++c) {
-        uint32_t raw[8];
-        ptx::tmem_ld_32x32b_x8(tbase + c * 8, raw);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          ssum += expf(__uint_as_float(raw[i]) + st.bias[c0 + c * 8 + i] - m);
-      }
-      // the accumulator is free for the next tile
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&st.tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-
-#pragma unroll
-      for (int j = 0; j <= K; ++j) {
-        ep.pv[sl][r][j] = lv[j];
-        ep.pi[sl][r][j] = li[j];
-      }
-      ep.pm[sl][r] = m;
-      ep.ps[sl][r] = ssum;
-      epi_bar();
-
-      // merge the four slices: one thread per token
-      if (sl == 0 && valid) {
-        float fv[K + 1];
-        int fi[K + 1];
-        int h0 = 0, h1 = 0, h2 = 0, h3 = 0;
-#pragma unroll
-        for (int j = 0; j <= K; ++j) {
-          float bv = h0 <= K ? ep.pv[0][r][h0] : -INFINITY;
-          int bi = h0 <= K ? ep.pi[0][r][h0] : 0x7fffffff;
-          int bw = 0;
-          const float v1 = h1 <= K ? ep.pv[1][r][h1] : -INFINITY;
-          const int i1 = h1 <= K ? ep.pi[1][r][h1] : 0x7fffffff;
-          if (ranks_above(v1, i1, bv, bi)) { bv = v1; bi = i1; bw = 1; }
-          const float v2 = h2 <= K ? ep.pv[2][r][h2] : -INFINITY;
-          const int i2 = h2 <= K ? ep.pi[2][r][h2] : 0x7fffffff;
-          if (ranks_above(v2, i2, bv, bi)) { bv = v2; bi = i2; bw = 2; }
-          const float v3 = h3 <= K ? ep.pv[3][r][h3] : -INFINITY;
-          const int i3 = h3 <= K ? ep.pi[3][r][h3] : 0x7fffffff;
-          if (ranks_above(v3, i3, bv, bi)) { bv = v3; bi = i3; bw = 3; }
-          fv[j] = bv;
-          fi[j] = bi;
-          h0 += bw == 0;
-          h1 += bw == 1;
-          h2 += bw == 2;
-          h3 += bw == 3;
-        }
-        float M = ep.pm[0][r];
-#pragma unroll
-        for (int w = 1; w < RT_SLICES; ++w) M = fmaxf(M, ep.pm[w][r]);
-        float S = 0.f;
-#pragma unroll
-        for (int w = 0; w < RT_SLICES; ++w) S += ep.ps[w][r] * expf(ep.pm[w][r] - M);
-        const float tau = tau_rel * fmaxf(1.f, fabsf(M));
-        bool amb = false;
-#pragma unroll
-        for (int j = 0; j < K; ++j)
-          if (isfinite(fv[j]) && isfinite(fv[j + 1]) && fv[j] - fv[j + 1] < tau) amb = true;
-        if (!amb) {
-          float w[K];
-          float wsum = 0.f;
-#pragma unroll
-          for (int j = 0; j < K; ++j) {
-            w[j] = expf(fv[j] - M) / S;
-            wsum += w[j];
-          }
-#pragma unroll
-          for (int j = 0; j < K; ++j) {
-            topk_idx[(size_t)tok * K + j] = fi[j];
-            topk_w[(size_t)tok * K + j] = norm ? w[j] / wsum : w[j];
-          }
-        } else {
-          topk_idx[(size_t)tok * K] = -1;  // flagged: router_rescore_kernel decides
-        }
-      }
-      epi_bar();  // the selection lists are reused by the next tile
     }
   }
 
@@ -644,24 +660,38 @@ cudaError_t launch_router_tc(const Desc &d, const void *x, const void *w_gate, c
   CUtensorMap mX, mW;
   if (!rt_map_2d(&mX, x, d.H, d.n, RT_BK, RT_BM) || !rt_map_2d(&mW, w_gate, d.E, d.H, 64, RT_BK))
     return cudaErrorInvalidValue;
+  // the received partials must fit in the idle operand stages
+  if (red_bytes(d.E) > (size_t)rt_stages(d.E) * (RT_A_BYTES + (d.E / 64) * RT_BOX_BYTES))
+    return cudaErrorInvalidValue;
   uint32_t cols = 32;
-  while (cols < 2u * (uint32_t)d.E) cols <<= 1;
+  while (cols < (uint32_t)d.E) cols <<= 1;
   const int n_tiles = (d.n + RT_BM - 1) / RT_BM;
   const int sms = device_sm_count();
-  const int grid = n_tiles < sms ? n_tiles : sms;
   const uint32_t idesc = ptx::idesc_bf16_f32(RT_BM, d.E, false, true);
   const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
   const __nv_bfloat16 *wb = reinterpret_cast<const __nv_bfloat16 *>(w_gate);
   const int rgrid = d.n < 2 * sms ? d.n : 2 * sms;
   const float tau_rel = tie_margin_tc(d.H);
-  // the tile kernel, then the exact rescoring of the tokens it flagged
+  // the tile kernel (clusters of RC CTAs), then the exact rescoring of the
+  // tokens it flagged
   auto run = [&](auto kernel, auto rescore, size_t smem_max, size_t smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem_max);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, RT_THREADS, smem, s>>>(mX, mW, bias, logits, topk_idx, topk_w, d.n, d.H, d.E,
-                                          d.norm ? 1 : 0, idesc, cols, status);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(RC * n_tiles));
+    cfg.blockDim = dim3(RT_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = RC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, mX, mW, bias, logits, topk_idx, topk_w, d.n, d.H, d.E,
+                           d.norm ? 1 : 0, idesc, cols, status);
     if (e != cudaSuccess) return e;
     rescore<<<rgrid, RR_THREADS, 0, s>>>(xb, wb, bias, logits, topk_idx, topk_w, d.n, d.H, d.E,
                                          d.norm ? 1 : 0, tau_rel);
