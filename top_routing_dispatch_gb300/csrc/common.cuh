@@ -92,6 +92,34 @@ int device_sm_count();
 // ---- device helpers
 namespace moe {
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation (launch_pdl) and starts with pdl_enter():
+// it waits until the preceding kernel of its stream has completed and its
+// writes are visible (griddepcontrol.wait, before any global-memory access),
+// then lets the next kernel of the stream begin launching.  The next kernel's
+// launch and set-up thus overlap this kernel's tail; no kernel reads or
+// writes global memory before its predecessor has finished.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 __device__ __forceinline__ void flag_status(int32_t *status, int bits) {
   if (status) atomicOr(status, bits);
 }

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(256) simt_gemm1(const float *__restrict__ xp,
                                                   const int32_t *__restrict__ offsets, int E,
                                                   int nK, int H, int I, float *__restrict__ h,
                                                   int32_t *status) {
+  pdl_enter();
   __shared__ SimtTiles s;
   __shared__ float As[SBK][SBM];
   __shared__ float Bg[SBK][SBN];
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(256) simt_gemm2(const float *__restrict__ h,
                                                   const int32_t *__restrict__ offsets, int E,
                                                   int nK, int H, int I, float *__restrict__ yp,
                                                   int32_t *status) {
+  pdl_enter();
   __shared__ SimtTiles s;
   __shared__ float As[SBK][SBM];
   __shared__ float Bs[SBK][SBN];
@@ -186,10 +188,9 @@ cudaError_t launch_gemm1_simt(const Desc &d, const void *x_perm, const void *w13
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
   dim3 g(simt_max_mtiles(d), (d.I + SBN - 1) / SBN);
-  simt_gemm1<<<g, 256, 0, s>>>(reinterpret_cast<const float *>(x_perm),
-                               reinterpret_cast<const float *>(w13), offsets, d.E, (int)nK, d.H,
-                               d.I, reinterpret_cast<float *>(h), status);
-  return cudaGetLastError();
+  return launch_pdl(simt_gemm1, g, dim3(256), 0, s, reinterpret_cast<const float *>(x_perm),
+                    reinterpret_cast<const float *>(w13), offsets, d.E, (int)nK, d.H, d.I,
+                    reinterpret_cast<float *>(h), status);
 }
 
 cudaError_t launch_gemm2_simt(const Desc &d, const void *h, const void *w2,
@@ -198,10 +199,9 @@ cudaError_t launch_gemm2_simt(const Desc &d, const void *h, const void *w2,
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
   dim3 g(simt_max_mtiles(d), (d.H + SBN - 1) / SBN);
-  simt_gemm2<<<g, 256, 0, s>>>(reinterpret_cast<const float *>(h),
-                               reinterpret_cast<const float *>(w2), offsets, d.E, (int)nK, d.H,
-                               d.I, reinterpret_cast<float *>(y_perm), status);
-  return cudaGetLastError();
+  return launch_pdl(simt_gemm2, g, dim3(256), 0, s, reinterpret_cast<const float *>(h),
+                    reinterpret_cast<const float *>(w2), offsets, d.E, (int)nK, d.H, d.I,
+                    reinterpret_cast<float *>(y_perm), status);
 }
 
 }  // namespace moe

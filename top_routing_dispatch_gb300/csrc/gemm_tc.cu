@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                            int Nout, __nv_bfloat16 *__restrict__ out, int32_t *status,
                            const int32_t *__restrict__ perm, int Kslots,
                            const __nv_bfloat16 *__restrict__ xg) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -515,10 +516,9 @@ cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_attr<1>();
   if (e != cudaSuccess) return e;
-  grouped_gemm_tc_kernel<1><<<gemm_grid(sm_reserve), NUM_THREADS, SMEM_BYTES, s>>>(
-      mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I, reinterpret_cast<__nv_bfloat16 *>(h),
-      status, nullptr, 0, nullptr);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_tc_kernel<1>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
+                    SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
+                    reinterpret_cast<__nv_bfloat16 *>(h), status, nullptr, 0, nullptr);
 }
 
 cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *perm,
@@ -530,10 +530,10 @@ cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *
   if (!make_map_3d(&mB, w13, 2ull * d.I, d.H, d.E, 64, BK)) return cudaErrorInvalidValue;
   cudaError_t e = set_smem_attr<3>();
   if (e != cudaSuccess) return e;
-  grouped_gemm_tc_kernel<3><<<gemm_grid(sm_reserve), threads_for(3), SMEM_BYTES, s>>>(
-      mB, mB, offsets, d.E, (int)nK, d.H, d.I, d.I, reinterpret_cast<__nv_bfloat16 *>(h),
-      status, perm, d.K, reinterpret_cast<const __nv_bfloat16 *>(x));
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_tc_kernel<3>, dim3(gemm_grid(sm_reserve)), dim3(threads_for(3)),
+                    SMEM_BYTES, s, mB, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
+                    reinterpret_cast<__nv_bfloat16 *>(h), status, perm, d.K,
+                    reinterpret_cast<const __nv_bfloat16 *>(x));
 }
 
 cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const int32_t *offsets,
@@ -545,10 +545,9 @@ cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const 
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_attr<2>();
   if (e != cudaSuccess) return e;
-  grouped_gemm_tc_kernel<2><<<gemm_grid(sm_reserve), NUM_THREADS, SMEM_BYTES, s>>>(
-      mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H, reinterpret_cast<__nv_bfloat16 *>(y_perm),
-      status, nullptr, 0, nullptr);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_tc_kernel<2>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
+                    SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
+                    reinterpret_cast<__nv_bfloat16 *>(y_perm), status, nullptr, 0, nullptr);
 }
 
 }  // namespace moe

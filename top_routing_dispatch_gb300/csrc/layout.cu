@@ -24,6 +24,7 @@ constexpr int CH = LW * SLICE;        // pairs per block (2048)
 __global__ void __launch_bounds__(LT) layout_count(const int32_t *__restrict__ idx, long long nK,
                                                    int E, int32_t *__restrict__ cnt,
                                                    int32_t *status) {
+  pdl_enter();
   __shared__ int hist[kMaxE + 1];
   for (int c = threadIdx.x; c <= E; c += LT) hist[c] = 0;
   __syncthreads();
@@ -61,6 +62,7 @@ __global__ void __launch_bounds__(LT) layout_scan_scatter(const int32_t *__restr
                                                           int32_t *__restrict__ offsets,
                                                           int32_t *__restrict__ perm,
                                                           int32_t *__restrict__ inv_perm) {
+  pdl_enter();
   __shared__ int tot[kMaxE + 1];
   __shared__ int pre[kMaxE + 1];
   __shared__ int run[LW][kMaxE + 1];
@@ -177,10 +179,10 @@ cudaError_t launch_layout(const Desc &d, const int32_t *topk_idx, int32_t *count
     return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d.E + 1), s);
   }
   int32_t *cnt = reinterpret_cast<int32_t *>(ws);
-  layout_count<<<nb, LT, 0, s>>>(topk_idx, nK, d.E, cnt, status);
-  layout_scan_scatter<<<nb, LT, 0, s>>>(topk_idx, nK, d.E, nb, cnt, counts, offsets, perm,
-                                        inv_perm);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(layout_count, dim3(nb), dim3(LT), 0, s, topk_idx, nK, d.E, cnt, status);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(layout_scan_scatter, dim3(nb), dim3(LT), 0, s, topk_idx, nK, d.E, nb, cnt,
+                    counts, offsets, perm, inv_perm);
 }
 
 }  // namespace moe

@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(PT) permute_kernel(const uint4 *__restrict__ x
                                                      const int32_t *__restrict__ perm,
                                                      uint4 *__restrict__ xp, long long nK, int K,
                                                      int V, int32_t *status) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const long long W = ((long long)gridDim.x * PT) >> 5;
   const long long wid = ((long long)blockIdx.x * PT + threadIdx.x) >> 5;
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(PT) combine_kernel(const uint4 *__restrict__ y
                                                      const int32_t *__restrict__ inv,
                                                      uint4 *__restrict__ y, int n, int K, int V,
                                                      long long nK, int32_t *status) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int nseg = (V + CV - 1) / CV;
   const long long T = (long long)n * nseg;
@@ -179,10 +181,9 @@ cudaError_t combine_k(const Desc &d, const void *y_perm, const float *topk_w,
   const long long res = resident_grid<combine_kernel<BF16, KM>>();
   const long long want = (items + (PT / 32) - 1) / (PT / 32);
   const int grid = (int)(want < res ? want : res);
-  combine_kernel<BF16, KM><<<grid, PT, 0, s>>>(
-      reinterpret_cast<const uint4 *>(y_perm), topk_w, inv_perm, reinterpret_cast<uint4 *>(y),
-      d.n, d.K, V, d.nK(), status);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel<BF16, KM>, dim3(grid), dim3(PT), 0, s,
+                    reinterpret_cast<const uint4 *>(y_perm), topk_w, inv_perm,
+                    reinterpret_cast<uint4 *>(y), d.n, d.K, V, d.nK(), status);
 }
 
 template <bool BF16>
@@ -204,10 +205,9 @@ cudaError_t launch_permute(const Desc &d, const void *x, const int32_t *perm, vo
   const int V = (int)((size_t)d.H * elem_bytes(d) / 16);
   const long long res = resident_grid<permute_kernel>();
   const long long want = (nK + (PT / 32) - 1) / (PT / 32);
-  permute_kernel<<<(int)(want < res ? want : res), PT, 0, s>>>(reinterpret_cast<const uint4 *>(x), perm,
-                                                  reinterpret_cast<uint4 *>(x_perm), nK, d.K, V,
-                                                  status);
-  return cudaGetLastError();
+  return launch_pdl(permute_kernel, dim3((int)(want < res ? want : res)), dim3(PT), 0, s,
+                    reinterpret_cast<const uint4 *>(x), perm, reinterpret_cast<uint4 *>(x_perm),
+                    nK, d.K, V, status);
 }
 
 cudaError_t launch_combine(const Desc &d, const void *y_perm, const float *topk_w,

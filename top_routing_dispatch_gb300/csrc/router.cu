@@ -38,6 +38,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(RTHREADS) router_logits_kernel(
     const void *__restrict__ x, const void *__restrict__ wg, const float *__restrict__ bias,
     float *__restrict__ logits, int n, int H, int E) {
+  pdl_enter();
   __shared__ float As[RBK][RBM + 4];  // k-major
   __shared__ float Bs[RBK][RBN + 4];
   const int tid = threadIdx.x;
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) router_topk_kernel(
     const float *__restrict__ logits, const void *__restrict__ x, const void *__restrict__ wg,
     const float *__restrict__ bias, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
     int n, int H, int E, int K, int norm, int only_flagged) {
+  pdl_enter();
   __shared__ float s_hi[TOPK_WARPS][kMaxK];
   __shared__ float s_lo[TOPK_WARPS][kMaxK];
   __shared__ int s_e[TOPK_WARPS][kMaxK];
@@ -301,12 +303,10 @@ cudaError_t launch_topk(const Desc &d, const float *logits, const void *x, const
                         cudaStream_t s) {
   dim3 grid((d.n + TOPK_WARPS - 1) / TOPK_WARPS);
   if (d.bf16)
-    router_topk_kernel<EPL, true><<<grid, TOPK_WARPS * 32, 0, s>>>(
-        logits, x, wg, bias, idx, w, d.n, d.H, d.E, d.K, d.norm, only_flagged);
-  else
-    router_topk_kernel<EPL, false><<<grid, TOPK_WARPS * 32, 0, s>>>(
-        logits, x, wg, bias, idx, w, d.n, d.H, d.E, d.K, d.norm, only_flagged);
-  return cudaGetLastError();
+    return launch_pdl(router_topk_kernel<EPL, true>, grid, dim3(TOPK_WARPS * 32), 0, s, logits, x,
+                      wg, bias, idx, w, d.n, d.H, d.E, d.K, d.norm, only_flagged);
+  return launch_pdl(router_topk_kernel<EPL, false>, grid, dim3(TOPK_WARPS * 32), 0, s, logits, x,
+                    wg, bias, idx, w, d.n, d.H, d.E, d.K, d.norm, only_flagged);
 }
 
 cudaError_t launch_topk_any(const Desc &d, const float *logits, const void *x, const void *wg,
@@ -329,11 +329,11 @@ cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, cons
     return launch_router_tc(d, x, w_gate, bias, topk_idx, topk_w, logits, status, s);
   }
   dim3 grid((d.n + RBM - 1) / RBM, (d.E + RBN - 1) / RBN);
-  if (d.bf16)
-    router_logits_kernel<true><<<grid, RTHREADS, 0, s>>>(x, w_gate, bias, logits, d.n, d.H, d.E);
-  else
-    router_logits_kernel<false><<<grid, RTHREADS, 0, s>>>(x, w_gate, bias, logits, d.n, d.H, d.E);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err =
+      d.bf16 ? launch_pdl(router_logits_kernel<true>, grid, dim3(RTHREADS), 0, s, x, w_gate, bias,
+                          logits, d.n, d.H, d.E)
+             : launch_pdl(router_logits_kernel<false>, grid, dim3(RTHREADS), 0, s, x, w_gate,
+                          bias, logits, d.n, d.H, d.E);
   if (err != cudaSuccess) return err;
   return launch_topk_any(d, logits, x, w_gate, bias, topk_idx, topk_w, 0, s);
 }

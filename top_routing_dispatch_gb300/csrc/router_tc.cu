@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(RR_THREADS)
                           const float *__restrict__ logits, int32_t *__restrict__ topk_idx,
                           float *__restrict__ topk_w, int n, int H, int E, int norm,
                           float tau_rel) {
+  pdl_enter();
   static_assert(RR_THREADS >= kMaxE, "one thread per expert");
   constexpr int K = KM;
   constexpr int MAXT = 64;  // tokens one CTA inspects per pass
@@ -343,6 +344,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
                      const float *__restrict__ bias, float *__restrict__ logits,
                      int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int n, int H,
                      int E, int norm, uint32_t idesc, uint32_t tmem_cols, int32_t *status) {
+  pdl_enter();
   constexpr int K = KM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -683,19 +685,20 @@ cudaError_t launch_router_tc(const Desc &d, const void *x, const void *w_gate, c
     cfg.blockDim = dim3(RT_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = RC;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kernel, mX, mW, bias, logits, topk_idx, topk_w, d.n, d.H, d.E,
                            d.norm ? 1 : 0, idesc, cols, status);
     if (e != cudaSuccess) return e;
-    rescore<<<rgrid, RR_THREADS, 0, s>>>(xb, wb, bias, logits, topk_idx, topk_w, d.n, d.H, d.E,
-                                         d.norm ? 1 : 0, tau_rel);
-    return cudaGetLastError();
+    return launch_pdl(rescore, dim3(rgrid), dim3(RR_THREADS), 0, s, xb, wb, bias, logits, topk_idx,
+                      topk_w, d.n, d.H, d.E, d.norm ? 1 : 0, tau_rel);
   };
 #define MOE_RT_CASE(KK)                                                                    \
   case KK:                                                                                 \
