@@ -257,8 +257,11 @@ def algorithmic(cfg, counts=None):
         # perm, the used experts' W13, h
         "gemm1_gather": {"flop": 4 * nK * H * I,
                          "bytes": n * H * b + nK * 4 + used * H * 2 * I * b + nK * I * b},
-        "gemm2": {"flop": 2 * nK * I * H, "bytes": nK * I * b + used * I * H * b + nK * H * b},
-        "combine": {"flop": 2 * nK * H, "bytes": nK * H * b + n * H * b + 2 * nK * 4},
+        # GEMM2 applies the routing weights (reads perm and topk_w) and writes
+        # rows in (token, slot) order; the combine sums each token's K rows
+        "gemm2": {"flop": 2 * nK * I * H + nK * H,
+                  "bytes": nK * I * b + used * I * H * b + nK * H * b + 2 * nK * 4},
+        "combine": {"flop": nK * H, "bytes": nK * H * b + n * H * b},
     }
 
 
@@ -352,10 +355,10 @@ def run_ours(args, cfg):
         ("permute", lambda: M.moe_permute(desc, x, v["perm"], v["x_perm"], st, stream)),
         ("gemm1", lambda: M.moe_expert_gemm1_swiglu(desc, v["x_perm"], L["w13"], v["offsets"],
                                                     v["h"], 0, st, stream)),
-        ("gemm2", lambda: M.moe_expert_gemm2(desc, v["h"], L["w2"], v["offsets"], v["y_perm"], 0,
-                                             st, stream)),
-        ("combine", lambda: M.moe_combine(desc, v["y_perm"], v["topk_w"], v["inv_perm"], y, st,
-                                          stream)),
+        ("gemm2", lambda: M.moe_expert_gemm2_weighted(desc, v["h"], L["w2"], v["offsets"],
+                                                      v["perm"], v["topk_w"], v["y_perm"], 0, st,
+                                                      stream)),
+        ("combine", lambda: M.moe_combine_slots(desc, v["y_perm"], y, stream)),
     ]
     T = Timer(torch, stream, dev)
 
@@ -529,11 +532,12 @@ def domino(args, torch, M, synth, cfg, dev, peaks):
     def gemms(j):
         v = V[j]
         M.moe_expert_gemm1_swiglu(desc, v["x_perm"], L["w13"], v["offsets"], v["h"], 0, st, sc)
-        M.moe_expert_gemm2(desc, v["h"], L["w2"], v["offsets"], v["y_perm"], 0, st, sc)
+        M.moe_expert_gemm2_weighted(desc, v["h"], L["w2"], v["offsets"], v["perm"], v["topk_w"],
+                                    v["y_perm"], 0, st, sc)
 
     def back(j):
         v = V[j]
-        M.moe_combine(desc, v["y_perm"], v["topk_w"], v["inv_perm"], ys[j], st, sc)
+        M.moe_combine_slots(desc, v["y_perm"], ys[j], sc)
 
     R = max(5, args.steps)
     med = lambda fn: statistics.median(T.measure(fn, R))

@@ -225,6 +225,38 @@ moe_status_t moe_combine(const moe_layer_desc_t *desc, const void *y_perm, const
                          moe_stream_t stream);
 
 /*
+ * GEMM2 with the combine's weighting moved into its epilogue (bf16 layers):
+ * for every row r of an expert segment, with f = perm[r] (the flat index
+ * t*K + k of its (token, slot) pair),
+ *   y_slot[f] = topk_w[f] * (h[r] . W2[e]),
+ * rounded once to bf16.  The rows land in (token, slot) order, so the
+ * combine becomes moe_combine_slots, a contiguous read of each token's K
+ * rows: Algorithm 2 step 10's weighting done where Y_e is produced, as the
+ * GEMM + gather + top-k reduce of FLUX/COMET ("大模型系统中的通算融合",
+ * §4.2.5) does.  moe_forward_microbatches uses this pair for bf16 layers.
+ *   h (n*K, I); perm and topk_w as from moe_dispatch_layout / moe_route_topk;
+ *   y_slot (n*K, H).  A perm entry outside [0, n*K) sets MOE_DEV_BAD_LAYOUT and
+ *   its row is not written; rows of pairs with an invalid expert id (at or
+ *   after offsets[E]) are not written either.  float32 layers:
+ *   MOE_ERR_UNSUPPORTED.
+ */
+moe_status_t moe_expert_gemm2_weighted(const moe_layer_desc_t *desc, const void *h,
+                                       const void *w2, const int32_t *offsets,
+                                       const int32_t *perm, const float *topk_w, void *y_slot,
+                                       int sm_reserve, int32_t *status_word,
+                                       moe_stream_t stream);
+
+/*
+ * Combine of slot-ordered, already weighted rows:
+ *   y[t] = sum over k = 0..K-1 of y_slot[t*K + k]
+ * accumulated in float32 in slot order and rounded once (Algorithm 2 step 11
+ * as a per-token sum of K contiguous rows; deterministic, no atomics).
+ *   y_slot (n*K, H) dtype, y (n, H) dtype.
+ */
+moe_status_t moe_combine_slots(const moe_layer_desc_t *desc, const void *y_slot, void *y,
+                               moe_stream_t stream);
+
+/*
  * Whole layer for num_mb micro-batches that share one set of weights,
  * scheduled on two streams as in "XTuner Domino EP" (执行路径) and the
  * two-micro-batch interleave of "大模型系统中的通算融合" §3.1:
@@ -238,7 +270,8 @@ moe_status_t moe_combine(const moe_layer_desc_t *desc, const void *y_perm, const
  * dispatch == compute (or NULL) everything runs in order on one stream.
  *   x[j], y[j]: arrays of num_mb device pointers, each (n,H) dtype.
  *   ws: num_mb * moe_workspace_size(desc) bytes, 256-byte aligned; it holds
- *   each micro-batch's intermediates (logits, topk, layout, x_perm, h, y_perm).
+ *   each micro-batch's intermediates (logits, topk, layout, x_perm, h, y_perm;
+ *   for bf16 layers the y_perm slot holds moe_expert_gemm2_weighted's y_slot).
  *   status_word: one int32 (device) or NULL; cleared at the start of the call
  *   (stream-ordered) and then OR-ed into.  NULL uses a word inside ws.
  *   sm_reserve: SMs the GEMMs leave free for the dispatch stream.

@@ -97,31 +97,71 @@ def check_permute(run, sample_rows=None):
 
 
 def check_experts(run, sample_rows=None):
-    """GPU h and y_perm against the oracle's SwiGLU: GEMM1 on the oracle's
-    gather of x (Algorithm 2 step 7), GEMM2 on the GPU's (rounded) h."""
+    """GPU h and the GEMM2 output against the oracle's SwiGLU: GEMM1 on the
+    oracle's gather of x (Algorithm 2 step 7), GEMM2 on the GPU's (rounded) h.
+    bf16 layers: the workspace holds y_slot[perm[r]] = w[perm[r]] * Y[r]
+    (moe_expert_gemm2_weighted); float32 layers: y_perm[r] = Y[r]."""
     cfg = run.cfg
     off = run.np("offsets")
     perm = run.np("perm")
+    tw = run.np("topk_w").reshape(-1)
     h = run.view("h")
     yp = run.view("y_perm")
     nK = cfg.nK
     rows = np.arange(nK) if sample_rows is None else np.asarray(sorted(set(sample_rows)))
     experts = np.searchsorted(off, rows, side="right") - 1
     x64 = f64(run.x)
+    weighted = cfg.dtype == "bf16"
     hs, ys, ho, yo = [], [], [], []
     for e in np.unique(experts):
         r = rows[experts == e]
         ri = torch.as_tensor(r, device=h.device)
         ho.append(O.expert_up(O.permute(x64, perm[r], cfg.K), run.w13_get(int(e))))
-        yo.append(O.expert_down(f64(h[ri]), run.w2_get(int(e))))
+        ye = O.expert_down(f64(h[ri]), run.w2_get(int(e)))
+        if weighted:
+            f = perm[r]
+            yo.append(ye * tw[f][:, None])
+            ys.append(f64(yp[torch.as_tensor(f, device=yp.device)]))
+        else:
+            yo.append(ye)
+            ys.append(f64(yp[ri]))
         hs.append(f64(h[ri]))
-        ys.append(f64(yp[ri]))
     tol = TOL[cfg.dtype]
     eh = rel_fro(np.concatenate(hs), np.concatenate(ho))
     ey = rel_fro(np.concatenate(ys), np.concatenate(yo))
     assert eh <= tol, f"h error {eh:.3e}"
     assert ey <= tol, f"y_perm error {ey:.3e}"
     return eh, ey
+
+
+def check_unweighted_gemm2_and_combine(run, sample_rows=None):
+    """bf16: the unweighted pair moe_expert_gemm2 + moe_combine on the same h,
+    against the oracle and against the forward's y."""
+    import top_routing_dispatch_gb300 as M
+    cfg = run.cfg
+    if cfg.dtype != "bf16":
+        return
+    yp = torch.empty((cfg.nK, cfg.H), dtype=run.x.dtype, device=run.dev)
+    y = torch.empty_like(run.x)
+    st = torch.zeros(1, dtype=torch.int32, device=run.dev)
+    M.moe_expert_gemm2(run.desc, run.view("h"), run.L["w2"], run.view("offsets"), yp,
+                       status_word=st)
+    M.moe_combine(run.desc, yp, run.view("topk_w"), run.view("inv_perm"), y, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    off = run.np("offsets")
+    h = run.view("h")
+    rows = np.arange(cfg.nK) if sample_rows is None else np.asarray(sorted(set(sample_rows)))
+    experts = np.searchsorted(off, rows, side="right") - 1
+    ys, yo = [], []
+    for e in np.unique(experts):
+        r = rows[experts == e]
+        ri = torch.as_tensor(r, device=h.device)
+        yo.append(O.expert_down(f64(h[ri]), run.w2_get(int(e))))
+        ys.append(f64(yp[ri]))
+    assert rel_fro(np.concatenate(ys), np.concatenate(yo)) <= TOL[cfg.dtype]
+    # the same layer output up to the two bf16 roundings of y_perm vs y_slot
+    assert rel_fro(f64(y), f64(run.y)) <= 8e-3
 
 
 def check_gather_fusion(run):
@@ -149,7 +189,11 @@ def check_gather_fusion(run):
 
 def check_combine(run):
     cfg = run.cfg
-    yo = O.combine(run.np("y_perm"), run.np("topk_w"), run.np("inv_perm"))
+    if cfg.dtype == "bf16":   # y[t] = sum of the token's K weighted slot rows
+        ys = run.np("y_perm").reshape(cfg.n, cfg.K, cfg.H)
+        yo = ys.sum(axis=1)
+    else:
+        yo = O.combine(run.np("y_perm"), run.np("topk_w"), run.np("inv_perm"))
     err = rel_fro(f64(run.y), yo)
     assert err <= (4e-3 if cfg.dtype == "bf16" else 1e-6), err
 
@@ -174,6 +218,7 @@ def test_small_all_steps(cfg):
     check_permute(run)
     check_experts(run)
     check_gather_fusion(run)
+    check_unweighted_gemm2_and_combine(run)
     check_combine(run)
     check_layer(run)
 
@@ -201,6 +246,7 @@ def test_full_size(cfg):
             rng.choice(seg, size=min(64, len(seg)), replace=False))
     check_experts(run, rows)
     check_gather_fusion(run)
+    check_unweighted_gemm2_and_combine(run, rows)
     check_combine(run)
     toks = sorted(set(rng.choice(cfg.n, size=96, replace=False).tolist() + [0, cfg.n - 1]))
     check_layer(run, toks)

@@ -17,7 +17,8 @@ SYMBOLS = (
     "moe_dispatch_layout", "moe_dispatch_layout_noalloc", "moe_permute", "moe_grouped_swiglu", "moe_expert_gemm1_swiglu",
     "moe_expert_gemm1_swiglu_gather", "moe_expert_gemm2", "moe_combine",
     "moe_workspace_size", "moe_forward_microbatches", "moe_workspace_slot", "moe_check_status",
-    "moe_host_workspace_size", "moe_forward_host",
+    "moe_host_workspace_size", "moe_forward_host", "moe_expert_gemm2_weighted",
+    "moe_combine_slots",
 )
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -67,6 +68,9 @@ def _declare(lib):
         "moe_workspace_slot": (_vp, [_desc_p, _vp, ctypes.c_int, ctypes.c_int]),
         "moe_check_status": (_st, [_vp, _vp]),
         "moe_host_workspace_size": (ctypes.c_size_t, [_desc_p]),
+        "moe_expert_gemm2_weighted": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
+                                            _vp, _vp]),
+        "moe_combine_slots": (_st, [_desc_p, _vp, _vp, _vp]),
         "moe_forward_host": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                                    ctypes.c_longlong, _vp, _vp, _vp, _vp]),
     }

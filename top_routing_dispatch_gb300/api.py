@@ -124,6 +124,18 @@ def moe_expert_gemm2(desc, h, w2, offsets, y_perm, sm_reserve=0, status_word=Non
                                         _stream(stream)), "moe_expert_gemm2")
 
 
+def moe_expert_gemm2_weighted(desc, h, w2, offsets, perm, topk_w, y_slot, sm_reserve=0,
+                              status_word=None, stream=None):
+    _check(_lib.load().moe_expert_gemm2_weighted(
+        ctypes.byref(desc), _p(h), _p(w2), _p(offsets), _p(perm), _p(topk_w), _p(y_slot),
+        int(sm_reserve), _p(status_word), _stream(stream)), "moe_expert_gemm2_weighted")
+
+
+def moe_combine_slots(desc, y_slot, y, stream=None):
+    _check(_lib.load().moe_combine_slots(ctypes.byref(desc), _p(y_slot), _p(y), _stream(stream)),
+           "moe_combine_slots")
+
+
 def moe_combine(desc, y_perm, topk_w, inv_perm, y, status_word=None, stream=None):
     _check(_lib.load().moe_combine(ctypes.byref(desc), _p(y_perm), _p(topk_w), _p(inv_perm),
                                    _p(y), _p(status_word), _stream(stream)), "moe_combine")

@@ -67,6 +67,14 @@ cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *
                                    int sm_reserve, int32_t *status, cudaStream_t s);
 cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const int32_t *offsets,
                             void *y_perm, int sm_reserve, int32_t *status, cudaStream_t s);
+// GEMM2 with the routing weight applied and each row written to its
+// (token, slot) position: y_slot[perm[r]] = topk_w[perm[r]] * (h W2[e])[r]
+cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w2,
+                                     const int32_t *offsets, const int32_t *perm,
+                                     const float *topk_w, void *y_slot, int sm_reserve,
+                                     int32_t *status, cudaStream_t s);
+// y[t] = sum over k of y_slot[t*K + k] (float32, slot order, one rounding)
+cudaError_t launch_combine_slots(const Desc &d, const void *y_slot, void *y, cudaStream_t s);
 cudaError_t launch_gemm1_simt(const Desc &d, const void *x_perm, const void *w13,
                               const int32_t *offsets, void *h, int32_t *status, cudaStream_t s);
 cudaError_t launch_gemm2_simt(const Desc &d, const void *h, const void *w2,

@@ -139,8 +139,10 @@ __device__ __forceinline__ float silu(float g) {
 // rows per store instruction.  Rows are 80 B apart so that both the row-wise
 // writes and the segment-wise reads are (nearly) free of bank conflicts.
 
+// my_dst: the output row of this lane's tile row (-1: do not store); the
+// destination of tile row `row` is fetched from its lane.
 __device__ __forceinline__ void store_tile_chunk(uint8_t *wbuf, const uint32_t (&pk)[16], int lane,
-                                                 __nv_bfloat16 *out, size_t ld, int row0,
+                                                 __nv_bfloat16 *out, size_t ld, int my_dst,
                                                  int rows, int col0) {
   uint4 *mine = reinterpret_cast<uint4 *>(wbuf + lane * EPI_ROW_BYTES);
 #pragma unroll
@@ -150,16 +152,22 @@ __device__ __forceinline__ void store_tile_chunk(uint8_t *wbuf, const uint32_t (
   for (int i = 0; i < 4; ++i) {
     const int p = lane + 32 * i;
     const int row = p >> 2, c16 = p & 3;
-    if (row < rows) {
+    const int dst = __shfl_sync(0xffffffffu, my_dst, row);
+    if (row < rows && dst >= 0) {
       const uint4 val = *reinterpret_cast<const uint4 *>(wbuf + row * EPI_ROW_BYTES + c16 * 16);
-      *reinterpret_cast<uint4 *>(out + (size_t)(row0 + row) * ld + col0 + c16 * 8) = val;
+      *reinterpret_cast<uint4 *>(out + (size_t)dst * ld + col0 + c16 * 8) = val;
     }
   }
   __syncwarp();
 }
 
+__host__ __device__ constexpr bool gemm1_mode(int mode) { return mode == 1 || mode == 3; }
+
 // MODE 1: GEMM1 + SwiGLU (A = x_perm, B = W13, out = h, n-tile = 128 h columns)
 // MODE 2: GEMM2          (A = h,      B = W2,  out = y_perm, n-tile = 256 columns)
+// MODE 4: GEMM2 with the routing weight applied and the row scattered to its
+//         (token, slot) position: out[perm[r]] = topk_w[perm[r]] * (h W2)[r],
+//         so the combine reads each token's K rows as one contiguous block.
 // MODE 3: GEMM1 + SwiGLU with the permute fused into the A loads: the A rows of
 //         a tile are read straight from x (row perm[r] / K) by four gather
 //         warps with 16-byte cp.async, written in the same 128-byte swizzled
@@ -171,7 +179,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                            const int32_t *__restrict__ offsets, int E, int nK, int Kdim, int I,
                            int Nout, __nv_bfloat16 *__restrict__ out, int32_t *status,
                            const int32_t *__restrict__ perm, int Kslots,
-                           const __nv_bfloat16 *__restrict__ xg) {
+                           const __nv_bfloat16 *__restrict__ xg,
+                           const float *__restrict__ tw) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   SmemTail &st = *reinterpret_cast<SmemTail *>(smem + STAGES * STAGE_BYTES);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles = MODE != 2 ? I / 128 : (Nout + UMMA_N - 1) / UMMA_N;
+  const int n_tiles = gemm1_mode(MODE) ? I / 128 : (Nout + UMMA_N - 1) / UMMA_N;
   const int KB = Kdim / BK;
 
   if (tid == 0) {
@@ -253,7 +262,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             int ncol;
-            if (MODE != 2)
+            if (gemm1_mode(MODE))
               ncol = (q < 2 ? 0 : I) + ti.nt * 128 + (q & 1) * 64;
             else
               ncol = ti.nt * UMMA_N + q * 64;
@@ -333,7 +342,22 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       const int wrows = ti.rows - q * 32;
       const int wrow0 = ti.row0 + q * 32;
       uint8_t *wbuf = st.epi[q];
-      if (MODE != 2) {
+      // output row of this lane's tile row, and its routing weight (MODE 4)
+      int my_dst = wrow0 + lane;
+      float wscale = 1.f;
+      if (MODE == 4) {
+        my_dst = -1;
+        if (lane < wrows) {
+          const int f = __ldg(perm + wrow0 + lane);
+          if ((unsigned)f < (unsigned)nK) {
+            my_dst = f;
+            wscale = __ldg(tw + f);
+          } else {
+            flag_status(status, MOE_DEV_BAD_LAYOUT);
+          }
+        }
+      }
+      if (gemm1_mode(MODE)) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t g[32], u[32];
@@ -347,7 +371,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
             pk[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
           }
-          store_tile_chunk(wbuf, pk, lane, out, (size_t)I, wrow0, wrows, ti.nt * 128 + c * 32);
+          store_tile_chunk(wbuf, pk, lane, out, (size_t)I, my_dst, wrows, ti.nt * 128 + c * 32);
         }
       } else {
 #pragma unroll 1
@@ -358,9 +382,15 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           ptx::tmem_ld_wait();
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
-          store_tile_chunk(wbuf, pk, lane, out, (size_t)Nout, wrow0, wrows,
+          for (int i = 0; i < 16; ++i) {
+            float a0 = __uint_as_float(a[2 * i]), a1 = __uint_as_float(a[2 * i + 1]);
+            if (MODE == 4) {
+              a0 *= wscale;
+              a1 *= wscale;
+            }
+            pk[i] = pack_bf16x2(a0, a1);
+          }
+          store_tile_chunk(wbuf, pk, lane, out, (size_t)Nout, my_dst, wrows,
                            ti.nt * UMMA_N + c * 32);
         }
       }
@@ -518,7 +548,7 @@ cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
   if (e != cudaSuccess) return e;
   return launch_pdl(grouped_gemm_tc_kernel<1>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
                     SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
-                    reinterpret_cast<__nv_bfloat16 *>(h), status, nullptr, 0, nullptr);
+                    reinterpret_cast<__nv_bfloat16 *>(h), status, nullptr, 0, nullptr, nullptr);
 }
 
 cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *perm,
@@ -533,7 +563,7 @@ cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *
   return launch_pdl(grouped_gemm_tc_kernel<3>, dim3(gemm_grid(sm_reserve)), dim3(threads_for(3)),
                     SMEM_BYTES, s, mB, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
                     reinterpret_cast<__nv_bfloat16 *>(h), status, perm, d.K,
-                    reinterpret_cast<const __nv_bfloat16 *>(x));
+                    reinterpret_cast<const __nv_bfloat16 *>(x), nullptr);
 }
 
 cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const int32_t *offsets,
@@ -547,7 +577,25 @@ cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const 
   if (e != cudaSuccess) return e;
   return launch_pdl(grouped_gemm_tc_kernel<2>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
                     SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
-                    reinterpret_cast<__nv_bfloat16 *>(y_perm), status, nullptr, 0, nullptr);
+                    reinterpret_cast<__nv_bfloat16 *>(y_perm), status, nullptr, 0, nullptr,
+                    nullptr);
+}
+
+cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w2,
+                                     const int32_t *offsets, const int32_t *perm,
+                                     const float *topk_w, void *y_slot, int sm_reserve,
+                                     int32_t *status, cudaStream_t s) {
+  const long long nK = d.nK();
+  if (nK == 0) return cudaSuccess;
+  CUtensorMap mA, mB;
+  if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !make_map_3d(&mB, w2, d.H, d.I, d.E, 64, BK))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr<4>();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(grouped_gemm_tc_kernel<4>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
+                    SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
+                    reinterpret_cast<__nv_bfloat16 *>(y_slot), status, perm, d.K, nullptr,
+                    topk_w);
 }
 
 }  // namespace moe

@@ -250,6 +250,35 @@ moe_status_t moe_expert_gemm2(const moe_layer_desc_t *desc, const void *h, const
                             : launch_gemm2_simt(d, h, w2, offsets, y_perm, status_word, stream));
 }
 
+moe_status_t moe_expert_gemm2_weighted(const moe_layer_desc_t *desc, const void *h,
+                                       const void *w2, const int32_t *offsets,
+                                       const int32_t *perm, const float *topk_w, void *y_slot,
+                                       int sm_reserve, int32_t *status_word,
+                                       moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  if (!d.bf16) return MOE_ERR_UNSUPPORTED;
+  st = check_gemm_shape(d);
+  if (st != MOE_OK) return st;
+  if (d.nK() == 0) return MOE_OK;
+  if (!h || !w2 || !offsets || !perm || !topk_w || !y_slot || sm_reserve < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w2) || !aligned16(y_slot)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_gemm2_tc_weighted(d, h, w2, offsets, perm, topk_w, y_slot,
+                                              sm_reserve, status_word, stream));
+}
+
+moe_status_t moe_combine_slots(const moe_layer_desc_t *desc, const void *y_slot, void *y,
+                               moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  if (d.n == 0) return MOE_OK;
+  if (!y_slot || !y || !aligned16(y_slot) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine_slots(d, y_slot, y, stream));
+}
+
 moe_status_t moe_combine(const moe_layer_desc_t *desc, const void *y_perm, const float *topk_w,
                          const int32_t *inv_perm, void *y, int32_t *status_word,
                          moe_stream_t stream) {
@@ -315,12 +344,27 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
     return launch_permute(d, x[j], (int32_t *)slot_ptr(d, ws, j, S_PERM),
                           slot_ptr(d, ws, j, S_X_PERM), status, s);
   };
+  // bf16: GEMM2 applies the routing weights and writes each row to its
+  // (token, slot) position (slot y_perm of the workspace), and the combine
+  // adds each token's K contiguous rows; float32: GEMM2 writes y_perm in
+  // expert order and the combine gathers and weights
   auto experts = [&](int j, cudaStream_t s) -> cudaError_t {
-    return launch_experts(d, slot_ptr(d, ws, j, S_X_PERM), w13, w2,
-                          (const int32_t *)slot_ptr(d, ws, j, S_OFFSETS), slot_ptr(d, ws, j, S_H),
-                          slot_ptr(d, ws, j, S_Y_PERM), two ? sm_reserve : 0, status, s);
+    const int32_t *off = (const int32_t *)slot_ptr(d, ws, j, S_OFFSETS);
+    const int reserve = two ? sm_reserve : 0;
+    if (!d.bf16)
+      return launch_experts(d, slot_ptr(d, ws, j, S_X_PERM), w13, w2, off,
+                            slot_ptr(d, ws, j, S_H), slot_ptr(d, ws, j, S_Y_PERM), reserve,
+                            status, s);
+    cudaError_t e = launch_gemm1_tc(d, slot_ptr(d, ws, j, S_X_PERM), w13, off,
+                                    slot_ptr(d, ws, j, S_H), reserve, status, s);
+    if (e != cudaSuccess) return e;
+    return launch_gemm2_tc_weighted(d, slot_ptr(d, ws, j, S_H), w2, off,
+                                    (const int32_t *)slot_ptr(d, ws, j, S_PERM),
+                                    (const float *)slot_ptr(d, ws, j, S_TOPK_W),
+                                    slot_ptr(d, ws, j, S_Y_PERM), reserve, status, s);
   };
   auto back = [&](int j, cudaStream_t s) -> cudaError_t {
+    if (d.bf16) return launch_combine_slots(d, slot_ptr(d, ws, j, S_Y_PERM), y[j], s);
     return launch_combine(d, slot_ptr(d, ws, j, S_Y_PERM),
                           (const float *)slot_ptr(d, ws, j, S_TOPK_W),
                           (const int32_t *)slot_ptr(d, ws, j, S_INV_PERM), y[j], status, s);

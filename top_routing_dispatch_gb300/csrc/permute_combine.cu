@@ -85,7 +85,9 @@ __device__ __forceinline__ void acc_vec(float (&a)[8], uint4 v, float w, bool bf
 // item are loaded before they are accumulated.
 constexpr int CV = 64;  // vectors per combine item
 
-template <bool BF16, int KM>
+// SLOTS: the rows of token t are t*K .. t*K+K-1 of an already weighted,
+// slot-ordered array (GEMM2's weighted epilogue), added with weight 1.
+template <bool BF16, int KM, bool SLOTS = false>
 __global__ void __launch_bounds__(PT) combine_kernel(const uint4 *__restrict__ yp,
                                                      const float *__restrict__ tw,
                                                      const int32_t *__restrict__ inv,
@@ -111,9 +113,14 @@ __global__ void __launch_bounds__(PT) combine_kernel(const uint4 *__restrict__ y
       float my_w = 0.f;
       bool my_ok = true;
       if (lane < K) {
-        my_row = __ldg(inv + (size_t)t * K + lane);
-        my_w = __ldg(tw + (size_t)t * K + lane);
-        my_ok = my_row >= 0 && (long long)my_row < nK;
+        if (SLOTS) {
+          my_row = t * K + lane;
+          my_w = 1.f;
+        } else {
+          my_row = __ldg(inv + (size_t)t * K + lane);
+          my_w = __ldg(tw + (size_t)t * K + lane);
+          my_ok = my_row >= 0 && (long long)my_row < nK;
+        }
       }
       okmask = __ballot_sync(0xffffffffu, my_ok);
       if (okmask != 0xffffffffu && lane == 0 && v0 == lane) flag_status(status, MOE_DEV_BAD_LAYOUT);
@@ -173,27 +180,27 @@ int resident_grid() {
   return c;
 }
 
-template <bool BF16, int KM>
+template <bool BF16, int KM, bool SLOTS = false>
 cudaError_t combine_k(const Desc &d, const void *y_perm, const float *topk_w,
                       const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s) {
   const int V = (int)((size_t)d.H * elem_bytes(d) / 16);
   const long long items = (long long)d.n * ((V + CV - 1) / CV);
-  const long long res = resident_grid<combine_kernel<BF16, KM>>();
+  const long long res = resident_grid<combine_kernel<BF16, KM, SLOTS>>();
   const long long want = (items + (PT / 32) - 1) / (PT / 32);
   const int grid = (int)(want < res ? want : res);
-  return launch_pdl(combine_kernel<BF16, KM>, dim3(grid), dim3(PT), 0, s,
+  return launch_pdl(combine_kernel<BF16, KM, SLOTS>, dim3(grid), dim3(PT), 0, s,
                     reinterpret_cast<const uint4 *>(y_perm), topk_w, inv_perm,
                     reinterpret_cast<uint4 *>(y), d.n, d.K, V, d.nK(), status);
 }
 
-template <bool BF16>
+template <bool BF16, bool SLOTS = false>
 cudaError_t combine_dispatch_k(const Desc &d, const void *y_perm, const float *topk_w,
                                const int32_t *inv_perm, void *y, int32_t *status,
                                cudaStream_t s) {
-  if (d.K <= 2) return combine_k<BF16, 2>(d, y_perm, topk_w, inv_perm, y, status, s);
-  if (d.K <= 4) return combine_k<BF16, 4>(d, y_perm, topk_w, inv_perm, y, status, s);
-  if (d.K <= 8) return combine_k<BF16, 8>(d, y_perm, topk_w, inv_perm, y, status, s);
-  return combine_k<BF16, kMaxK>(d, y_perm, topk_w, inv_perm, y, status, s);
+  if (d.K <= 2) return combine_k<BF16, 2, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s);
+  if (d.K <= 4) return combine_k<BF16, 4, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s);
+  if (d.K <= 8) return combine_k<BF16, 8, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s);
+  return combine_k<BF16, kMaxK, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s);
 }
 
 }  // namespace
@@ -208,6 +215,12 @@ cudaError_t launch_permute(const Desc &d, const void *x, const int32_t *perm, vo
   return launch_pdl(permute_kernel, dim3((int)(want < res ? want : res)), dim3(PT), 0, s,
                     reinterpret_cast<const uint4 *>(x), perm, reinterpret_cast<uint4 *>(x_perm),
                     nK, d.K, V, status);
+}
+
+cudaError_t launch_combine_slots(const Desc &d, const void *y_slot, void *y, cudaStream_t s) {
+  if (d.n == 0) return cudaSuccess;
+  if (d.bf16) return combine_dispatch_k<true, true>(d, y_slot, nullptr, nullptr, y, nullptr, s);
+  return combine_dispatch_k<false, true>(d, y_slot, nullptr, nullptr, y, nullptr, s);
 }
 
 cudaError_t launch_combine(const Desc &d, const void *y_perm, const float *topk_w,
