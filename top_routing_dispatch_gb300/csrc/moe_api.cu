@@ -102,7 +102,7 @@ uint8_t *slot_ptr(const Desc &d, void *ws, int mb, int which) {
 // safe; the mutex serialises enqueueing from several host threads.
 constexpr int kMaxMB = 64;
 struct EventPool {
-  cudaEvent_t ev[2 * kMaxMB + 2];
+  cudaEvent_t ev[3 * kMaxMB + 2];
   bool ready = false;
 };
 EventPool g_pools[64];
@@ -329,20 +329,26 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
   cudaStream_t sd = dispatch ? dispatch : compute;
   const bool two = sd != sc;
 
-  auto front = [&](int j, cudaStream_t s) -> cudaError_t {  // route + layout + permute
-    int32_t *idx = (int32_t *)slot_ptr(d, ws, j, S_TOPK_IDX);
-    cudaError_t e = launch_router(d, x[j], w_gate, bias, idx,
-                                  (float *)slot_ptr(d, ws, j, S_TOPK_W),
-                                  (float *)slot_ptr(d, ws, j, S_LOGITS), status, s);
-    if (e != cudaSuccess) return e;
-    e = launch_layout(d, idx, (int32_t *)slot_ptr(d, ws, j, S_COUNTS),
-                      (int32_t *)slot_ptr(d, ws, j, S_OFFSETS),
-                      (int32_t *)slot_ptr(d, ws, j, S_PERM),
-                      (int32_t *)slot_ptr(d, ws, j, S_INV_PERM), status,
-                      slot_ptr(d, ws, j, S_LAYOUT_WS), s);
+  auto route = [&](int j, cudaStream_t s) -> cudaError_t {
+    return launch_router(d, x[j], w_gate, bias, (int32_t *)slot_ptr(d, ws, j, S_TOPK_IDX),
+                         (float *)slot_ptr(d, ws, j, S_TOPK_W),
+                         (float *)slot_ptr(d, ws, j, S_LOGITS), status, s);
+  };
+  auto layout_permute = [&](int j, cudaStream_t s) -> cudaError_t {
+    cudaError_t e = launch_layout(d, (const int32_t *)slot_ptr(d, ws, j, S_TOPK_IDX),
+                                  (int32_t *)slot_ptr(d, ws, j, S_COUNTS),
+                                  (int32_t *)slot_ptr(d, ws, j, S_OFFSETS),
+                                  (int32_t *)slot_ptr(d, ws, j, S_PERM),
+                                  (int32_t *)slot_ptr(d, ws, j, S_INV_PERM), status,
+                                  slot_ptr(d, ws, j, S_LAYOUT_WS), s);
     if (e != cudaSuccess) return e;
     return launch_permute(d, x[j], (int32_t *)slot_ptr(d, ws, j, S_PERM),
                           slot_ptr(d, ws, j, S_X_PERM), status, s);
+  };
+  auto front = [&](int j, cudaStream_t s) -> cudaError_t {  // route + layout + permute
+    cudaError_t e = route(j, s);
+    if (e != cudaSuccess) return e;
+    return layout_permute(j, s);
   };
   // bf16: GEMM2 applies the routing weights and writes each row to its
   // (token, slot) position (slot y_perm of the workspace), and the combine
@@ -385,20 +391,35 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
   std::lock_guard<std::mutex> lock(g_pool_mu);
   EventPool &pool = g_pools[dev];
   if (!pool.ready) {
-    for (int i = 0; i < 2 * kMaxMB + 2; ++i)
+    for (int i = 0; i < 3 * kMaxMB + 2; ++i)
       if (cudaEventCreateWithFlags(&pool.ev[i], cudaEventDisableTiming) != cudaSuccess)
         return MOE_ERR_CUDA;
     pool.ready = true;
   }
-  cudaEvent_t ev_start = pool.ev[2 * kMaxMB], ev_done = pool.ev[2 * kMaxMB + 1];
-  cudaEvent_t *ev_front = pool.ev, *ev_gemm = pool.ev + kMaxMB;
+  cudaEvent_t ev_start = pool.ev[3 * kMaxMB], ev_done = pool.ev[3 * kMaxMB + 1];
+  cudaEvent_t *ev_front = pool.ev, *ev_gemm = pool.ev + kMaxMB, *ev_route = pool.ev + 2 * kMaxMB;
 
-  // the dispatch stream starts after whatever the caller queued on `compute`
+  // Schedule (D = dispatch stream, C = compute stream):
+  //   D: route(0) | layout+permute(0) | layout+permute(1) | combine(0) | layout+permute(2) | ...
+  //   C:          | route(1)  | GEMMs(0)                  | route(2) | GEMMs(1)           | ...
+  // The router of micro-batch j+1 runs on C right before GEMMs(j), beside
+  // micro-batch j's layout and permute; j+1's layout and permute run beside
+  // GEMMs(j) and combine(j) beside GEMMs(j+1).  Only the router's tile kernel
+  // cannot share an SM with a GEMM CTA (both need most of the shared memory),
+  // so it is placed where the other stream runs memory-bound kernels.
   cudaError_t e = cudaEventRecord(ev_start, sc);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_start, 0);
   if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), sd);
+  if (e == cudaSuccess) e = route(0, sd);
+  if (e == cudaSuccess) e = cudaEventRecord(ev_route[0], sd);
   for (int j = 0; j < num_mb && e == cudaSuccess; ++j) {
-    e = front(j, sd);                                            // dispatch of j
+    if (j + 1 < num_mb) {                                        // route of j+1 on C
+      e = cudaStreamWaitEvent(sc, ev_route[j], 0);
+      if (e == cudaSuccess) e = route(j + 1, sc);
+      if (e == cudaSuccess) e = cudaEventRecord(ev_route[j + 1], sc);
+    }
+    if (e == cudaSuccess && j > 0) e = cudaStreamWaitEvent(sd, ev_route[j], 0);
+    if (e == cudaSuccess) e = layout_permute(j, sd);             // rest of j's dispatch
     if (e == cudaSuccess) e = cudaEventRecord(ev_front[j], sd);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, ev_front[j], 0);
     if (e == cudaSuccess) e = experts(j, sc);                    // experts of j
