@@ -295,6 +295,38 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
 void *moe_workspace_slot(const moe_layer_desc_t *desc, void *ws, int mb, int which);
 
 /*
+ * Backward of the layer for an upstream gradient dy = dL/dy (bf16 layers,
+ * H % 256 == 0, I % 128 == 0), with the expert choice of the forward held
+ * fixed (as differentiating a top-k selection does).  The pages give the
+ * structure: in training the backward of dispatch is a combine and the
+ * backward of combine is a dispatch ("大模型系统中的通算融合" §6.2.4), and
+ * the top-k reduce and the routing scores have their own backward kernels
+ * (DModel notes "0. goin", §2.3).  Steps:
+ *   dY[r] = w[f] dy[t], dw[f] = <dy[t], Y[r]>          (f = t*K + k, r = inv_perm[f])
+ *   dh = dY W2[e]^T;  dG = dh U s (1 + G (1 - s)), dU = dh G s  (s = sigmoid(G),
+ *   G|U recomputed from x_perm W13[e]);  dX = [dG|dU] W13[e]^T
+ *   dW2[e] = h_e^T dY_e;  dW13[e] = x_perm_e^T [dG|dU]_e
+ *   dp from dw (through the renormalisation when norm_topk_prob),
+ *   dlogits = p (dp - <p, dp>);  dx = sum_k dX[inv_perm[t*K+k]] + dlogits W_gate^T;
+ *   dW_gate = x^T dlogits;  dbias = sum_t dlogits[t]
+ * Inputs: the layer (x (n,H), w_gate (H,E), w13, w2), dy (n,H) bf16, and the
+ * forward's intermediates as written by moe_route_topk (logits, topk_idx,
+ * topk_w), moe_dispatch_layout (offsets, inv_perm), moe_permute (x_perm),
+ * moe_expert_gemm1_swiglu (h) and the UNWEIGHTED moe_expert_gemm2 (y_perm).
+ * Outputs: dx (n,H) bf16; dw_gate (H,E), dbias (E, or NULL), dw13 (E,H,2I),
+ * dw2 (E,I,H) float32.  ws: moe_backward_workspace_size(desc) bytes, 256-byte
+ * aligned.  Every sum has a fixed order (bitwise reproducible).
+ */
+size_t moe_backward_workspace_size(const moe_layer_desc_t *desc);
+moe_status_t moe_backward(const moe_layer_desc_t *desc, const void *x, const void *w_gate,
+                          const void *w13, const void *w2, const void *dy, const float *logits,
+                          const int32_t *topk_idx, const float *topk_w, const int32_t *offsets,
+                          const int32_t *inv_perm, const void *x_perm, const void *h,
+                          const void *y_perm, void *dx, float *dw_gate, float *dbias,
+                          float *dw13, float *dw2, void *ws, size_t ws_bytes,
+                          int32_t *status_word, moe_stream_t stream);
+
+/*
  * Device bytes moe_forward_host needs: one layer workspace and two staging
  * slots (x and y of one call each).  0 for an invalid descriptor.
  */

@@ -1,0 +1,101 @@
+"""GPU backward (moe_backward) against the fp64 backward oracle
+(oracle/moe_backward.py) on the same seeded inputs, through the C ABI.
+The forward intermediates come from the library's own entry points (router,
+layout, permute, GEMM1 + SwiGLU, unweighted GEMM2); near-tie tokens use the
+GPU's expert choice in the oracle, as the forward parity tests do."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from oracle import moe_backward as OB
+from tests.gpu_helpers import NEAR_TIE_GAP, rel_fro, f64
+from workloads import synth
+from workloads.configs import MoEConfig
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    MoEConfig("bwd_bf16", n=384, H=256, I=128, E=8, K=2, dtype="bf16", norm_topk_prob=True,
+              seed=41),
+    MoEConfig("bwd_skew_e64", n=600, H=512, I=256, E=64, K=6, dtype="bf16",
+              norm_topk_prob=False, seed=42, skew=True),
+    MoEConfig("bwd_one_token", n=1, H=256, I=128, E=8, K=2, dtype="bf16", norm_topk_prob=True,
+              seed=43),
+]
+TOL = 2e-2
+
+
+def _run(cfg):
+    import top_routing_dispatch_gb300 as M
+    dev = torch.device("cuda:0")
+    L = synth.make_layer(cfg, dev)
+    x = synth.make_x(cfg, dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(synth.sub_seed(cfg.seed, "dy"))
+    dy = torch.randn((cfg.n, cfg.H), generator=g, device=dev).to(torch.bfloat16)
+    desc = M.desc_for(cfg)
+    n, H, I, E, K, nK = cfg.n, cfg.H, cfg.I, cfg.E, cfg.K, cfg.nK
+    i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+    logits = torch.empty((n, E), dtype=f32, device=dev)
+    idx = torch.empty((n, K), dtype=i32, device=dev)
+    w = torch.empty((n, K), dtype=f32, device=dev)
+    counts = torch.empty(E, dtype=i32, device=dev)
+    offsets = torch.empty(E + 1, dtype=i32, device=dev)
+    perm = torch.empty(nK, dtype=i32, device=dev)
+    inv = torch.empty(nK, dtype=i32, device=dev)
+    st = torch.zeros(1, dtype=i32, device=dev)
+    lws = torch.empty(max(M.moe_layout_workspace_size(desc), 1), dtype=torch.uint8, device=dev)
+    xp = torch.empty((nK, H), dtype=bf, device=dev)
+    h = torch.empty((nK, I), dtype=bf, device=dev)
+    yp = torch.empty((nK, H), dtype=bf, device=dev)
+    M.moe_route_topk(desc, x, L["w_gate"], L["bias"], idx, w, logits)
+    M.moe_dispatch_layout(desc, idx, counts, offsets, perm, inv, st, lws)
+    M.moe_permute(desc, x, perm, xp, st)
+    M.moe_expert_gemm1_swiglu(desc, xp, L["w13"], offsets, h, status_word=st)
+    M.moe_expert_gemm2(desc, h, L["w2"], offsets, yp, status_word=st)
+    dx = torch.empty_like(x)
+    dwg = torch.empty((H, E), dtype=f32, device=dev)
+    dbias = torch.empty(E, dtype=f32, device=dev)
+    dw13 = torch.empty((E, H, 2 * I), dtype=f32, device=dev)
+    dw2 = torch.empty((E, I, H), dtype=f32, device=dev)
+    ws = torch.empty(M.moe_backward_workspace_size(desc), dtype=torch.uint8, device=dev)
+    M.moe_backward(desc, x, L["w_gate"], L["w13"], L["w2"], dy, logits, idx, w, offsets, inv, xp,
+                   h, yp, dx, dwg, dbias, dw13, dw2, ws, st)
+    torch.cuda.synchronize()
+    return dict(L=L, x=x, dy=dy, idx=idx, status=int(st.item()), dx=dx, dwg=dwg, dbias=dbias,
+                dw13=dw13, dw2=dw2)
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
+def test_backward_matches_oracle(cfg):
+    r = _run(cfg)
+    assert r["status"] == 0
+    L = r["L"]
+    x64 = f64(r["x"])
+    wg64 = f64(L["w_gate"])
+    b64 = f64(L["bias"])
+    lo = O.router_logits(x64, wg64, b64)
+    near = O.near_tie_tokens(lo, cfg.K, NEAR_TIE_GAP)
+    gidx = r["idx"].cpu().numpy()
+    forced = (np.where(near)[0], gidx[near])
+    w13 = lambda e: L["w13"][e].to(torch.float64).cpu().numpy()
+    w2 = lambda e: L["w2"][e].to(torch.float64).cpu().numpy()
+    o = OB.moe_backward(x64, wg64, b64, w13, w2, cfg.K, cfg.norm_topk_prob, f64(r["dy"]),
+                        forced=forced)
+    errs = dict(dx=rel_fro(f64(r["dx"]), o["dx"]),
+                dw_gate=rel_fro(f64(r["dwg"]), o["dw_gate"]),
+                dw13=rel_fro(f64(r["dw13"]), o["dw13"]),
+                dw2=rel_fro(f64(r["dw2"]), o["dw2"]))
+    if cfg.skew:
+        errs["dbias"] = rel_fro(f64(r["dbias"]), o["dbias"])
+    print(cfg.name, {k: f"{v:.2e}" for k, v in errs.items()})
+    for k, v in errs.items():
+        assert v <= TOL, (k, v)
+
+
+def test_backward_is_deterministic():
+    cfg = CASES[0]
+    a, b = _run(cfg), _run(cfg)
+    for k in ("dx", "dwg", "dbias", "dw13", "dw2"):
+        assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), k

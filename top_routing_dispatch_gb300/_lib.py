@@ -18,7 +18,7 @@ SYMBOLS = (
     "moe_expert_gemm1_swiglu_gather", "moe_expert_gemm2", "moe_combine",
     "moe_workspace_size", "moe_forward_microbatches", "moe_workspace_slot", "moe_check_status",
     "moe_host_workspace_size", "moe_forward_host", "moe_expert_gemm2_weighted",
-    "moe_combine_slots",
+    "moe_combine_slots", "moe_backward_workspace_size", "moe_backward",
 )
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -71,6 +71,8 @@ def _declare(lib):
         "moe_expert_gemm2_weighted": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                             _vp, _vp]),
         "moe_combine_slots": (_st, [_desc_p, _vp, _vp, _vp]),
+        "moe_backward_workspace_size": (ctypes.c_size_t, [_desc_p]),
+        "moe_backward": (_st, [_desc_p] + [_vp] * 19 + [ctypes.c_size_t, _vp, _vp]),
         "moe_forward_host": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                                    ctypes.c_longlong, _vp, _vp, _vp, _vp]),
     }

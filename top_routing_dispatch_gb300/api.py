@@ -240,6 +240,21 @@ class MoELayer:
         _check(moe_check_status(self.status, stream), "device status")
 
 
+def moe_backward_workspace_size(desc) -> int:
+    return int(_lib.load().moe_backward_workspace_size(ctypes.byref(desc)))
+
+
+def moe_backward(desc, x, w_gate, w13, w2, dy, logits, topk_idx, topk_w, offsets, inv_perm,
+                 x_perm, h, y_perm, dx, dw_gate, dbias, dw13, dw2, ws, status_word=None,
+                 stream=None):
+    nbytes = ws.numel() * ws.element_size()
+    _check(_lib.load().moe_backward(
+        ctypes.byref(desc), _p(x), _p(w_gate), _p(w13), _p(w2), _p(dy), _p(logits), _p(topk_idx),
+        _p(topk_w), _p(offsets), _p(inv_perm), _p(x_perm), _p(h), _p(y_perm), _p(dx),
+        _p(dw_gate), _p(dbias), _p(dw13), _p(dw2), _p(ws), nbytes, _p(status_word),
+        _stream(stream)), "moe_backward")
+
+
 class HostPipeline:
     """moe_forward_host over one staging workspace: each call enqueues the copy
     of a pinned host x in, the layer, and the copy of y out, on three streams,

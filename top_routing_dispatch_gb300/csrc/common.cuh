@@ -75,6 +75,24 @@ cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w
                                      int32_t *status, cudaStream_t s);
 // y[t] = sum over k of y_slot[t*K + k] (float32, slot order, one rounding)
 cudaError_t launch_combine_slots(const Desc &d, const void *y_slot, void *y, cudaStream_t s);
+// backward (backward.cu, gemm_tc.cu modes 5 and 6, gemm_wgrad.cu)
+cudaError_t launch_combine_bwd(const Desc &d, const void *dy, const void *y_perm,
+                               const float *topk_w, const int32_t *inv_perm, void *dY, float *dw,
+                               int32_t *status, cudaStream_t s);
+cudaError_t launch_router_bwd(const Desc &d, const void *x, const void *w_gate,
+                              const float *logits, const int32_t *topk_idx, const float *topk_w,
+                              const float *dw, float *dlogits, float *dx_router,
+                              float *dw_gate, float *dbias, cudaStream_t s);
+cudaError_t launch_dx_gather(const Desc &d, const void *dx_perm, const float *dx_router,
+                             const int32_t *inv_perm, void *dx, cudaStream_t s);
+cudaError_t launch_gemm_dgrad_tc(const Desc &d, const void *a, const void *w, int Kdim, int Nout,
+                                 const int32_t *offsets, void *out, int32_t *status,
+                                 cudaStream_t s);
+cudaError_t launch_gemm1_swiglu_bwd_tc(const Desc &d, const void *x_perm, const void *w13,
+                                       const int32_t *offsets, const void *dh, void *dgu,
+                                       int32_t *status, cudaStream_t s);
+cudaError_t launch_wgrad_tc(const Desc &d, const void *a, int M, const void *b, int N,
+                            const int32_t *offsets, float *out, int32_t *status, cudaStream_t s);
 cudaError_t launch_gemm1_simt(const Desc &d, const void *x_perm, const void *w13,
                               const int32_t *offsets, void *h, int32_t *status, cudaStream_t s);
 cudaError_t launch_gemm2_simt(const Desc &d, const void *h, const void *w2,

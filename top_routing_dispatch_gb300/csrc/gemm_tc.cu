@@ -72,6 +72,7 @@ constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_
                               sizeof(SmemTail);
 
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/true);
+constexpr uint32_t IDESC_KB = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/false);
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
                                               volatile int *abort_flag, int32_t *status) {
@@ -161,7 +162,12 @@ __device__ __forceinline__ void store_tile_chunk(uint8_t *wbuf, const uint32_t (
   __syncwarp();
 }
 
-__host__ __device__ constexpr bool gemm1_mode(int mode) { return mode == 1 || mode == 3; }
+// modes whose B is W13's gate/up column pairs (n-tile = 128 h columns)
+__host__ __device__ constexpr bool gemm1_mode(int mode) {
+  return mode == 1 || mode == 3 || mode == 6;
+}
+// mode 5: B stored n-major (rows n, k contiguous): a K-major UMMA operand
+__host__ __device__ constexpr bool kmajor_b(int mode) { return mode == 5; }
 
 // MODE 1: GEMM1 + SwiGLU (A = x_perm, B = W13, out = h, n-tile = 128 h columns)
 // MODE 2: GEMM2          (A = h,      B = W2,  out = y_perm, n-tile = 256 columns)
@@ -180,7 +186,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                            int Nout, __nv_bfloat16 *__restrict__ out, int32_t *status,
                            const int32_t *__restrict__ perm, int Kslots,
                            const __nv_bfloat16 *__restrict__ xg,
-                           const float *__restrict__ tw) {
+                           const float *__restrict__ tw,
+                           const __nv_bfloat16 *__restrict__ aux) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -259,15 +266,20 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           if (MODE != 3)
             ptx::tma_load_2d(smemA + stage * A_STAGE_BYTES, &tmA, &st.full[stage], kb * BK,
                              ti.row0);
+          if (kmajor_b(MODE)) {  // one box: 64 k x 256 n rows
+            ptx::tma_load_3d(smemB + stage * B_STAGE_BYTES, &tmB, &st.full[stage], kb * BK,
+                             ti.nt * UMMA_N, ti.e);
+          } else {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            int ncol;
-            if (gemm1_mode(MODE))
-              ncol = (q < 2 ? 0 : I) + ti.nt * 128 + (q & 1) * 64;
-            else
-              ncol = ti.nt * UMMA_N + q * 64;
-            ptx::tma_load_3d(smemB + stage * B_STAGE_BYTES + q * B_BOX_BYTES, &tmB,
-                             &st.full[stage], ncol, kb * BK, ti.e);
+            for (int q = 0; q < 4; ++q) {
+              int ncol;
+              if (gemm1_mode(MODE))
+                ncol = (q < 2 ? 0 : I) + ti.nt * 128 + (q & 1) * 64;
+              else
+                ncol = ti.nt * UMMA_N + q * 64;
+              ptx::tma_load_3d(smemB + stage * B_STAGE_BYTES + q * B_BOX_BYTES, &tmB,
+                               &st.full[stage], ncol, kb * BK, ti.e);
+            }
           }
           used |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -309,9 +321,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             // A: K-major SW128, k step of 16 elements = 32 bytes inside the atom
             const uint64_t adesc = ptx::smem_desc(a0 + kk * 32, 16, 1024);
-            // B: MN-major SW128, 64-wide n atoms 8 KB apart, k step = 16 rows
-            const uint64_t bdesc = ptx::smem_desc(b0 + kk * 2048, B_BOX_BYTES, 1024);
-            ptx::mma_bf16(d, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            // B: MN-major SW128, 64-wide n atoms 8 KB apart, k step = 16 rows;
+            // or (mode 5) K-major SW128 like A, 256 n rows
+            const uint64_t bdesc = kmajor_b(MODE) ? ptx::smem_desc(b0 + kk * 32, 16, 1024)
+                                                  : ptx::smem_desc(b0 + kk * 2048, B_BOX_BYTES, 1024);
+            ptx::mma_bf16(d, adesc, bdesc, kmajor_b(MODE) ? IDESC_KB : IDESC,
+                          (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit(&st.empty[stage]);
           if (++stage == STAGES) {
@@ -364,14 +379,54 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           ptx::tmem_ld_32x32b_x32(tbase + c * 32, g);
           ptx::tmem_ld_32x32b_x32(tbase + 128 + c * 32, u);
           ptx::tmem_ld_wait();
-          uint32_t pk[16];
+          const int col = ti.nt * 128 + c * 32;
+          if (MODE == 6) {
+            // SwiGLU backward: dG = dh U s (1 + G (1 - s)), dU = dh G s, s = sigmoid(G)
+            float dh[32];
+            if (lane < wrows) {
+              const uint4 *src = reinterpret_cast<const uint4 *>(aux + (size_t)(wrow0 + lane) * I + col);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-            const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-            pk[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+              for (int v = 0; v < 4; ++v) {
+                const uint4 q4 = __ldg(src + v);
+                const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&q4);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float2 f = __bfloat1622float2(b2[j]);
+                  dh[8 * v + 2 * j] = f.x;
+                  dh[8 * v + 2 * j + 1] = f.y;
+                }
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) dh[i] = 0.f;
+            }
+            uint32_t pg[16], pu[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float dg[2], du[2];
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const float gv = __uint_as_float(g[2 * i + j]), uv = __uint_as_float(u[2 * i + j]);
+                const float sg = __fdividef(1.f, 1.f + __expf(fminf(-gv, 80.f)));
+                const float d = dh[2 * i + j];
+                dg[j] = d * uv * sg * (1.f + gv * (1.f - sg));
+                du[j] = d * gv * sg;
+              }
+              pg[i] = pack_bf16x2(dg[0], dg[1]);
+              pu[i] = pack_bf16x2(du[0], du[1]);
+            }
+            store_tile_chunk(wbuf, pg, lane, out, (size_t)Nout, my_dst, wrows, col);
+            store_tile_chunk(wbuf, pu, lane, out, (size_t)Nout, my_dst, wrows, I + col);
+          } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+              const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+              pk[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+            }
+            store_tile_chunk(wbuf, pk, lane, out, (size_t)I, my_dst, wrows, col);
           }
-          store_tile_chunk(wbuf, pk, lane, out, (size_t)I, my_dst, wrows, ti.nt * 128 + c * 32);
         }
       } else {
 #pragma unroll 1
@@ -548,7 +603,8 @@ cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
   if (e != cudaSuccess) return e;
   return launch_pdl(grouped_gemm_tc_kernel<1>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
                     SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
-                    reinterpret_cast<__nv_bfloat16 *>(h), status, nullptr, 0, nullptr, nullptr);
+                    reinterpret_cast<__nv_bfloat16 *>(h), status, nullptr, 0, nullptr, nullptr,
+                    nullptr);
 }
 
 cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *perm,
@@ -563,7 +619,7 @@ cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *
   return launch_pdl(grouped_gemm_tc_kernel<3>, dim3(gemm_grid(sm_reserve)), dim3(threads_for(3)),
                     SMEM_BYTES, s, mB, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
                     reinterpret_cast<__nv_bfloat16 *>(h), status, perm, d.K,
-                    reinterpret_cast<const __nv_bfloat16 *>(x), nullptr);
+                    reinterpret_cast<const __nv_bfloat16 *>(x), nullptr, nullptr);
 }
 
 cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const int32_t *offsets,
@@ -578,7 +634,7 @@ cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const 
   return launch_pdl(grouped_gemm_tc_kernel<2>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
                     SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
                     reinterpret_cast<__nv_bfloat16 *>(y_perm), status, nullptr, 0, nullptr,
-                    nullptr);
+                    nullptr, nullptr);
 }
 
 cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w2,
@@ -595,7 +651,42 @@ cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w
   return launch_pdl(grouped_gemm_tc_kernel<4>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
                     SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
                     reinterpret_cast<__nv_bfloat16 *>(y_slot), status, perm, d.K, nullptr,
-                    topk_w);
+                    topk_w, nullptr);
+}
+
+cudaError_t launch_gemm_dgrad_tc(const Desc &d, const void *a, const void *w, int Kdim, int Nout,
+                                 const int32_t *offsets, void *out, int32_t *status,
+                                 cudaStream_t s) {
+  const long long nK = d.nK();
+  if (nK == 0) return cudaSuccess;
+  CUtensorMap mA, mB;
+  // A (nK, Kdim) K-major; W[e] (Nout, Kdim): rows n with k contiguous
+  if (!make_map_2d(&mA, a, Kdim, nK, BK, BM) ||
+      !make_map_3d(&mB, w, Kdim, Nout, d.E, BK, UMMA_N))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr<5>();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(grouped_gemm_tc_kernel<5>, dim3(gemm_grid(0)), dim3(threads_for(5)),
+                    SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, Kdim, 0, Nout,
+                    reinterpret_cast<__nv_bfloat16 *>(out), status, nullptr, 0, nullptr, nullptr,
+                    nullptr);
+}
+
+cudaError_t launch_gemm1_swiglu_bwd_tc(const Desc &d, const void *x_perm, const void *w13,
+                                       const int32_t *offsets, const void *dh, void *dgu,
+                                       int32_t *status, cudaStream_t s) {
+  const long long nK = d.nK();
+  if (nK == 0) return cudaSuccess;
+  CUtensorMap mA, mB;
+  if (!make_map_2d(&mA, x_perm, d.H, nK, BK, BM) ||
+      !make_map_3d(&mB, w13, 2ull * d.I, d.H, d.E, 64, BK))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr<6>();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(grouped_gemm_tc_kernel<6>, dim3(gemm_grid(0)), dim3(threads_for(6)),
+                    SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, 2 * d.I,
+                    reinterpret_cast<__nv_bfloat16 *>(dgu), status, nullptr, 0, nullptr, nullptr,
+                    reinterpret_cast<const __nv_bfloat16 *>(dh));
 }
 
 }  // namespace moe

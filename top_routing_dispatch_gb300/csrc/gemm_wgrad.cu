@@ -1,0 +1,341 @@
+// Weight gradients of the expert GEMMs on the tcgen05 tensor cores:
+//   dW2[e]  = h_e^T dY_e        (I x H)      dW13[e] = X_e^T [dG | dU]_e   (H x 2I)
+// where _e are the rows [offsets[e], offsets[e+1]) of the expert-ordered
+// arrays (the backward of Algorithm 2 steps 8-9 of "MoE 分布式推理基础（基于
+// vLLM）" §1.2, with the expert's routed rows as the reduction dimension).
+//
+// C_e = A_e^T B_e with A (rows x M) and B (rows x N) row-major: both are
+// MN-major UMMA operands (M or N contiguous), loaded by TMA as 64-wide,
+// 64-row boxes with the 128-byte swizzle (the same layout as the forward's
+// weight operand).  Tiles are (expert, 128 M rows, 256 N columns); the K loop
+// runs over the expert's rows in blocks of 64, starting at the segment start.
+// In the last block the rows past the segment belong to the next expert: the
+// MMA warp zeroes those k-rows of the B stage (whole 128-byte lines in this
+// layout) and makes the writes visible to the tensor cores with a proxy fence
+// before issuing the MMAs.  A tile of an expert without rows is written as
+// zeros.  float32 output, one CTA per SM, persistent, double-buffered TMEM
+// accumulators as in gemm_tc.cu.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int WM = 128, WN = 256, WK = 64, WSTAGES = 4;
+constexpr int WA_BOX = 64 * WK * 2;               // 8 KB: 64 m x 64 k
+constexpr int WA_STAGE = 2 * WA_BOX;              // 16 KB
+constexpr int WB_BOX = 64 * WK * 2;               // 8 KB: 64 n x 64 k
+constexpr int WB_STAGE = 4 * WB_BOX;              // 32 KB
+constexpr int WSTAGE = WA_STAGE + WB_STAGE;
+constexpr int W_THREADS = 192;
+constexpr int W_TMEM = 512;
+
+struct WTail {
+  uint64_t full[WSTAGES];
+  uint64_t empty[WSTAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int ok;
+  int off[kMaxE + 1];
+};
+
+constexpr size_t W_SMEM = 1024 + (size_t)WSTAGES * WSTAGE + sizeof(WTail);
+constexpr uint32_t W_IDESC = ptx::idesc_bf16_f32(WM, WN, /*a_mn=*/true, /*b_mn=*/true);
+
+__device__ __forceinline__ bool w_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                       int32_t *status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > ptx::kWaitLimitCycles) {
+      *abort_flag = 1;
+      flag_status(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+struct WTile {
+  int e, m0, n0, r0, rows, nkb;
+};
+
+__device__ __forceinline__ WTile w_decode(const WTail &st, int t, int mt, int nt) {
+  WTile w;
+  const int per = mt * nt;
+  w.e = t / per;
+  const int rem = t - w.e * per;
+  w.m0 = (rem / nt) * WM;
+  w.n0 = (rem % nt) * WN;
+  w.r0 = st.off[w.e];
+  w.rows = st.off[w.e + 1] - w.r0;
+  w.nkb = (w.rows + WK - 1) / WK;
+  return w;
+}
+
+__global__ void __launch_bounds__(W_THREADS, 1)
+    wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const int32_t *__restrict__ offsets, int E, int nK, int M, int N,
+                    float *__restrict__ out, int32_t *status) {
+  pdl_enter();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *smemA = smem;
+  uint8_t *smemB = smem + WSTAGES * WA_STAGE;
+  WTail &st = *reinterpret_cast<WTail *>(smem + WSTAGES * WSTAGE);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = M / WM, nt = N / WN;
+
+  if (tid == 0) {
+    for (int s = 0; s < WSTAGES; ++s) {
+      ptx::mbar_init(&st.full[s], 1);
+      ptx::mbar_init(&st.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&st.tfull[a], 1);
+      ptx::mbar_init(&st.tempty[a], 4);
+    }
+    ptx::mbar_init(&st.drain, 1);
+    st.abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  for (int c = tid; c <= E; c += W_THREADS) st.off[c] = offsets[c];
+  __syncthreads();
+  if (tid == 0) {
+    bool ok = st.off[0] == 0 && st.off[E] <= nK;
+    for (int e = 0; e < E; ++e) ok = ok && st.off[e + 1] >= st.off[e];
+    st.ok = ok;
+    if (!ok && blockIdx.x == 0) flag_status(status, MOE_DEV_BAD_LAYOUT);
+  }
+  __syncthreads();
+  if (!st.ok) return;
+  const int total = E * mt * nt;
+  if ((int)blockIdx.x >= total) return;
+
+  if (warp == 1) {
+    ptx::tmem_alloc(&st.tmem_base, W_TMEM);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = st.tmem_base;
+  volatile int *abort_flag = &st.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmB);
+      int stage = 0;
+      uint32_t phase = 0, used = 0, last_par = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const WTile w = w_decode(st, t, mt, nt);
+        bool stop = false;
+        for (int kb = 0; kb < w.nkb; ++kb) {
+          if (!w_wait(&st.empty[stage], phase ^ 1u, abort_flag, status)) {
+            stop = true;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&st.full[stage], WSTAGE);
+          const int row = w.r0 + kb * WK;
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            ptx::tma_load_2d(smemA + stage * WA_STAGE + q * WA_BOX, &tmA, &st.full[stage],
+                             w.m0 + q * 64, row);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            ptx::tma_load_2d(smemB + stage * WB_STAGE + q * WB_BOX, &tmB, &st.full[stage],
+                             w.n0 + q * 64, row);
+          used |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == WSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (stop) break;
+      }
+      for (int s = 0; s < WSTAGES; ++s)
+        if (used >> s & 1u) ptx::mbar_wait(&st.full[s], last_par >> s & 1u);
+    }
+  } else if (warp == 1) {
+    // the whole warp: lane 0 issues the MMAs, all lanes zero the rows past
+    // the segment in an expert's last k-block
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const WTile w = w_decode(st, t, mt, nt);
+      int ok = 1;
+      if (lane == 0) ok = w_wait(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      ptx::tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)(acc * WN);
+      bool stop = false;
+      for (int kb = 0; kb < w.nkb; ++kb) {
+        ok = 1;
+        if (lane == 0) ok = w_wait(&st.full[stage], phase, abort_flag, status);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          stop = true;
+          break;
+        }
+        const int valid = min(WK, w.rows - kb * WK);
+        if (valid < WK) {  // zero k-rows [valid, 64) of the four B boxes
+          uint8_t *bst = smemB + stage * WB_STAGE;
+          const int lines = WK - valid;
+          for (int i = lane; i < 4 * lines * 8; i += 32) {
+            const int box = i / (lines * 8), rem = i - box * lines * 8;
+            const int line = valid + rem / 8, chunk = rem % 8;
+            *reinterpret_cast<uint4 *>(bst + box * WB_BOX + line * 128 + chunk * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          ptx::fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_u32(smemA + stage * WA_STAGE);
+          const uint32_t b0 = ptx::smem_u32(smemB + stage * WB_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < WK / 16; ++kk) {
+            // both MN-major SW128: 64-wide atoms one box apart, k step = 16 rows
+            const uint64_t adesc = ptx::smem_desc(a0 + kk * 2048, WA_BOX, 1024);
+            const uint64_t bdesc = ptx::smem_desc(b0 + kk * 2048, WB_BOX, 1024);
+            ptx::mma_bf16(d, adesc, bdesc, W_IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&st.empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == WSTAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (stop) break;
+      if (lane == 0) ptx::mma_commit(&st.tfull[acc]);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) {
+      ptx::mma_commit(&st.drain);
+      ptx::mbar_wait(&st.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // epilogue warps 2..5 -> TMEM lane quarter (warp % 4) = 32 rows of M
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const WTile w = w_decode(st, t, mt, nt);
+      if (!w_wait(&st.tfull[acc], acc_phase, abort_flag, status)) break;
+      ptx::tc_fence_after();
+      const uint32_t tb = tmem + (uint32_t)(acc * WN) + ((uint32_t)(q * 32) << 16);
+      float4 *row = reinterpret_cast<float4 *>(out + ((size_t)w.e * M + w.m0 + q * 32 + lane) * N +
+                                               w.n0);
+#pragma unroll 1
+      for (int c = 0; c < WN / 32; ++c) {
+        uint32_t a[32];
+        if (w.nkb > 0) {  // uniform across the warp
+          ptx::tmem_ld_32x32b_x32(tb + c * 32, a);
+          ptx::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          row[c * 8 + i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
+                                       __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&st.tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    __syncwarp();
+    ptx::tmem_dealloc(tmem, W_TMEM);
+  }
+}
+
+typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                             const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                             const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                             CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn w_encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// rows x cols row-major bf16, boxes of 64 columns x 64 rows, 128-byte swizzle
+bool w_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows) {
+  EncodeFn enc = w_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, WK};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// out[e] (M x N, float32) = a[seg_e]^T b[seg_e]; a (nK x M), b (nK x N) bf16;
+// M % 128 == 0, N % 256 == 0
+cudaError_t launch_wgrad_tc(const Desc &d, const void *a, int M, const void *b, int N,
+                            const int32_t *offsets, float *out, int32_t *status, cudaStream_t s) {
+  if (M % WM || N % WN) return cudaErrorInvalidValue;
+  const long long nK = d.nK();
+  CUtensorMap mA, mB;
+  // a zero-row map is not encodable: point an empty layout at one row (no
+  // expert has rows, so nothing is loaded; every tile writes zeros)
+  const uint64_t rows = nK > 0 ? (uint64_t)nK : 1;
+  if (!w_map(&mA, a, M, rows) || !w_map(&mB, b, N, rows)) return cudaErrorInvalidValue;
+  static int done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !done[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(wgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W_SMEM);
+    if (e != cudaSuccess) return e;
+    done[dev] = 1;
+  }
+  const int total = d.E * (M / WM) * (N / WN);
+  const int sms = device_sm_count();
+  const int grid = total < sms ? total : sms;
+  return launch_pdl(wgrad_tc_kernel, dim3(grid), dim3(W_THREADS), W_SMEM, s, mA, mB, offsets, d.E,
+                    (int)nK, M, N, out, status);
+}
+
+}  // namespace moe

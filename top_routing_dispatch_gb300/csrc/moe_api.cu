@@ -503,6 +503,83 @@ moe_status_t moe_forward_host(const moe_layer_desc_t *desc, const void *x_host,
   return cuda_status(e);
 }
 
+// backward workspace: dY (nK,H) bf16 | dw (nK) f32 | dh (nK,I) bf16 | dGU (nK,2I) bf16 |
+// dx_perm (nK,H) bf16 | dlogits (n,E) f32 | dx_router (n,H) f32
+namespace {
+struct BwdSlots {
+  size_t off[7];
+  size_t total;
+};
+BwdSlots bwd_slots(const Desc &d) {
+  const size_t nK = (size_t)d.nK();
+  const size_t sz[7] = {nK * d.H * 2, nK * 4, nK * d.I * 2, nK * 2 * d.I * 2, nK * d.H * 2,
+                        (size_t)d.n * d.E * 4, (size_t)d.n * d.H * 4};
+  BwdSlots b;
+  size_t o = 0;
+  for (int i = 0; i < 7; ++i) {
+    b.off[i] = o;
+    o += up(sz[i]);
+  }
+  b.total = o;
+  return b;
+}
+}  // namespace
+
+size_t moe_backward_workspace_size(const moe_layer_desc_t *desc) {
+  Desc d;
+  if (check_desc(desc, &d) != MOE_OK) return 0;
+  return bwd_slots(d).total;
+}
+
+moe_status_t moe_backward(const moe_layer_desc_t *desc, const void *x, const void *w_gate,
+                          const void *w13, const void *w2, const void *dy, const float *logits,
+                          const int32_t *topk_idx, const float *topk_w, const int32_t *offsets,
+                          const int32_t *inv_perm, const void *x_perm,
+                          const void *h, const void *y_perm, void *dx, float *dw_gate,
+                          float *dbias, float *dw13, float *dw2, void *ws, size_t ws_bytes,
+                          int32_t *status_word, moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  if (!d.bf16 || d.H % 256 || d.I % 128) return MOE_ERR_UNSUPPORTED;
+  if (!x || !w_gate || !w13 || !w2 || !dy || !logits || !topk_idx || !topk_w || !offsets ||
+      !inv_perm || !x_perm || !h || !y_perm || !dx || !dw_gate || !dw13 || !dw2 || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  const void *aligned[] = {x, w_gate, w13, w2, dy, x_perm, h, y_perm, dx, dw13, dw2};
+  for (const void *p : aligned)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  const BwdSlots b = bwd_slots(d);
+  if (ws_bytes < b.total) return MOE_ERR_WORKSPACE;
+  uint8_t *w = reinterpret_cast<uint8_t *>(ws);
+  void *dY = w + b.off[0];
+  float *dwt = reinterpret_cast<float *>(w + b.off[1]);
+  void *dh = w + b.off[2];
+  void *dgu = w + b.off[3];
+  void *dxp = w + b.off[4];
+  float *dl = reinterpret_cast<float *>(w + b.off[5]);
+  float *dxr = reinterpret_cast<float *>(w + b.off[6]);
+  cudaStream_t s = stream;
+  cudaError_t e = cudaSuccess;
+  // combine backward (a dispatch): dY = w dy in expert order, dw = <dy, Y>
+  e = launch_combine_bwd(d, dy, y_perm, topk_w, inv_perm, dY, dwt, status_word, s);
+  // expert backward: dh = dY W2^T; dG|dU from the recomputed G|U; dX = dGU W13^T
+  if (e == cudaSuccess) e = launch_gemm_dgrad_tc(d, dY, w2, d.H, d.I, offsets, dh, status_word, s);
+  if (e == cudaSuccess)
+    e = launch_gemm1_swiglu_bwd_tc(d, x_perm, w13, offsets, dh, dgu, status_word, s);
+  if (e == cudaSuccess)
+    e = launch_gemm_dgrad_tc(d, dgu, w13, 2 * d.I, d.H, offsets, dxp, status_word, s);
+  // weight gradients over each expert's rows
+  if (e == cudaSuccess) e = launch_wgrad_tc(d, h, d.I, dY, d.H, offsets, dw2, status_word, s);
+  if (e == cudaSuccess)
+    e = launch_wgrad_tc(d, x_perm, d.H, dgu, 2 * d.I, offsets, dw13, status_word, s);
+  // router backward, then dx = sum of the slots' dX rows (a combine) + router term
+  if (e == cudaSuccess)
+    e = launch_router_bwd(d, x, w_gate, logits, topk_idx, topk_w, dwt, dl, dxr, dw_gate, dbias, s);
+  if (e == cudaSuccess) e = launch_dx_gather(d, dxp, dxr, inv_perm, dx, s);
+  return cuda_status(e);
+}
+
 moe_status_t moe_check_status(const int32_t *status_word, moe_stream_t stream) {
   if (!status_word) return MOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
