@@ -55,6 +55,7 @@ def parse_args():
                     help="CPU-baseline: repeat the oracle on the sample until this much wall time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-domino", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -494,6 +495,9 @@ def run_ours(args, cfg):
     }
     if not args.no_domino:
         out["domino"] = domino(args, torch, M, synth, DOMINO, dev, peaks)
+    if not args.no_backward and cfg.dtype == "bf16":
+        out["backward"] = backward(args, torch, M, synth, cfg, dev, peaks, layer, L, x, v, st,
+                                   stream, T)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg, L, x, args.cpu_sample, args.cpu_seconds)
     if rank == 0:
@@ -501,6 +505,40 @@ def run_ours(args, cfg):
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+def backward(args, torch, M, synth, cfg, dev, peaks, layer, L, x, v, st, stream, T):
+    """moe_backward on the same layer: one C-ABI call per step (combine
+    backward, two dgrad GEMMs, the SwiGLU-backward GEMM, two weight-gradient
+    GEMMs, router backward, dx gather), L2 flushed before each step."""
+    n, H, I, E, K = cfg.n, cfg.H, cfg.I, cfg.E, cfg.K
+    nK = n * K
+    f32, bf = torch.float32, torch.bfloat16
+    g = torch.Generator(device=dev)
+    g.manual_seed(synth.sub_seed(cfg.seed, "dy"))
+    dy = torch.randn((n, H), generator=g, device=dev).to(bf)
+    yp = torch.empty((nK, H), dtype=bf, device=dev)  # unweighted Y rows
+    M.moe_expert_gemm2(layer.desc, v["h"], L["w2"], v["offsets"], yp, 0, st, stream)
+    dx = torch.empty_like(x)
+    dwg = torch.empty((H, E), dtype=f32, device=dev)
+    dbias = torch.empty(E, dtype=f32, device=dev)
+    dw13 = torch.empty((E, H, 2 * I), dtype=f32, device=dev)
+    dw2 = torch.empty((E, I, H), dtype=f32, device=dev)
+    ws = torch.empty(M.moe_backward_workspace_size(layer.desc), dtype=torch.uint8, device=dev)
+
+    def step():
+        M.moe_backward(layer.desc, x, L["w_gate"], L["w13"], L["w2"], dy, v["logits"],
+                       v["topk_idx"], v["topk_w"], v["offsets"], v["inv_perm"], v["x_perm"],
+                       v["h"], yp, dx, dwg, dbias, dw13, dw2, ws, st, stream)
+    T.measure(step, 3)
+    ms = statistics.mean(T.measure(step, max(5, args.steps // 2)))
+    flop = 16 * nK * H * I
+    return {"ms_per_step": ms, "tokens_per_s": n / (ms * 1e-3),
+            "tensor_flop_per_step": flop, "tflops": flop / (ms * 1e-3) / 1e12,
+            "frac_bf16": flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "note": "dgrad dh, SwiGLU-backward recompute, dgrad dX, wgrad dW2 and dW13 on "
+                    "the tensor cores; router backward and the dx gather on the FMA units; "
+                    "L2 flushed before each step"}
 
 
 def domino(args, torch, M, synth, cfg, dev, peaks):

@@ -99,3 +99,52 @@ def test_backward_is_deterministic():
     a, b = _run(cfg), _run(cfg)
     for k in ("dx", "dwg", "dbias", "dw13", "dw2"):
         assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), k
+
+
+def test_backward_full_size_sampled():
+    """The OLMoE-shaped layer (n=4096, H=2048, I=1024, E=64, K=8): dW_gate and
+    the routing-weight gradients for every token; dx for sampled tokens
+    (the expert backward is row-local); dW13 and dW2 for three experts (the
+    hottest, the coldest, one at random) over all of their rows."""
+    from workloads import OLMOE
+    cfg = OLMOE
+    r = _run(cfg)
+    assert r["status"] == 0
+    L = r["L"]
+    K = cfg.K
+    x64, wg64, dy64 = f64(r["x"]), f64(L["w_gate"]), f64(r["dy"])
+    lo = O.router_logits(x64, wg64, None)
+    near = O.near_tie_tokens(lo, K, NEAR_TIE_GAP)
+    gidx = r["idx"].cpu().numpy()
+    forced = (np.where(near)[0], gidx[near])
+    w13 = lambda e: L["w13"][e].to(torch.float64).cpu().numpy()
+    w2 = lambda e: L["w2"][e].to(torch.float64).cpu().numpy()
+    fw = O.moe_forward(x64, wg64, None, w13, w2, K, cfg.norm_topk_prob, forced=forced)
+    dY, dw = OB.combine_backward(dy64, fw["y_perm"], fw["w_top"], fw["inv_perm"])
+    dl, dx_router, dwg = OB.router_backward(x64, wg64, fw["logits"], fw["e_top"], fw["w_top"],
+                                            dw, cfg.norm_topk_prob)
+    assert rel_fro(f64(r["dwg"]), dwg) <= TOL
+    # dx for sampled tokens, from their K rows
+    rng = np.random.default_rng(0)
+    toks = np.unique(np.concatenate([rng.choice(cfg.n, 48, replace=False), [0, cfg.n - 1]]))
+    inv = fw["inv_perm"].reshape(cfg.n, K)
+    off = fw["offsets"]
+    x_perm = O.permute(x64, fw["perm"], K)
+    dx_ref = dx_router[toks].copy()
+    for i, t in enumerate(toks):
+        for k in range(K):
+            row = inv[t, k]
+            e = int(np.searchsorted(off, row, side="right") - 1)
+            b = OB.expert_backward(x_perm[row:row + 1], w13(e), w2(e), dY[row:row + 1])
+            dx_ref[i] += b["dX"][0]
+    assert rel_fro(f64(r["dx"][torch.as_tensor(toks, device=r["dx"].device)]), dx_ref) <= TOL
+    # weight gradients of three experts
+    counts = np.diff(off)
+    nz = np.where(counts > 0)[0]
+    experts = {int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])]),
+               int(rng.choice(nz))}
+    for e in sorted(experts):
+        lo_, hi_ = int(off[e]), int(off[e + 1])
+        b = OB.expert_backward(x_perm[lo_:hi_], w13(e), w2(e), dY[lo_:hi_])
+        assert rel_fro(f64(r["dw13"][e]), b["dW13"]) <= TOL, e
+        assert rel_fro(f64(r["dw2"][e]), b["dW2"]) <= TOL, e

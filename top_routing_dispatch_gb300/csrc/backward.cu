@@ -19,6 +19,7 @@ namespace moe {
 namespace {
 
 constexpr int BT = 256;  // threads per block
+constexpr int RB_SPLIT = kRouterBwdSplit;
 
 __device__ __forceinline__ void bf16x8_to_f32(uint4 v, float (&f)[8]) {
   const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&v);
@@ -155,32 +156,41 @@ __global__ void __launch_bounds__(BT) router_bwd_kernel(const float *__restrict_
   }
 }
 
-// C[m][n] = sum_k A(m,k) B(k,n) (+ C0[m][n] when given), float32 accumulate
-// in ascending k, 32x32 output tiles, 256 threads (2x2 outputs each).
-// A(m,k) = a[m*sam + k*sak], B(k,n) = b[k*sbk + n*sbn].
-template <typename TA, typename TB>
+// C[m][n] = sum over k in [k0, k1) of A(m,k) B(k,n), float32 accumulate in
+// ascending k, 32x32 output tiles, 256 threads (2x2 outputs each).
+// A(m,k) = a[m*sam + k*sak], B(k,n) = b[k*sbk + n*sbn].  AK / BK: the
+// operand's k stride is 1 (its tile is loaded with consecutive threads along
+// k, else along m / n), so either layout is read in whole sectors.
+// blockIdx.z selects the k range [z*kc, min(Kd, (z+1)*kc)) and the output
+// c + z*M*N (split-K partials, added later in order).
+template <typename TA, typename TB, bool AK, bool BK>
 __global__ void __launch_bounds__(BT) small_gemm_kernel(const TA *__restrict__ a, long long sam,
                                                         long long sak, const TB *__restrict__ b,
                                                         long long sbk, long long sbn,
                                                         float *__restrict__ c, int M, int N,
-                                                        int Kd) {
+                                                        int Kd, int kc) {
   pdl_enter();
-  __shared__ float As[16][32 + 1];
-  __shared__ float Bs[16][32 + 1];
+  __shared__ float As[32][32 + 1];
+  __shared__ float Bs[32][32 + 1];
   const int m0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
+  const int kb = blockIdx.z * kc, ke = min(Kd, kb + kc);
+  c += (size_t)blockIdx.z * M * N;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   float acc[2][2] = {};
-  for (int k0 = 0; k0 < Kd; k0 += 16) {
-    for (int i = threadIdx.x; i < 16 * 32; i += BT) {
-      const int kk = i / 32, mm = i % 32;
+  for (int k0 = kb; k0 < ke; k0 += 32) {
+    for (int i = threadIdx.x; i < 32 * 32; i += BT) {
+      const int kk = AK ? i % 32 : i / 32, mm = AK ? i / 32 : i % 32;
       const int gm = m0 + mm, gk = k0 + kk;
-      As[kk][mm] = (gm < M && gk < Kd) ? (float)a[(long long)gm * sam + (long long)gk * sak] : 0.f;
-      const int gn = n0 + mm;
-      Bs[kk][mm] = (gn < N && gk < Kd) ? (float)b[(long long)gk * sbk + (long long)gn * sbn] : 0.f;
+      As[kk][mm] = (gm < M && gk < ke) ? (float)a[(long long)gm * sam + (long long)gk * sak] : 0.f;
+    }
+    for (int i = threadIdx.x; i < 32 * 32; i += BT) {
+      const int kk = BK ? i % 32 : i / 32, nn = BK ? i / 32 : i % 32;
+      const int gn = n0 + nn, gk = k0 + kk;
+      Bs[kk][nn] = (gn < N && gk < ke) ? (float)b[(long long)gk * sbk + (long long)gn * sbn] : 0.f;
     }
     __syncthreads();
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
+    for (int kk = 0; kk < 32; ++kk) {
 #pragma unroll
       for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -198,15 +208,43 @@ __global__ void __launch_bounds__(BT) small_gemm_kernel(const TA *__restrict__ a
     }
 }
 
-// dbias[e] = sum over t of dlogits[t][e], ascending t (one thread per e)
-__global__ void __launch_bounds__(BT) column_sum_kernel(const float *__restrict__ dl,
-                                                        float *__restrict__ out, int n, int E) {
+// out[i] = sum over z = 0..S-1 of part[z][i] (ascending z)
+__global__ void __launch_bounds__(BT) sum_parts_kernel(const float *__restrict__ part,
+                                                       float *__restrict__ out, long long count,
+                                                       int S) {
   pdl_enter();
-  const int e = blockIdx.x * BT + threadIdx.x;
-  if (e >= E) return;
+  for (long long i = (long long)blockIdx.x * BT + threadIdx.x; i < count;
+       i += (long long)gridDim.x * BT) {
+    float s = 0.f;
+    for (int z = 0; z < S; ++z) s += part[(size_t)z * count + i];
+    out[i] = s;
+  }
+}
+
+// partial column sums of dlogits: block (x, z) adds tokens [z*tc, (z+1)*tc)
+// of experts [32x, 32x + 32) in 8 token groups (coalesced over experts), the
+// group sums in order, into part[z][e]
+__global__ void __launch_bounds__(BT) column_sum_kernel(const float *__restrict__ dl,
+                                                        float *__restrict__ part, int n, int E,
+                                                        int tc) {
+  pdl_enter();
+  __shared__ float grp[8][32];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + tx;
+  const int t0 = blockIdx.z * tc, t1 = min(n, t0 + tc);
   float s = 0.f;
-  for (int t = 0; t < n; ++t) s += dl[(long long)t * E + e];
-  out[e] = s;
+  if (e < E) {
+#pragma unroll 4
+    for (int t = t0 + ty; t < t1; t += 8) s += dl[(long long)t * E + e];
+  }
+  grp[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && e < E) {
+    float r = 0.f;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) r += grp[g][tx];
+    part[(size_t)blockIdx.z * E + e] = r;
+  }
 }
 
 // dx[t] = sum_k dx_perm[inv(t,k)] (slot order) + dx_router[t], float32, one rounding
@@ -289,27 +327,38 @@ cudaError_t launch_combine_bwd(const Desc &d, const void *dy, const void *y_perm
 cudaError_t launch_router_bwd(const Desc &d, const void *x, const void *w_gate,
                               const float *logits, const int32_t *topk_idx, const float *topk_w,
                               const float *dw, float *dlogits, float *dx_router,
-                              float *dw_gate, float *dbias, cudaStream_t s) {
+                              float *dw_part, float *dw_gate, float *dbias, cudaStream_t s) {
   if (d.n == 0) return cudaSuccess;
   cudaError_t e = launch_pdl(router_bwd_kernel, dim3(grid_warps(d.n)), dim3(BT), 0, s, logits,
                              topk_idx, topk_w, dw, dlogits, d.n, d.E, d.K, d.norm ? 1 : 0);
   if (e != cudaSuccess) return e;
   const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
   const __nv_bfloat16 *wg = reinterpret_cast<const __nv_bfloat16 *>(w_gate);
-  // dx_router[t][h] = sum_e dlogits[t][e] W_gate[h][e]
-  e = launch_pdl(small_gemm_kernel<float, __nv_bfloat16>,
-                 dim3((d.n + 31) / 32, (d.H + 31) / 32), dim3(BT), 0, s,
+  // dx_router[t][h] = sum_e dlogits[t][e] W_gate[h][e]   (both k-contiguous)
+  e = launch_pdl(small_gemm_kernel<float, __nv_bfloat16, true, true>,
+                 dim3((d.n + 31) / 32, (d.H + 31) / 32, 1), dim3(BT), 0, s,
                  (const float *)dlogits, (long long)d.E, 1ll, wg, 1ll, (long long)d.E, dx_router,
-                 d.n, d.H, d.E);
+                 d.n, d.H, d.E, d.E);
   if (e != cudaSuccess) return e;
-  // dW_gate[h][e] = sum_t x[t][h] dlogits[t][e]
-  e = launch_pdl(small_gemm_kernel<__nv_bfloat16, float>,
-                 dim3((d.H + 31) / 32, (d.E + 31) / 32), dim3(BT), 0, s, xb, 1ll,
-                 (long long)d.H, (const float *)dlogits, (long long)d.E, 1ll, dw_gate, d.H, d.E,
-                 d.n);
+  // dW_gate[h][e] = sum_t x[t][h] dlogits[t][e]: the tokens split into
+  // RB_SPLIT ranges (partials in dw_part), then added in order
+  const int kc = (d.n + RB_SPLIT - 1) / RB_SPLIT;
+  e = launch_pdl(small_gemm_kernel<__nv_bfloat16, float, false, false>,
+                 dim3((d.H + 31) / 32, (d.E + 31) / 32, RB_SPLIT), dim3(BT), 0, s, xb, 1ll,
+                 (long long)d.H, (const float *)dlogits, (long long)d.E, 1ll, dw_part, d.H, d.E,
+                 d.n, kc);
+  if (e != cudaSuccess) return e;
+  const long long cnt = (long long)d.H * d.E;
+  e = launch_pdl(sum_parts_kernel, dim3((int)((cnt + BT - 1) / BT)), dim3(BT), 0, s,
+                 (const float *)dw_part, dw_gate, cnt, RB_SPLIT);
   if (e != cudaSuccess || !dbias) return e;
-  return launch_pdl(column_sum_kernel, dim3((d.E + BT - 1) / BT), dim3(BT), 0, s,
-                    (const float *)dlogits, dbias, d.n, d.E);
+  // dbias: the same token ranges, partials after the dW_gate partials
+  float *bpart = dw_part + (size_t)RB_SPLIT * d.H * d.E;
+  e = launch_pdl(column_sum_kernel, dim3((d.E + 31) / 32, 1, RB_SPLIT), dim3(BT), 0, s,
+                 (const float *)dlogits, bpart, d.n, d.E, kc);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(sum_parts_kernel, dim3((d.E + BT - 1) / BT), dim3(BT), 0, s,
+                    (const float *)bpart, dbias, (long long)d.E, RB_SPLIT);
 }
 
 cudaError_t launch_dx_gather(const Desc &d, const void *dx_perm, const float *dx_router,

@@ -76,13 +76,14 @@ cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w
 // y[t] = sum over k of y_slot[t*K + k] (float32, slot order, one rounding)
 cudaError_t launch_combine_slots(const Desc &d, const void *y_slot, void *y, cudaStream_t s);
 // backward (backward.cu, gemm_tc.cu modes 5 and 6, gemm_wgrad.cu)
+constexpr int kRouterBwdSplit = 16;  // token ranges of the dW_gate reduction
 cudaError_t launch_combine_bwd(const Desc &d, const void *dy, const void *y_perm,
                                const float *topk_w, const int32_t *inv_perm, void *dY, float *dw,
                                int32_t *status, cudaStream_t s);
 cudaError_t launch_router_bwd(const Desc &d, const void *x, const void *w_gate,
                               const float *logits, const int32_t *topk_idx, const float *topk_w,
                               const float *dw, float *dlogits, float *dx_router,
-                              float *dw_gate, float *dbias, cudaStream_t s);
+                              float *dw_part, float *dw_gate, float *dbias, cudaStream_t s);
 cudaError_t launch_dx_gather(const Desc &d, const void *dx_perm, const float *dx_router,
                              const int32_t *inv_perm, void *dx, cudaStream_t s);
 cudaError_t launch_gemm_dgrad_tc(const Desc &d, const void *a, const void *w, int Kdim, int Nout,

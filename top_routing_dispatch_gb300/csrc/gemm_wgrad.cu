@@ -44,6 +44,7 @@ struct WTail {
   int abort_flag;
   int ok;
   int off[kMaxE + 1];
+  alignas(16) uint8_t epi[4][32 * 144];  // per epilogue warp: 32 rows x 128 B (+16 pad)
 };
 
 constexpr size_t W_SMEM = 1024 + (size_t)WSTAGES * WSTAGE + sizeof(WTail);
@@ -242,8 +243,10 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       if (!w_wait(&st.tfull[acc], acc_phase, abort_flag, status)) break;
       ptx::tc_fence_after();
       const uint32_t tb = tmem + (uint32_t)(acc * WN) + ((uint32_t)(q * 32) << 16);
-      float4 *row = reinterpret_cast<float4 *>(out + ((size_t)w.e * M + w.m0 + q * 32 + lane) * N +
-                                               w.n0);
+      // rows of this warp's 32-row slice; each 32-column chunk is staged in
+      // shared memory and stored as whole 128-byte row segments (8 lanes a row)
+      float *base = out + ((size_t)w.e * M + w.m0 + q * 32) * N + w.n0;
+      uint8_t *eb = st.epi[warp - 2];
 #pragma unroll 1
       for (int c = 0; c < WN / 32; ++c) {
         uint32_t a[32];
@@ -254,10 +257,18 @@ __global__ void __launch_bounds__(W_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = 0u;
         }
+        uint4 *mine = reinterpret_cast<uint4 *>(eb + lane * 144);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          row[c * 8 + i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
-                                       __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+        for (int v = 0; v < 8; ++v) mine[v] = make_uint4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int p = lane + 32 * i;
+          const int r = p >> 3, c16 = p & 7;
+          const uint4 val = *reinterpret_cast<const uint4 *>(eb + r * 144 + c16 * 16);
+          *reinterpret_cast<uint4 *>(base + (size_t)r * N + c * 32 + c16 * 4) = val;
+        }
+        __syncwarp();
       }
       ptx::tc_fence_before();
       __syncwarp();

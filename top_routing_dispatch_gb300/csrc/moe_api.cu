@@ -504,19 +504,21 @@ moe_status_t moe_forward_host(const moe_layer_desc_t *desc, const void *x_host,
 }
 
 // backward workspace: dY (nK,H) bf16 | dw (nK) f32 | dh (nK,I) bf16 | dGU (nK,2I) bf16 |
-// dx_perm (nK,H) bf16 | dlogits (n,E) f32 | dx_router (n,H) f32
+// dx_perm (nK,H) bf16 | dlogits (n,E) f32 | dx_router (n,H) f32 |
+// dW_gate partials (16,H,E) and dbias partials (16,E) f32
 namespace {
 struct BwdSlots {
-  size_t off[7];
+  size_t off[8];
   size_t total;
 };
 BwdSlots bwd_slots(const Desc &d) {
   const size_t nK = (size_t)d.nK();
-  const size_t sz[7] = {nK * d.H * 2, nK * 4, nK * d.I * 2, nK * 2 * d.I * 2, nK * d.H * 2,
-                        (size_t)d.n * d.E * 4, (size_t)d.n * d.H * 4};
+  const size_t sz[8] = {nK * d.H * 2, nK * 4, nK * d.I * 2, nK * 2 * d.I * 2, nK * d.H * 2,
+                        (size_t)d.n * d.E * 4, (size_t)d.n * d.H * 4,
+                        (size_t)kRouterBwdSplit * (d.H + 1) * d.E * 4};
   BwdSlots b;
   size_t o = 0;
-  for (int i = 0; i < 7; ++i) {
+  for (int i = 0; i < 8; ++i) {
     b.off[i] = o;
     o += up(sz[i]);
   }
@@ -559,6 +561,7 @@ moe_status_t moe_backward(const moe_layer_desc_t *desc, const void *x, const voi
   void *dxp = w + b.off[4];
   float *dl = reinterpret_cast<float *>(w + b.off[5]);
   float *dxr = reinterpret_cast<float *>(w + b.off[6]);
+  float *dwp = reinterpret_cast<float *>(w + b.off[7]);
   cudaStream_t s = stream;
   cudaError_t e = cudaSuccess;
   // combine backward (a dispatch): dY = w dy in expert order, dw = <dy, Y>
@@ -575,7 +578,8 @@ moe_status_t moe_backward(const moe_layer_desc_t *desc, const void *x, const voi
     e = launch_wgrad_tc(d, x_perm, d.H, dgu, 2 * d.I, offsets, dw13, status_word, s);
   // router backward, then dx = sum of the slots' dX rows (a combine) + router term
   if (e == cudaSuccess)
-    e = launch_router_bwd(d, x, w_gate, logits, topk_idx, topk_w, dwt, dl, dxr, dw_gate, dbias, s);
+    e = launch_router_bwd(d, x, w_gate, logits, topk_idx, topk_w, dwt, dl, dxr, dwp, dw_gate,
+                          dbias, s);
   if (e == cudaSuccess) e = launch_dx_gather(d, dxp, dxr, inv_perm, dx, s);
   return cuda_status(e);
 }
