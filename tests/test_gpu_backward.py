@@ -26,7 +26,10 @@ CASES = [
 TOL = 2e-2
 
 
-def _run(cfg):
+def _run(cfg, force=None):
+    """Forward intermediates from the library's entry points, then
+    moe_backward.  `force` (n, K) replaces the router's expert choice (the
+    weights are then the softmax of the router's logits at those experts)."""
     import top_routing_dispatch_gb300 as M
     dev = torch.device("cuda:0")
     L = synth.make_layer(cfg, dev)
@@ -50,6 +53,12 @@ def _run(cfg):
     h = torch.empty((nK, I), dtype=bf, device=dev)
     yp = torch.empty((nK, H), dtype=bf, device=dev)
     M.moe_route_topk(desc, x, L["w_gate"], L["bias"], idx, w, logits)
+    if force is not None:
+        idx.copy_(torch.as_tensor(force, dtype=i32, device=dev))
+        p = torch.softmax(logits.double(), dim=1).gather(1, idx.long())
+        if cfg.norm_topk_prob:
+            p = p / p.sum(dim=1, keepdim=True)
+        w.copy_(p.float())
     M.moe_dispatch_layout(desc, idx, counts, offsets, perm, inv, st, lws)
     M.moe_permute(desc, x, perm, xp, st)
     M.moe_expert_gemm1_swiglu(desc, xp, L["w13"], offsets, h, status_word=st)
@@ -64,7 +73,7 @@ def _run(cfg):
                    h, yp, dx, dwg, dbias, dw13, dw2, ws, st)
     torch.cuda.synchronize()
     return dict(L=L, x=x, dy=dy, idx=idx, status=int(st.item()), dx=dx, dwg=dwg, dbias=dbias,
-                dw13=dw13, dw2=dw2)
+                dw13=dw13, dw2=dw2, counts=counts.cpu().numpy())
 
 
 @pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
@@ -148,3 +157,30 @@ def test_backward_full_size_sampled():
         b = OB.expert_backward(x_perm[lo_:hi_], w13(e), w2(e), dY[lo_:hi_])
         assert rel_fro(f64(r["dw13"][e]), b["dW13"]) <= TOL, e
         assert rel_fro(f64(r["dw2"][e]), b["dW2"]) <= TOL, e
+
+
+def test_backward_segment_lengths_at_block_edges():
+    """Expert segments of 0, 1, 16, 17, 48, 64, 65 and 129 rows (forced
+    routing, K = 1): whole and partial 16-row k steps, whole and partial
+    64-row blocks, an empty expert.  The weight gradients are sums over each
+    segment's rows only; rows of the neighbouring expert must not leak in."""
+    counts = np.array([0, 16, 48, 64, 65, 17, 1, 129])
+    cfg = MoEConfig("bwd_edges", n=int(counts.sum()), H=256, I=128, E=8, K=1, dtype="bf16",
+                    norm_topk_prob=False, seed=44)
+    rng = np.random.default_rng(44)
+    ids = rng.permutation(np.repeat(np.arange(cfg.E), counts))[:, None]
+    r = _run(cfg, force=ids)
+    assert r["status"] == 0
+    assert np.array_equal(r["counts"], counts)
+    L = r["L"]
+    x64, wg64, b64 = f64(r["x"]), f64(L["w_gate"]), f64(L["bias"])
+    w13 = lambda e: L["w13"][e].to(torch.float64).cpu().numpy()
+    w2 = lambda e: L["w2"][e].to(torch.float64).cpu().numpy()
+    o = OB.moe_backward(x64, wg64, b64, w13, w2, 1, False, f64(r["dy"]),
+                        forced=(np.arange(cfg.n), ids))
+    assert np.all(f64(r["dw13"][0]) == 0) and np.all(f64(r["dw2"][0]) == 0)
+    for e in range(1, cfg.E):
+        assert rel_fro(f64(r["dw13"][e]), o["dw13"][e]) <= TOL, e
+        assert rel_fro(f64(r["dw2"][e]), o["dw2"][e]) <= TOL, e
+    assert rel_fro(f64(r["dx"]), o["dx"]) <= TOL
+    assert rel_fro(f64(r["dwg"]), o["dw_gate"]) <= TOL

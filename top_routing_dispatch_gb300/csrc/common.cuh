@@ -92,8 +92,10 @@ cudaError_t launch_gemm_dgrad_tc(const Desc &d, const void *a, const void *w, in
 cudaError_t launch_gemm1_swiglu_bwd_tc(const Desc &d, const void *x_perm, const void *w13,
                                        const int32_t *offsets, const void *dh, void *dgu,
                                        int32_t *status, cudaStream_t s);
+size_t wgrad_tail_bytes(const Desc &d, int M, int N);
 cudaError_t launch_wgrad_tc(const Desc &d, const void *a, int M, const void *b, int N,
-                            const int32_t *offsets, float *out, int32_t *status, cudaStream_t s);
+                            const int32_t *offsets, void *tail, float *out, int32_t *status,
+                            cudaStream_t s);
 cudaError_t launch_gemm1_simt(const Desc &d, const void *x_perm, const void *w13,
                               const int32_t *offsets, void *h, int32_t *status, cudaStream_t s);
 cudaError_t launch_gemm2_simt(const Desc &d, const void *h, const void *w2,
