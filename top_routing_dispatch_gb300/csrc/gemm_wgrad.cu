@@ -17,8 +17,9 @@
 // 16-row k steps that hold segment rows are issued.  No generic-proxy write
 // ever reaches a pipeline stage, so no proxy fence sits in the MMA issue path
 // (zeroing the rows in place with a fence there cost about 2 us per tile).  A
-// tile of an expert without rows is written as zeros.  float32 output, one CTA
-// per SM, persistent, double-buffered TMEM accumulators as in gemm_tc.cu.
+// tile of an expert without rows is written as zeros.  float32 output, written
+// by TMA tile stores from swizzled shared-memory staging buffers; one CTA per
+// SM, persistent, double-buffered TMEM accumulators as in gemm_tc.cu.
 #include <cuda.h>
 
 #include <mutex>
@@ -40,6 +41,8 @@ constexpr int W_TMEM = 512;
 constexpr int W_GROUP = 16;                       // rows of one k step
 constexpr int W_GROUP_BYTES = W_GROUP * 128;      // one 16-row slice of a 64-wide box
 
+constexpr int W_EPI_BYTES = 32 * 128;  // 32 rows x 32 float32 columns, 128-byte swizzle
+
 struct WTail {
   uint64_t full[WSTAGES];
   uint64_t empty[WSTAGES];
@@ -50,10 +53,11 @@ struct WTail {
   int abort_flag;
   int ok;
   int off[kMaxE + 1];
-  alignas(16) uint8_t epi[4][32 * 144];  // per epilogue warp: 32 rows x 128 B (+16 pad)
 };
 
-constexpr size_t W_SMEM = 1024 + (size_t)WSTAGES * WSTAGE + sizeof(WTail);
+// stages | per epilogue warp two 1024-aligned staging buffers | WTail
+constexpr size_t W_SMEM = 1024 + (size_t)WSTAGES * WSTAGE + 8 * W_EPI_BYTES + sizeof(WTail);
+static_assert(W_SMEM <= 232448, "wgrad shared memory above the per-block limit");
 constexpr uint32_t W_IDESC = ptx::idesc_bf16_f32(WM, WN, /*a_mn=*/true, /*b_mn=*/true);
 
 __device__ __forceinline__ bool w_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
@@ -75,12 +79,15 @@ struct WTile {
   int e, m0, n0, r0, rows, nkb;
 };
 
-__device__ __forceinline__ WTile w_decode(const WTail &st, int t, int mt, int nt) {
+// Work unit g of a cluster of CL CTAs: expert e, CL consecutive 128-row M
+// tiles (one per CTA: rank), one 256-column N tile.
+template <int CL>
+__device__ __forceinline__ WTile w_decode(const WTail &st, int g, int mt, int nt, int rank) {
   WTile w;
-  const int per = mt * nt;
-  w.e = t / per;
-  const int rem = t - w.e * per;
-  w.m0 = (rem / nt) * WM;
+  const int per = (mt / CL) * nt;
+  w.e = g / per;
+  const int rem = g - w.e * per;
+  w.m0 = ((rem / nt) * CL + rank) * WM;
   w.n0 = (rem % nt) * WN;
   w.r0 = st.off[w.e];
   w.rows = st.off[w.e + 1] - w.r0;
@@ -88,6 +95,23 @@ __device__ __forceinline__ WTile w_decode(const WTail &st, int t, int mt, int nt
   return w;
 }
 
+// One B box: local load (CL == 1) or multicast to every CTA of the cluster.
+template <int CL>
+__device__ __forceinline__ void w_load_b(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
+                                         int c1) {
+  if constexpr (CL == 1)
+    ptx::tma_load_2d(dst, map, bar, c0, c1);
+  else
+    ptx::tma_load_2d_multicast(dst, map, bar, c0, c1, (uint16_t)((1u << CL) - 1));
+}
+
+// CTAs of one cluster compute the tiles of CL consecutive M tiles that share
+// the expert, the N tile and hence every B operand block: each CTA loads its
+// own A boxes and 4/CL of the four B boxes, multicast to all CL CTAs, so the
+// B operand leaves L2 once per cluster.  A stage is refilled only after the
+// MMAs of every CTA of the cluster have read it (each CTA's MMA completion
+// arrives on the stage's empty barrier in all CL CTAs).
+template <int CL>
 __global__ void __launch_bounds__(W_THREADS, 1)
     wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -95,22 +119,28 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmB16,
                     const __grid_constant__ CUtensorMap tmAt,
                     const __grid_constant__ CUtensorMap tmBt,
+                    const __grid_constant__ CUtensorMap tmOut,
                     const int32_t *__restrict__ offsets, int E, int nK, int M, int N,
-                    float *__restrict__ out, int32_t *status) {
+                    int32_t *status) {
+  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster of 1, 2 or 4 CTAs");
+  constexpr int BQ = 4 / CL;  // B boxes this CTA loads per block
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *smemA = smem;
   uint8_t *smemB = smem + WSTAGES * WA_STAGE;
-  WTail &st = *reinterpret_cast<WTail *>(smem + WSTAGES * WSTAGE);
+  uint8_t *smemE = smem + WSTAGES * WSTAGE;
+  WTail &st = *reinterpret_cast<WTail *>(smemE + 8 * W_EPI_BYTES);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = M / WM, nt = N / WN;
+  const int rank = CL > 1 ? (int)ptx::cluster_ctarank() : 0;
+  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
 
   if (tid == 0) {
     for (int s = 0; s < WSTAGES; ++s) {
       ptx::mbar_init(&st.full[s], 1);
-      ptx::mbar_init(&st.empty[s], 1);
+      ptx::mbar_init(&st.empty[s], CL);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&st.tfull[a], 1);
@@ -130,9 +160,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     if (!ok && blockIdx.x == 0) flag_status(status, MOE_DEV_BAD_LAYOUT);
   }
   __syncthreads();
-  if (!st.ok) return;
-  const int total = E * mt * nt;
-  if ((int)blockIdx.x >= total) return;
+  if (!st.ok) return;  // the same decision in every CTA of the cluster
+  // work units; the grid holds at most one cluster per unit
+  const int total = E * (mt / CL) * nt;
 
   if (warp == 1) {
     ptx::tmem_alloc(&st.tmem_base, W_TMEM);
@@ -141,6 +171,8 @@ __global__ void __launch_bounds__(W_THREADS, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // every CTA's barriers are initialised before any peer copies or arrives
+  if constexpr (CL > 1) ptx::cluster_sync();
   const uint32_t tmem = st.tmem_base;
   volatile int *abort_flag = &st.abort_flag;
 
@@ -154,9 +186,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       ptx::prefetch_tmap(&tmBt);
       int stage = 0;
       uint32_t phase = 0, used = 0, last_par = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const WTile w = w_decode(st, t, mt, nt);
-        bool stop = false;
+      bool stop = false;
+      for (int g = cid; g < total && !stop; g += ncl) {
+        const WTile w = w_decode<CL>(st, g, mt, nt, rank);
         for (int kb = 0; kb < w.nkb; ++kb) {
           if (!w_wait(&st.empty[stage], phase ^ 1u, abort_flag, status)) {
             stop = true;
@@ -172,27 +204,27 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             for (int q = 0; q < 2; ++q)
               ptx::tma_load_2d(sa + q * WA_BOX, &tmA, &st.full[stage], w.m0 + q * 64, row);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              ptx::tma_load_2d(sb + q * WB_BOX, &tmB, &st.full[stage], w.n0 + q * 64, row);
+            for (int q = rank * BQ; q < (rank + 1) * BQ; ++q)
+              w_load_b<CL>(sb + q * WB_BOX, &tmB, &st.full[stage], w.n0 + q * 64, row);
           } else {
             // the segment's last rows: whole 16-row groups from the operands,
             // the partial group from the zero-padded tail rows of expert e
             const int groups = (valid + W_GROUP - 1) / W_GROUP;
             const bool partial = (valid % W_GROUP) != 0;
             ptx::mbar_arrive_expect_tx(&st.full[stage], groups * 6 * W_GROUP_BYTES);
-            for (int g = 0; g < groups; ++g) {
-              const bool tail = partial && g == groups - 1;
+            for (int gr = 0; gr < groups; ++gr) {
+              const bool tail = partial && gr == groups - 1;
               const CUtensorMap *ma = tail ? &tmAt : &tmA16;
               const CUtensorMap *mb = tail ? &tmBt : &tmB16;
-              const int r = tail ? w.e * W_GROUP : row + g * W_GROUP;
+              const int r = tail ? w.e * W_GROUP : row + gr * W_GROUP;
 #pragma unroll
               for (int q = 0; q < 2; ++q)
-                ptx::tma_load_2d(sa + q * WA_BOX + g * W_GROUP_BYTES, ma, &st.full[stage],
+                ptx::tma_load_2d(sa + q * WA_BOX + gr * W_GROUP_BYTES, ma, &st.full[stage],
                                  w.m0 + q * 64, r);
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                ptx::tma_load_2d(sb + q * WB_BOX + g * W_GROUP_BYTES, mb, &st.full[stage],
-                                 w.n0 + q * 64, r);
+              for (int q = rank * BQ; q < (rank + 1) * BQ; ++q)
+                w_load_b<CL>(sb + q * WB_BOX + gr * W_GROUP_BYTES, mb, &st.full[stage],
+                             w.n0 + q * 64, r);
             }
           }
           used |= 1u << stage;
@@ -202,18 +234,28 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             phase ^= 1u;
           }
         }
-        if (stop) break;
       }
+      // copies into this CTA's stages (its own and its peers') have landed
       for (int s = 0; s < WSTAGES; ++s)
         if (used >> s & 1u) ptx::mbar_wait(&st.full[s], last_par >> s & 1u);
+      // and every CTA's MMAs have released every stage (their arrivals on
+      // this CTA's barriers are done before it may exit)
+      if (!stop && !*abort_flag)
+        for (int i = 0; i < WSTAGES; ++i) {
+          if (!w_wait(&st.empty[stage], phase ^ 1u, abort_flag, status)) break;
+          if (++stage == WSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
     }
   } else if (warp == 1) {
     // one thread issues the MMAs; the rest of the warp waits at the end
     if (lane == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const WTile w = w_decode(st, t, mt, nt);
+      for (int g = cid; g < total; g += ncl) {
+        const WTile w = w_decode<CL>(st, g, mt, nt, rank);
         if (!w_wait(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * WN);
@@ -234,7 +276,10 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             const uint64_t bdesc = ptx::smem_desc(b0 + kk * W_GROUP_BYTES, WB_BOX, 1024);
             ptx::mma_bf16(d, adesc, bdesc, W_IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(&st.empty[stage]);
+          if constexpr (CL == 1)
+            ptx::mma_commit(&st.empty[stage]);
+          else
+            ptx::mma_commit_multicast(&st.empty[stage], (uint16_t)((1u << CL) - 1));
           if (++stage == WSTAGES) {
             stage = 0;
             phase ^= 1u;
@@ -252,17 +297,17 @@ __global__ void __launch_bounds__(W_THREADS, 1)
   } else {
     // epilogue warps 2..5 -> TMEM lane quarter (warp % 4) = 32 rows of M
     const int q = warp & 3;
-    int acc = 0;
+    int acc = 0, nstore = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const WTile w = w_decode(st, t, mt, nt);
+    for (int g = cid; g < total; g += ncl) {
+      const WTile w = w_decode<CL>(st, g, mt, nt, rank);
       if (!w_wait(&st.tfull[acc], acc_phase, abort_flag, status)) break;
       ptx::tc_fence_after();
       const uint32_t tb = tmem + (uint32_t)(acc * WN) + ((uint32_t)(q * 32) << 16);
-      // rows of this warp's 32-row slice; each 32-column chunk is staged in
-      // shared memory and stored as whole 128-byte row segments (8 lanes a row)
-      float *base = out + ((size_t)w.e * M + w.m0 + q * 32) * N + w.n0;
-      uint8_t *eb = st.epi[warp - 2];
+      // each 32-column chunk of this warp's 32 rows goes through a swizzled
+      // staging buffer (lane = row; 16-byte piece j of row r at piece
+      // j ^ (r % 8): conflict-free) and leaves as one TMA tile store
+      const int orow = w.e * M + w.m0 + q * 32;
 #pragma unroll 1
       for (int c = 0; c < WN / 32; ++c) {
         uint32_t a[32];
@@ -273,18 +318,21 @@ __global__ void __launch_bounds__(W_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = 0u;
         }
-        uint4 *mine = reinterpret_cast<uint4 *>(eb + lane * 144);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) mine[v] = make_uint4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
+        uint8_t *buf = smemE + (2 * q + (nstore & 1)) * W_EPI_BYTES;
+        // the store that last read this buffer (two chunks ago) must be done
+        if (lane == 0) ptx::bulk_wait_group_read<1>();
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int p = lane + 32 * i;
-          const int r = p >> 3, c16 = p & 7;
-          const uint4 val = *reinterpret_cast<const uint4 *>(eb + r * 144 + c16 * 16);
-          *reinterpret_cast<uint4 *>(base + (size_t)r * N + c * 32 + c16 * 4) = val;
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4 *>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+              make_uint4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&tmOut, buf, w.n0 + c * 32, orow);
+          ptx::bulk_commit_group();
         }
-        __syncwarp();
+        ++nstore;
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -292,10 +340,14 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) ptx::bulk_wait_group<0>();  // this warp's stores are complete
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
   __syncthreads();
+  // no CTA leaves while a peer may still copy into it or arrive on it
+  if constexpr (CL > 1) ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     __syncwarp();
@@ -366,6 +418,80 @@ bool w_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint3
 
 }  // namespace
 
+// out viewed as (rows x cols) float32, boxes of 32 columns x 32 rows, 128-byte
+// swizzle (the epilogue's staging layout)
+bool w_out_map(CUtensorMap *m, float *base, uint64_t cols, uint64_t rows) {
+  EncodeFn enc = w_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// preferred cluster size (CTAs sharing the B operand); smaller when the M
+// tiles do not divide.  Measured at the OLMoE dW13 shape (GB300): 299 us with
+// pairs, 305 us with 4 CTAs, 311 us without clusters.
+constexpr int kWgradCluster = 2;
+
+struct WgradArgs {
+  CUtensorMap mA, mB, mA16, mB16, mAt, mBt, mOut;
+  const int32_t *offsets;
+  int E, nK, M, N;
+  int32_t *status;
+};
+
+// Persistent launch: as many clusters as fit on the device at once (cached
+// per device), at most one per work unit.
+template <int CL>
+cudaError_t wgrad_launch(const WgradArgs &p, cudaStream_t s) {
+  auto kernel = wgrad_tc_kernel<CL>;
+  static int clusters[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(W_THREADS);
+  cfg.dynamicSmemBytes = W_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (CL > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = CL;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (!clusters[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W_SMEM);
+    if (e != cudaSuccess) return e;
+    int nc = device_sm_count();
+    if (CL > 1) {
+      cfg.gridDim = dim3(CL * 16);
+      cfg.attrs = attr;
+      cfg.numAttrs = na;
+      e = cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+    }
+    if (nc < 1) return cudaErrorInvalidConfiguration;
+    clusters[dev] = nc;
+  }
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  const int units = p.E * (p.M / WM / CL) * (p.N / WN);
+  cfg.gridDim = dim3((unsigned)(CL * (units < clusters[dev] ? units : clusters[dev])));
+  return cudaLaunchKernelEx(&cfg, kernel, p.mA, p.mB, p.mA16, p.mB16, p.mAt, p.mBt, p.mOut,
+                            p.offsets, p.E, p.nK, p.M, p.N, p.status);
+}
+
 size_t wgrad_tail_bytes(const Desc &d, int M, int N) {
   return (size_t)d.E * W_GROUP * ((size_t)M + N) * 2;
 }
@@ -389,25 +515,18 @@ cudaError_t launch_wgrad_tc(const Desc &d, const void *a, int M, const void *b, 
       !w_map(&mA16, a, M, rows, W_GROUP) || !w_map(&mB16, b, N, rows, W_GROUP) ||
       !w_map(&mAt, ta, M, trows, W_GROUP) || !w_map(&mBt, tb, N, trows, W_GROUP))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaSuccess;
-  static int done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !done[dev]) {
-    e = cudaFuncSetAttribute(wgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)W_SMEM);
-    if (e != cudaSuccess) return e;
-    done[dev] = 1;
-  }
-  e = launch_pdl(wgrad_pack_tails_kernel, dim3(d.E * W_GROUP), dim3(256), 0, s,
-                 (const __nv_bfloat16 *)a, M, (const __nv_bfloat16 *)b, N, offsets, (int)nK, ta,
-                 tb);
+  CUtensorMap mOut;
+  if (!w_out_map(&mOut, out, N, (uint64_t)d.E * M)) return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(wgrad_pack_tails_kernel, dim3(d.E * W_GROUP), dim3(256), 0, s,
+                             (const __nv_bfloat16 *)a, M, (const __nv_bfloat16 *)b, N, offsets,
+                             (int)nK, ta, tb);
   if (e != cudaSuccess) return e;
-  const int total = d.E * (M / WM) * (N / WN);
-  const int sms = device_sm_count();
-  const int grid = total < sms ? total : sms;
-  return launch_pdl(wgrad_tc_kernel, dim3(grid), dim3(W_THREADS), W_SMEM, s, mA, mB, mA16, mB16,
-                    mAt, mBt, offsets, d.E, (int)nK, M, N, out, status);
+  const int mt = M / WM;
+  const int cl = mt % kWgradCluster == 0 ? kWgradCluster : (mt % 2 == 0 ? 2 : 1);
+  const WgradArgs args{mA, mB, mA16, mB16, mAt, mBt, mOut, offsets, d.E, (int)nK, M, N, status};
+  if (cl == 4) return wgrad_launch<4>(args, s);
+  if (cl == 2) return wgrad_launch<2>(args, s);
+  return wgrad_launch<1>(args, s);
 }
 
 }  // namespace moe

@@ -98,6 +98,29 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// Shared -> global tile store of the tensor map's box at (c0, c1); completion
+// is tracked per thread with bulk groups (commit, then wait).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0,
+                                             int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// at most N of this thread's bulk groups still reading their shared source
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// at most N of this thread's bulk groups not yet complete
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Four rows (r0..r3) of a 2-D tensor, each box[0] elements wide from column
 // c0, written as one 4-row tile (the tensor map's box is one row high).
 // Rows outside the tensor read the fill value (zero).
@@ -113,6 +136,17 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
 // The same box written to every CTA of the cluster named in cta_mask, at the
 // same shared-memory offset; each receiving CTA's mbarrier at `bar`'s offset
 // gets the transaction bytes.  Used only inside one GPU's own memory.
+__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *map,
+                                                      uint64_t *bar, int c0, int c1,
+                                                      uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
+      : "memory");
+}
+
+// As tma_load_2d_multicast, for a 3-D tensor map.
 __device__ __forceinline__ void tma_load_3d_multicast(void *dst, const CUtensorMap *map,
                                                       uint64_t *bar, int c0, int c1, int c2,
                                                       uint16_t cta_mask) {
