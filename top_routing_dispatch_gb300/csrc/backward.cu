@@ -10,8 +10,9 @@
 //     combine backward  dY[inv(t,k)] = w[t,k] dy[t],  dw[t,k] = <dy[t], Y[inv(t,k)]>
 //     permute backward  dx[t] = sum_k dx_perm[inv(t,k)]  (+ the router's term)
 //     router backward   dp from dw (through the renormalisation), dlogits =
-//                       p (dp - <p, dp>), dx += dlogits W_gate^T,
-//                       dW_gate = x^T dlogits, dbias = sum_t dlogits[t]
+//                       p (dp - <p, dp>), dx += dlogits W_gate^T (fused with the
+//                       permute backward), dW_gate = x^T dlogits,
+//                       dbias = sum_t dlogits[t]
 // Every sum has a fixed order: results are bitwise reproducible.
 #include "common.cuh"
 
@@ -47,8 +48,9 @@ __device__ __forceinline__ float warp_sum(float v) {  // fixed butterfly order
 
 // One warp per token: dy[t] is streamed once in 16-byte vectors; for each of
 // the K slots the Y row is read, <dy, Y> accumulated per lane in float32, and
-// dY = w dy written (bf16).  The K dot products are added over the lanes by a
-// fixed butterfly.
+// dY = w dy written (bf16).  All K row pieces of a vector are loaded before
+// any dY piece is stored, so the loads overlap.  The K dot products are added
+// over the lanes by a fixed butterfly.
 template <int KM>
 __global__ void __launch_bounds__(BT) combine_bwd_kernel(const uint4 *__restrict__ dy,
                                                          const uint4 *__restrict__ y_perm,
@@ -83,11 +85,16 @@ __global__ void __launch_bounds__(BT) combine_bwd_kernel(const uint4 *__restrict
     for (int v = lane; v < V; v += 32) {
       float g[8];
       bf16x8_to_f32(__ldg(dy + t * V + v), g);
+      uint4 yr[KM];
+#pragma unroll
+      for (int k = 0; k < KM; ++k)
+        yr[k] = (k < K && rows[k] >= 0) ? __ldg(y_perm + (size_t)rows[k] * V + v)
+                                        : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int k = 0; k < KM; ++k) {
         if (k >= K || rows[k] < 0) continue;
         float yv[8];
-        bf16x8_to_f32(__ldg(y_perm + (size_t)rows[k] * V + v), yv);
+        bf16x8_to_f32(yr[k], yv);
         float o[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -156,55 +163,72 @@ __global__ void __launch_bounds__(BT) router_bwd_kernel(const float *__restrict_
   }
 }
 
-// C[m][n] = sum over k in [k0, k1) of A(m,k) B(k,n), float32 accumulate in
-// ascending k, 32x32 output tiles, 256 threads (2x2 outputs each).
-// A(m,k) = a[m*sam + k*sak], B(k,n) = b[k*sbk + n*sbn].  AK / BK: the
-// operand's k stride is 1 (its tile is loaded with consecutive threads along
-// k, else along m / n), so either layout is read in whole sectors.
-// blockIdx.z selects the k range [z*kc, min(Kd, (z+1)*kc)) and the output
-// c + z*M*N (split-K partials, added later in order).
-template <typename TA, typename TB, bool AK, bool BK>
-__global__ void __launch_bounds__(BT) small_gemm_kernel(const TA *__restrict__ a, long long sam,
-                                                        long long sak, const TB *__restrict__ b,
-                                                        long long sbk, long long sbn,
-                                                        float *__restrict__ c, int M, int N,
-                                                        int Kd, int kc) {
+// Partial dW_gate over one token range: part[z][h][e] = sum over t in
+// [z*tc, min(n, (z+1)*tc)) of x[t][h] dlogits[t][e], ascending t, float32.
+// A block computes 64 h x 64 e (each thread 4 x 4); the tokens pass through
+// shared memory 32 at a time (x rows as 128-byte bf16 pieces, dlogits rows
+// coalesced over e).
+constexpr int GW_T = 32;
+__global__ void __launch_bounds__(BT) dw_gate_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                     const float *__restrict__ dl,
+                                                     float *__restrict__ part, int n, int H,
+                                                     int E, int tc) {
   pdl_enter();
-  __shared__ float As[32][32 + 1];
-  __shared__ float Bs[32][32 + 1];
-  const int m0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
-  const int kb = blockIdx.z * kc, ke = min(Kd, kb + kc);
-  c += (size_t)blockIdx.z * M * N;
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[2][2] = {};
-  for (int k0 = kb; k0 < ke; k0 += 32) {
-    for (int i = threadIdx.x; i < 32 * 32; i += BT) {
-      const int kk = AK ? i % 32 : i / 32, mm = AK ? i / 32 : i % 32;
-      const int gm = m0 + mm, gk = k0 + kk;
-      As[kk][mm] = (gm < M && gk < ke) ? (float)a[(long long)gm * sam + (long long)gk * sak] : 0.f;
+  __shared__ __align__(16) float xs[GW_T][64];
+  __shared__ __align__(16) float ds[GW_T][64];
+  const int h0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
+  const int t0 = blockIdx.z * tc, t1 = min(n, t0 + tc);
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float acc[4][4] = {};
+  // this thread's share of a chunk (32 tokens x 64 h of x: one 16-byte piece;
+  // 32 tokens x 64 e of dlogits: 8 values), loaded one chunk ahead
+  const int xr = tid >> 3, xc = tid & 7;
+  uint4 xv_next = make_uint4(0u, 0u, 0u, 0u);
+  float dv_next[GW_T * 64 / BT];
+  auto fetch = [&](int tb) {
+    xv_next = tb + xr < t1
+                  ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(tb + xr) * H + h0 + xc * 8))
+                  : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int q = 0; q < GW_T * 64 / BT; ++q) {
+      const int i = tid + q * BT, r = i >> 6, c = i & 63;
+      dv_next[q] = (tb + r < t1 && e0 + c < E) ? __ldg(dl + (size_t)(tb + r) * E + e0 + c) : 0.f;
     }
-    for (int i = threadIdx.x; i < 32 * 32; i += BT) {
-      const int kk = BK ? i % 32 : i / 32, nn = BK ? i / 32 : i % 32;
-      const int gn = n0 + nn, gk = k0 + kk;
-      Bs[kk][nn] = (gn < N && gk < ke) ? (float)b[(long long)gk * sbk + (long long)gn * sbn] : 0.f;
+  };
+  if (t0 < t1) fetch(t0);
+  for (int tb = t0; tb < t1; tb += GW_T) {
+    {
+      float f[8];
+      bf16x8_to_f32(xv_next, f);
+      *reinterpret_cast<float4 *>(&xs[xr][xc * 8]) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4 *>(&xs[xr][xc * 8 + 4]) = make_float4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+      for (int q = 0; q < GW_T * 64 / BT; ++q) {
+        const int i = tid + q * BT;
+        ds[i >> 6][i & 63] = dv_next[q];
+      }
     }
     __syncthreads();
+    if (tb + GW_T < t1) fetch(tb + GW_T);  // in flight while this chunk is used
+#pragma unroll 8
+    for (int tt = 0; tt < GW_T; ++tt) {
+      const float4 xv = *reinterpret_cast<const float4 *>(&xs[tt][ty * 4]);
+      const float4 dv = *reinterpret_cast<const float4 *>(&ds[tt][tx * 4]);
+      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
-    for (int kk = 0; kk < 32; ++kk) {
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-          acc[i][j] = fmaf(As[kk][ty * 2 + i], Bs[kk][tx * 2 + j], acc[i][j]);
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], da[j], acc[i][j]);
     }
     __syncthreads();
   }
+  float *out = part + (size_t)blockIdx.z * H * E;
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int gm = m0 + ty * 2 + i, gn = n0 + tx * 2 + j;
-      if (gm < M && gn < N) c[(long long)gm * N + gn] = acc[i][j];
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) out[(size_t)(h0 + ty * 4 + i) * E + e] = acc[i][j];
     }
 }
 
@@ -247,41 +271,114 @@ __global__ void __launch_bounds__(BT) column_sum_kernel(const float *__restrict_
   }
 }
 
-// dx[t] = sum_k dx_perm[inv(t,k)] (slot order) + dx_router[t], float32, one rounding
+// dx[t][h] = sum_e dlogits[t][e] W_gate[h][e] (ascending e) + sum_k
+// dx_perm[inv(t,k)][h] (slot order), float32, one rounding to bf16: the
+// router's term as a small GEMM (K = E) with the permute backward in its
+// epilogue.  A block computes 128 tokens x 128 h; dlogits and W_gate pass
+// through shared memory in chunks of 32 experts, transposed (expert-major) so
+// that each k step is four 16-byte loads for 64 FMAs.  A thread holds 8
+// tokens x two 4-wide h quads 64 apart (conflict-free loads; each quad of the
+// gathered rows and of dx is an 8-byte piece of a 128-byte run).
+constexpr int DX_T = 128, DX_H = 128, DX_E = 32, DX_P = DX_T + 4;
+static_assert(DX_T == DX_H, "one padded row length for both tiles");
+
+__device__ __forceinline__ void bf16x4_to_f32(uint2 v, float *f) {
+  const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&v);
+  const float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
+  f[0] = a.x;
+  f[1] = a.y;
+  f[2] = b.x;
+  f[3] = b.y;
+}
+
+__device__ __forceinline__ uint2 f32_to_bf16x4(const float *f) {
+  uint2 o;
+  __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&o);
+  p[0] = __floats2bfloat162_rn(f[0], f[1]);
+  p[1] = __floats2bfloat162_rn(f[2], f[3]);
+  return o;
+}
+
 template <int KM>
-__global__ void __launch_bounds__(BT) dx_gather_kernel(const uint4 *__restrict__ dxp,
-                                                       const float4 *__restrict__ dxr,
-                                                       const int32_t *__restrict__ inv,
-                                                       uint4 *__restrict__ dx, int n, int K,
-                                                       int V, long long nK) {
+__global__ void __launch_bounds__(BT) dx_final_kernel(const __nv_bfloat16 *__restrict__ dxp,
+                                                      const float *__restrict__ dl,
+                                                      const __nv_bfloat16 *__restrict__ wg,
+                                                      const int32_t *__restrict__ inv,
+                                                      __nv_bfloat16 *__restrict__ dx, int n, int K,
+                                                      int E, int H, long long nK) {
   pdl_enter();
-  const int lane = threadIdx.x & 31;
-  const long long wid = ((long long)blockIdx.x * BT + threadIdx.x) >> 5;
-  const long long nw = ((long long)gridDim.x * BT) >> 5;
-  for (long long t = wid; t < n; t += nw) {
-    int rows[KM];
+  __shared__ __align__(16) float ds[DX_E][DX_P];  // [e][token]
+  __shared__ __align__(16) float ws[DX_E][DX_P];  // [e][h]
+  __shared__ int srow[DX_T][KM];                   // the tokens' expert rows, -1: none
+  const long long tb = (long long)blockIdx.x * DX_T;
+  const int h0 = blockIdx.y * DX_H;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  for (int i = threadIdx.x; i < DX_T * KM; i += BT) {
+    const int t = i / KM, k = i % KM;
+    int r = -1;
+    if (tb + t < n && k < K) {
+      r = __ldg(inv + (tb + t) * K + k);
+      if (r < 0 || (long long)r >= nK) r = -1;
+    }
+    srow[t][k] = r;
+  }
+  float acc[8][8];
 #pragma unroll
-    for (int k = 0; k < KM; ++k) {
-      rows[k] = -1;
-      if (k < K) {
-        const int r = __ldg(inv + t * K + k);
-        rows[k] = (r >= 0 && (long long)r < nK) ? r : -1;
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int e0 = 0; e0 < E; e0 += DX_E) {
+    for (int i = threadIdx.x; i < DX_T * DX_E; i += BT) {
+      const int t = i / DX_E, e = i % DX_E;
+      ds[e][t] = (tb + t < n && e0 + e < E) ? dl[(tb + t) * E + e0 + e] : 0.f;
+      ws[e][t] = (e0 + e < E) ? __bfloat162float(wg[(size_t)(h0 + t) * E + e0 + e]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int k = 0; k < DX_E; ++k) {
+      const float4 a0 = *reinterpret_cast<const float4 *>(&ds[k][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4 *>(&ds[k][ty * 8 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4 *>(&ws[k][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4 *>(&ws[k][64 + tx * 4]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  // + each token's K expert rows in slot order (slot outer: the 16 row pieces
+  // of one slot are loaded before any is added), then one rounding
+  const int hq0 = h0 + tx * 4, hq1 = h0 + 64 + tx * 4;
+#pragma unroll 1
+  for (int k = 0; k < K; ++k) {
+    uint2 raw[8][2];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = srow[ty * 8 + i][k];
+      raw[i][0] = raw[i][1] = make_uint2(0u, 0u);
+      if (r >= 0) {
+        raw[i][0] = __ldg(reinterpret_cast<const uint2 *>(dxp + (size_t)r * H + hq0));
+        raw[i][1] = __ldg(reinterpret_cast<const uint2 *>(dxp + (size_t)r * H + hq1));
       }
     }
-    for (int v = lane; v < V; v += 32) {
-      float acc[8];
-      const float4 r0 = dxr[(t * V + v) * 2], r1 = dxr[(t * V + v) * 2 + 1];
-      acc[0] = r0.x; acc[1] = r0.y; acc[2] = r0.z; acc[3] = r0.w;
-      acc[4] = r1.x; acc[5] = r1.y; acc[6] = r1.z; acc[7] = r1.w;
 #pragma unroll
-      for (int k = 0; k < KM; ++k) {
-        if (k >= K || rows[k] < 0) continue;
-        float f[8];
-        bf16x8_to_f32(__ldg(dxp + (size_t)rows[k] * V + v), f);
+    for (int i = 0; i < 8; ++i) {
+      float f[8];
+      bf16x4_to_f32(raw[i][0], f);
+      bf16x4_to_f32(raw[i][1], f + 4);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += f[i];
-      }
-      dx[t * V + v] = f32_to_bf16x8(acc);
+      for (int j = 0; j < 8; ++j) acc[i][j] += f[j];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const long long t = tb + ty * 8 + i;
+    if (t < n) {
+      *reinterpret_cast<uint2 *>(dx + t * H + hq0) = f32_to_bf16x4(acc[i]);
+      *reinterpret_cast<uint2 *>(dx + t * H + hq1) = f32_to_bf16x4(acc[i] + 4);
     }
   }
 }
@@ -303,13 +400,12 @@ cudaError_t combine_bwd_k(const Desc &d, const void *dy, const void *y_perm, con
 }
 
 template <int KM>
-cudaError_t dx_gather_k(const Desc &d, const void *dx_perm, const float *dx_router,
-                        const int32_t *inv, void *dx, cudaStream_t s) {
-  const int V = d.H * 2 / 16;
-  return launch_pdl(dx_gather_kernel<KM>, dim3(grid_warps(d.n)), dim3(BT), 0, s,
-                    reinterpret_cast<const uint4 *>(dx_perm),
-                    reinterpret_cast<const float4 *>(dx_router), inv,
-                    reinterpret_cast<uint4 *>(dx), d.n, d.K, V, d.nK());
+cudaError_t dx_final_k(const Desc &d, const void *dx_perm, const float *dlogits,
+                       const void *w_gate, const int32_t *inv, void *dx, cudaStream_t s) {
+  return launch_pdl(dx_final_kernel<KM>, dim3((d.n + DX_T - 1) / DX_T, d.H / DX_H), dim3(BT), 0,
+                    s, reinterpret_cast<const __nv_bfloat16 *>(dx_perm), dlogits,
+                    reinterpret_cast<const __nv_bfloat16 *>(w_gate), inv,
+                    reinterpret_cast<__nv_bfloat16 *>(dx), d.n, d.K, d.E, d.H, d.nK());
 }
 
 }  // namespace
@@ -324,29 +420,20 @@ cudaError_t launch_combine_bwd(const Desc &d, const void *dy, const void *y_perm
   return combine_bwd_k<kMaxK>(d, dy, y_perm, topk_w, inv_perm, dY, dw, status, s);
 }
 
-cudaError_t launch_router_bwd(const Desc &d, const void *x, const void *w_gate,
-                              const float *logits, const int32_t *topk_idx, const float *topk_w,
-                              const float *dw, float *dlogits, float *dx_router,
-                              float *dw_part, float *dw_gate, float *dbias, cudaStream_t s) {
+cudaError_t launch_router_bwd(const Desc &d, const void *x, const float *logits,
+                              const int32_t *topk_idx, const float *topk_w, const float *dw,
+                              float *dlogits, float *dw_part, float *dw_gate, float *dbias,
+                              cudaStream_t s) {
   if (d.n == 0) return cudaSuccess;
   cudaError_t e = launch_pdl(router_bwd_kernel, dim3(grid_warps(d.n)), dim3(BT), 0, s, logits,
                              topk_idx, topk_w, dw, dlogits, d.n, d.E, d.K, d.norm ? 1 : 0);
   if (e != cudaSuccess) return e;
-  const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
-  const __nv_bfloat16 *wg = reinterpret_cast<const __nv_bfloat16 *>(w_gate);
-  // dx_router[t][h] = sum_e dlogits[t][e] W_gate[h][e]   (both k-contiguous)
-  e = launch_pdl(small_gemm_kernel<float, __nv_bfloat16, true, true>,
-                 dim3((d.n + 31) / 32, (d.H + 31) / 32, 1), dim3(BT), 0, s,
-                 (const float *)dlogits, (long long)d.E, 1ll, wg, 1ll, (long long)d.E, dx_router,
-                 d.n, d.H, d.E, d.E);
-  if (e != cudaSuccess) return e;
   // dW_gate[h][e] = sum_t x[t][h] dlogits[t][e]: the tokens split into
   // RB_SPLIT ranges (partials in dw_part), then added in order
   const int kc = (d.n + RB_SPLIT - 1) / RB_SPLIT;
-  e = launch_pdl(small_gemm_kernel<__nv_bfloat16, float, false, false>,
-                 dim3((d.H + 31) / 32, (d.E + 31) / 32, RB_SPLIT), dim3(BT), 0, s, xb, 1ll,
-                 (long long)d.H, (const float *)dlogits, (long long)d.E, 1ll, dw_part, d.H, d.E,
-                 d.n, kc);
+  e = launch_pdl(dw_gate_kernel, dim3(d.H / 64, (d.E + 63) / 64, RB_SPLIT), dim3(BT), 0, s,
+                 reinterpret_cast<const __nv_bfloat16 *>(x), (const float *)dlogits, dw_part, d.n,
+                 d.H, d.E, kc);
   if (e != cudaSuccess) return e;
   const long long cnt = (long long)d.H * d.E;
   e = launch_pdl(sum_parts_kernel, dim3((int)((cnt + BT - 1) / BT)), dim3(BT), 0, s,
@@ -361,13 +448,14 @@ cudaError_t launch_router_bwd(const Desc &d, const void *x, const void *w_gate,
                     (const float *)bpart, dbias, (long long)d.E, RB_SPLIT);
 }
 
-cudaError_t launch_dx_gather(const Desc &d, const void *dx_perm, const float *dx_router,
-                             const int32_t *inv_perm, void *dx, cudaStream_t s) {
+cudaError_t launch_dx_final(const Desc &d, const void *dx_perm, const float *dlogits,
+                            const void *w_gate, const int32_t *inv_perm, void *dx,
+                            cudaStream_t s) {
   if (d.n == 0) return cudaSuccess;
-  if (d.K <= 2) return dx_gather_k<2>(d, dx_perm, dx_router, inv_perm, dx, s);
-  if (d.K <= 4) return dx_gather_k<4>(d, dx_perm, dx_router, inv_perm, dx, s);
-  if (d.K <= 8) return dx_gather_k<8>(d, dx_perm, dx_router, inv_perm, dx, s);
-  return dx_gather_k<kMaxK>(d, dx_perm, dx_router, inv_perm, dx, s);
+  if (d.K <= 2) return dx_final_k<2>(d, dx_perm, dlogits, w_gate, inv_perm, dx, s);
+  if (d.K <= 4) return dx_final_k<4>(d, dx_perm, dlogits, w_gate, inv_perm, dx, s);
+  if (d.K <= 8) return dx_final_k<8>(d, dx_perm, dlogits, w_gate, inv_perm, dx, s);
+  return dx_final_k<kMaxK>(d, dx_perm, dlogits, w_gate, inv_perm, dx, s);
 }
 
 }  // namespace moe

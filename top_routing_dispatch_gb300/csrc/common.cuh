@@ -80,12 +80,13 @@ constexpr int kRouterBwdSplit = 16;  // token ranges of the dW_gate reduction
 cudaError_t launch_combine_bwd(const Desc &d, const void *dy, const void *y_perm,
                                const float *topk_w, const int32_t *inv_perm, void *dY, float *dw,
                                int32_t *status, cudaStream_t s);
-cudaError_t launch_router_bwd(const Desc &d, const void *x, const void *w_gate,
-                              const float *logits, const int32_t *topk_idx, const float *topk_w,
-                              const float *dw, float *dlogits, float *dx_router,
-                              float *dw_part, float *dw_gate, float *dbias, cudaStream_t s);
-cudaError_t launch_dx_gather(const Desc &d, const void *dx_perm, const float *dx_router,
-                             const int32_t *inv_perm, void *dx, cudaStream_t s);
+cudaError_t launch_router_bwd(const Desc &d, const void *x, const float *logits,
+                              const int32_t *topk_idx, const float *topk_w, const float *dw,
+                              float *dlogits, float *dw_part, float *dw_gate, float *dbias,
+                              cudaStream_t s);
+cudaError_t launch_dx_final(const Desc &d, const void *dx_perm, const float *dlogits,
+                            const void *w_gate, const int32_t *inv_perm, void *dx,
+                            cudaStream_t s);
 cudaError_t launch_gemm_dgrad_tc(const Desc &d, const void *a, const void *w, int Kdim, int Nout,
                                  const int32_t *offsets, void *out, int32_t *status,
                                  cudaStream_t s);

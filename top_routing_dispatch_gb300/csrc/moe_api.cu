@@ -504,23 +504,23 @@ moe_status_t moe_forward_host(const moe_layer_desc_t *desc, const void *x_host,
 }
 
 // backward workspace: dY (nK,H) bf16 | dw (nK) f32 | dh (nK,I) bf16 | dGU (nK,2I) bf16 |
-// dx_perm (nK,H) bf16 | dlogits (n,E) f32 | dx_router (n,H) f32 |
-// dW_gate partials (16,H,E) and dbias partials (16,E) f32 | the weight
-// gradients' zero-padded tail rows (E*16 rows of both operands, bf16)
+// dx_perm (nK,H) bf16 | dlogits (n,E) f32 | dW_gate partials (16,H,E) and
+// dbias partials (16,E) f32 | the weight gradients' zero-padded tail rows
+// (E*16 rows of both operands, bf16)
 namespace {
 struct BwdSlots {
-  size_t off[9];
+  size_t off[8];
   size_t total;
 };
 BwdSlots bwd_slots(const Desc &d) {
   const size_t nK = (size_t)d.nK();
-  const size_t sz[9] = {nK * d.H * 2, nK * 4, nK * d.I * 2, nK * 2 * d.I * 2, nK * d.H * 2,
-                        (size_t)d.n * d.E * 4, (size_t)d.n * d.H * 4,
+  const size_t sz[8] = {nK * d.H * 2, nK * 4, nK * d.I * 2, nK * 2 * d.I * 2, nK * d.H * 2,
+                        (size_t)d.n * d.E * 4,
                         (size_t)kRouterBwdSplit * (d.H + 1) * d.E * 4,
                         wgrad_tail_bytes(d, d.H, 2 * d.I)};  // >= the (I, H) pair's
   BwdSlots b;
   size_t o = 0;
-  for (int i = 0; i < 9; ++i) {
+  for (int i = 0; i < 8; ++i) {
     b.off[i] = o;
     o += up(sz[i]);
   }
@@ -562,9 +562,8 @@ moe_status_t moe_backward(const moe_layer_desc_t *desc, const void *x, const voi
   void *dgu = w + b.off[3];
   void *dxp = w + b.off[4];
   float *dl = reinterpret_cast<float *>(w + b.off[5]);
-  float *dxr = reinterpret_cast<float *>(w + b.off[6]);
-  float *dwp = reinterpret_cast<float *>(w + b.off[7]);
-  void *tails = w + b.off[8];
+  float *dwp = reinterpret_cast<float *>(w + b.off[6]);
+  void *tails = w + b.off[7];
   cudaStream_t s = stream;
   cudaError_t e = cudaSuccess;
   // combine backward (a dispatch): dY = w dy in expert order, dw = <dy, Y>
@@ -582,9 +581,8 @@ moe_status_t moe_backward(const moe_layer_desc_t *desc, const void *x, const voi
     e = launch_wgrad_tc(d, x_perm, d.H, dgu, 2 * d.I, offsets, tails, dw13, status_word, s);
   // router backward, then dx = sum of the slots' dX rows (a combine) + router term
   if (e == cudaSuccess)
-    e = launch_router_bwd(d, x, w_gate, logits, topk_idx, topk_w, dwt, dl, dxr, dwp, dw_gate,
-                          dbias, s);
-  if (e == cudaSuccess) e = launch_dx_gather(d, dxp, dxr, inv_perm, dx, s);
+    e = launch_router_bwd(d, x, logits, topk_idx, topk_w, dwt, dl, dwp, dw_gate, dbias, s);
+  if (e == cudaSuccess) e = launch_dx_final(d, dxp, dl, w_gate, inv_perm, dx, s);
   return cuda_status(e);
 }
 
