@@ -22,6 +22,11 @@ CASES = [
               norm_topk_prob=False, seed=42, skew=True),
     MoEConfig("bwd_one_token", n=1, H=256, I=128, E=8, K=2, dtype="bf16", norm_topk_prob=True,
               seed=43),
+    # K = 12 (the 16-slot kernels), E = 20 (not a multiple of 8; the FMA router)
+    MoEConfig("bwd_k12", n=150, H=256, I=128, E=32, K=12, dtype="bf16", norm_topk_prob=True,
+              seed=45),
+    MoEConfig("bwd_e20", n=300, H=512, I=384, E=20, K=3, dtype="bf16", norm_topk_prob=False,
+              seed=46),
 ]
 TOL = 2e-2
 
