@@ -180,3 +180,37 @@ def test_forward_host_argument_checks(lib):
     assert call(nbytes=need - 1) == 3                           # MOE_ERR_WORKSPACE
     assert call(dd=_desc(n=64, H=256, I=100, E=8, K=2)) == 2    # bf16 GEMM needs I % 128
     assert call(dd=_desc(n=64, H=256, I=128, E=8, K=2), x=nullp) == 1
+
+
+@needs_nvcc
+def test_backward_workspace_and_argument_checks(lib):
+    """moe_backward_workspace_size is the sum of its 256-byte-aligned slots
+    (dY, dw, dh, dG|dU, dx_perm, dlogits, the 16 dW_gate/dbias partials, the
+    weight gradients' 16-row tails), and moe_backward rejects bad arguments
+    before any CUDA call."""
+    up = lambda b: (b + 255) // 256 * 256
+    n, H, I, E, K = 4096, 2048, 1024, 64, 8
+    nK = n * K
+    d = _desc()
+    want = sum(up(b) for b in (nK * H * 2, nK * 4, nK * I * 2, nK * 2 * I * 2, nK * H * 2,
+                               n * E * 4, 16 * (H + 1) * E * 4, E * 16 * (H + 2 * I) * 2))
+    need = lib.moe_backward_workspace_size(ctypes.byref(d))
+    assert need == want
+    assert lib.moe_backward_workspace_size(ctypes.byref(_desc(E=0))) == 0
+    nullp = ctypes.c_void_p(None)
+    fake = ctypes.c_void_p(1 << 12)  # never dereferenced: every call below fails first
+    ws = ctypes.c_void_p(1 << 20)
+
+    def call(dd=d, x=fake, dy=fake, dx=fake, dw13=fake, wsp=ws, nbytes=need):
+        a = [x, fake, fake, fake, dy] + [fake] * 8 + [dx, fake, nullp, dw13, fake]
+        return lib.moe_backward(ctypes.byref(dd), *a, wsp, nbytes, nullp, nullp)
+    assert call(dd=_desc(dtype=0)) == 2                      # float32 layers: unsupported
+    assert call(dd=_desc(H=2112)) == 2                       # H % 256
+    assert call(dd=_desc(I=1088)) == 2                       # I % 128
+    assert call(x=nullp) == 1
+    assert call(dy=nullp) == 1
+    assert call(dw13=nullp) == 1
+    assert call(wsp=nullp) == 1
+    assert call(wsp=ctypes.c_void_p((1 << 20) + 16)) == 1    # ws not 256-byte aligned
+    assert call(dx=ctypes.c_void_p((1 << 12) + 8)) == 1      # dx not 16-byte aligned
+    assert call(nbytes=need - 1) == 3                        # MOE_ERR_WORKSPACE
