@@ -302,9 +302,10 @@ class Timer:
         self.stream = stream
         self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def prep(self):
+    def prep(self, flush=True):
         with self.torch.cuda.stream(self.stream):
-            self.flush.zero_()
+            if flush:
+                self.flush.zero_()
             self.torch.cuda._sleep(300_000)
 
     def event(self):
@@ -363,8 +364,8 @@ def run_ours(args, cfg):
     ]
     T = Timer(torch, stream, dev)
 
-    def phased_step():
-        T.prep()
+    def phased_step(flush=True):
+        T.prep(flush)
         evs = [T.event()]
         for _, fn in phases:
             fn()
@@ -396,6 +397,12 @@ def run_ours(args, cfg):
     clk = clocks.stop()
     per_phase = {name: [s[i].elapsed_time(s[i + 1]) for s in steps]
                  for i, (name, _) in enumerate(phases)}
+    # the same without the L2 flush (each row finds its predecessor's output
+    # and, across steps, whatever of the weights L2 still holds)
+    warm_steps = [phased_step(flush=False) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    per_phase_warm = {name: [s[i].elapsed_time(s[i + 1]) for s in warm_steps]
+                      for i, (name, _) in enumerate(phases)}
     phased_ms = [s[0].elapsed_time(s[-1]) for s in steps]
     total_ms = max_over_ranks(sum(fwd_ms), dist, dev)
     status = M.moe_check_status(st, stream)
@@ -454,16 +461,33 @@ def run_ours(args, cfg):
             k["tflops"] = a["flop"] / (ms * 1e-3) / 1e12
         if name.startswith("gemm"):
             k["frac_bf16"] = k["tflops"] / peaks["bf16_tflops"]
+        # the kernel's own roofline: the larger of its tensor time (GEMMs and
+        # the tensor-core router) and its HBM time, over the measured time
+        on_tc = cfg.dtype == "bf16" and (name.startswith("gemm") or name == "router")
+        t_tensor = a["flop"] / (peaks["bf16_tflops"] * 1e12) if on_tc else 0.0
+        t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        k["roofline_bound"] = "tensor" if t_tensor >= t_hbm else "hbm"
+        k["frac_roofline"] = max(t_tensor, t_hbm) / (ms * 1e-3)
+        if name in per_phase_warm:
+            k["ms_warm"] = statistics.mean(per_phase_warm[name])
         kernels[name] = k
     g1 = kernels["gemm1"]
-    roofline = {"bound": "tensor", "kernel": "grouped_gemm_tc_kernel<1> (GEMM1 + SwiGLU)",
-                "achieved": g1["tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": g1["tflops"] / peaks["bf16_tflops"],
-                "peak_source": f"{peak_src} bf16 burst" + (" (of measured)" if peak_src ==
-                                                            "measured" else " (of fallback)"),
-                "traffic": recorded_traffic("gemm1_olmoe_bf16.md", GEMM_SOURCES),
-                "algorithmic_flop_per_launch": alg["gemm1"]["flop"],
-                "algorithmic_bytes_per_launch": alg["gemm1"]["bytes"]}
+    if g1["roofline_bound"] == "tensor":
+        roofline = {"bound": "tensor", "achieved": g1["tflops"], "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": g1["tflops"] / peaks["bf16_tflops"]}
+    else:  # the expert weights dominate (e.g. the DeepSeek-V3-sized layer)
+        roofline = {"bound": "hbm", "achieved": g1["gbs"], "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": g1["gbs"] / peaks["hbm_gbs"]}
+    peak_kind = "bf16 burst" if roofline["bound"] == "tensor" else "HBM copy"
+    roofline.update({
+        "kernel": "grouped_gemm_tc_kernel<1> (GEMM1 + SwiGLU)",
+        "peak_source": f"{peak_src} {peak_kind}" + (" (of measured)" if peak_src == "measured"
+                                                    else " (of fallback)"),
+        # DRAM bytes per launch from the ncu capture of this workload's GEMM1
+        "traffic": (recorded_traffic("gemm1_olmoe_bf16.md", GEMM_SOURCES)
+                    if cfg.name == "olmoe_bf16" else None),
+        "algorithmic_flop_per_launch": alg["gemm1"]["flop"],
+        "algorithmic_bytes_per_launch": alg["gemm1"]["bytes"]})
 
     out = {
         "metric": METRIC, "value": aggregate_tokens_per_s(cfg.n, args.steps, world, total_ms),
