@@ -17,7 +17,7 @@
  *    blocks.
  *  - Argument errors are returned synchronously, before anything is enqueued:
  *    MOE_ERR_INVALID_ARG (null pointer, bad size, misaligned pointer),
- *    MOE_ERR_UNSUPPORTED (a size this build does not handle),
+ *    MOE_ERR_UNSUPPORTED (a size the library does not handle),
  *    MOE_ERR_WORKSPACE (workspace too small).  A failed launch returns
  *    MOE_ERR_CUDA.
  *  - Problems found on the device (an expert id outside [0, E), an
