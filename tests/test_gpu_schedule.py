@@ -45,6 +45,25 @@ def test_two_stream_equals_sequential_bitwise():
         assert rel_fro(f64(y[ti]), r["y"]) <= TOL["bf16"]
 
 
+def test_four_micro_batches_two_streams_bitwise():
+    """Four micro-batches through the two-stream schedule (every cross-batch
+    dependency of the pipeline used more than once) equal four single-stream
+    calls bit for bit."""
+    cfg = MoEConfig("mb4_bf16", n=512, H=2048, I=1024, E=64, K=8, dtype="bf16",
+                    norm_topk_prob=False, seed=36)
+    dev = torch.device("cuda:0")
+    L, four = _layer(cfg, 4)
+    xs = [synth.make_x(cfg, dev, seed=60 + i) for i in range(4)]
+    sc, sd = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    ys = four.forward(xs, compute=sc, dispatch=sd)
+    torch.cuda.synchronize()
+    four.check()
+    one = M.MoELayer(M.desc_for(cfg), L["w_gate"], L["bias"], L["w13"], L["w2"])
+    for x, y in zip(xs, ys):
+        assert torch.equal(one(x), y)
+
+
 @pytest.mark.parametrize("reserve", [8, 40, 140])
 def test_sm_reserve_does_not_change_results(reserve):
     cfg = MoEConfig("reserve_bf16", n=700, H=256, I=256, E=8, K=2, dtype="bf16",
