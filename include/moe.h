@@ -315,7 +315,8 @@ void *moe_workspace_slot(const moe_layer_desc_t *desc, void *ws, int mb, int whi
  * moe_expert_gemm1_swiglu (h) and the UNWEIGHTED moe_expert_gemm2 (y_perm).
  * Outputs: dx (n,H) bf16; dw_gate (H,E), dbias (E, or NULL), dw13 (E,H,2I),
  * dw2 (E,I,H) float32.  ws: moe_backward_workspace_size(desc) bytes, 256-byte
- * aligned.  Every sum has a fixed order (bitwise reproducible).
+ * aligned.  Every sum has a fixed order (bitwise reproducible).  n = 0: the
+ * weight gradients are zeroed and the token arrays (and ws) may be NULL.
  */
 size_t moe_backward_workspace_size(const moe_layer_desc_t *desc);
 moe_status_t moe_backward(const moe_layer_desc_t *desc, const void *x, const void *w_gate,

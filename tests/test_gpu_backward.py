@@ -189,3 +189,23 @@ def test_backward_segment_lengths_at_block_edges():
         assert rel_fro(f64(r["dw2"][e]), o["dw2"][e]) <= TOL, e
     assert rel_fro(f64(r["dx"]), o["dx"]) <= TOL
     assert rel_fro(f64(r["dwg"]), o["dw_gate"]) <= TOL
+
+
+def test_backward_zero_tokens():
+    """No tokens: every weight gradient is zero; token arrays may be empty."""
+    import top_routing_dispatch_gb300 as M
+    cfg = MoEConfig("bwd_empty", n=0, H=256, I=128, E=8, K=2, dtype="bf16", norm_topk_prob=True,
+                    seed=47)
+    dev = torch.device("cuda:0")
+    L = synth.make_layer(cfg, dev)
+    desc = M.desc_for(cfg)
+    e = lambda shape, dt: torch.full(shape, 7.0, dtype=dt, device=dev)
+    none = torch.empty(0, dtype=torch.bfloat16, device=dev)
+    dwg, dbias = e((cfg.H, cfg.E), torch.float32), e((cfg.E,), torch.float32)
+    dw13 = e((cfg.E, cfg.H, 2 * cfg.I), torch.float32)
+    dw2 = e((cfg.E, cfg.I, cfg.H), torch.float32)
+    M.moe_backward(desc, none, L["w_gate"], L["w13"], L["w2"], none, none, none, none, none,
+                   none, none, none, none, none, dwg, dbias, dw13, dw2, none)
+    torch.cuda.synchronize()
+    for t in (dwg, dbias, dw13, dw2):
+        assert int(torch.count_nonzero(t)) == 0

@@ -546,6 +546,15 @@ moe_status_t moe_backward(const moe_layer_desc_t *desc, const void *x, const voi
   moe_status_t st = check_desc(desc, &d);
   if (st != MOE_OK) return st;
   if (!d.bf16 || d.H % 256 || d.I % 128) return MOE_ERR_UNSUPPORTED;
+  if (d.n == 0) {  // no tokens: every gradient is zero (token arrays may be NULL)
+    if (!w_gate || !w13 || !w2 || !dw_gate || !dw13 || !dw2) return MOE_ERR_INVALID_ARG;
+    const size_t E = d.E, H = d.H, I = d.I;
+    cudaError_t e = cudaMemsetAsync(dw_gate, 0, H * E * 4, stream);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, E * 4, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw13, 0, E * H * 2 * I * 4, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, E * I * H * 4, stream);
+    return cuda_status(e);
+  }
   if (!x || !w_gate || !w13 || !w2 || !dy || !logits || !topk_idx || !topk_w || !offsets ||
       !inv_perm || !x_perm || !h || !y_perm || !dx || !dw_gate || !dw13 || !dw2 || !ws)
     return MOE_ERR_INVALID_ARG;
