@@ -19,7 +19,10 @@ constexpr int PU = 8;     // 16-byte vectors in flight per lane
 
 // Permute: warp w copies the contiguous row range [w*nK/W, (w+1)*nK/W) of
 // x_perm (its writes are one contiguous block), two rows per step with every
-// load of both rows issued before their stores.
+// load of both rows issued before their stores.  The x_perm stores carry the
+// streaming (evict-first) cache hint, so the written rows do not push x,
+// which is re-read K times, out of L2 (measured: 30.5 -> 27.3 us at the
+// OLMoE shape, 134.6 -> 126.9 us for the skewed layer).
 __global__ void __launch_bounds__(PT) permute_kernel(const uint4 *__restrict__ x,
                                                      const int32_t *__restrict__ perm,
                                                      uint4 *__restrict__ xp, long long nK, int K,
@@ -56,7 +59,7 @@ __global__ void __launch_bounds__(PT) permute_kernel(const uint4 *__restrict__ x
 #pragma unroll
         for (int u = 0; u < PU; ++u) {
           const int v = v0 + u * 32 + lane;
-          if (v < V) dst[v] = buf[q][u];
+          if (v < V) __stcs(dst + v, buf[q][u]);  // streaming: x stays in L2
         }
       }
     }
