@@ -19,7 +19,9 @@
 // (zeroing the rows in place with a fence there cost about 2 us per tile).  A
 // tile of an expert without rows is written as zeros.  float32 output, written
 // by TMA tile stores from swizzled shared-memory staging buffers; one CTA per
-// SM, persistent, double-buffered TMEM accumulators as in gemm_tc.cu.
+// SM, persistent, double-buffered TMEM accumulators as in gemm_tc.cu; CTA
+// pairs of a cluster compute neighbouring M tiles and share the B operand
+// through TMA multicast (wgrad_tc_kernel<CL> below).
 #include <cuda.h>
 
 #include <mutex>
