@@ -209,3 +209,24 @@ def test_backward_zero_tokens():
     torch.cuda.synchronize()
     for t in (dwg, dbias, dw13, dw2):
         assert int(torch.count_nonzero(t)) == 0
+
+
+def test_backward_single_renormalised_slot_router_gradient_is_zero():
+    """K = 1 with renormalisation: the weight is 1 for every logit vector, so
+    dW_gate and dbias are exactly zero (dp = (dw - dw * 1) / p = 0 in float32
+    too); the expert gradients still match the oracle."""
+    cfg = MoEConfig("bwd_k1_norm", n=256, H=256, I=128, E=8, K=1, dtype="bf16",
+                    norm_topk_prob=True, seed=48)
+    r = _run(cfg)
+    assert r["status"] == 0
+    assert int(torch.count_nonzero(r["dwg"])) == 0
+    assert int(torch.count_nonzero(r["dbias"])) == 0
+    L = r["L"]
+    x64, wg64, b64 = f64(r["x"]), f64(L["w_gate"]), f64(L["bias"])
+    near = O.near_tie_tokens(O.router_logits(x64, wg64, b64), cfg.K, NEAR_TIE_GAP)
+    forced = (np.where(near)[0], r["idx"].cpu().numpy()[near])
+    o = OB.moe_backward(x64, wg64, b64, lambda e: L["w13"][e].to(torch.float64).cpu().numpy(),
+                        lambda e: L["w2"][e].to(torch.float64).cpu().numpy(), 1, True,
+                        f64(r["dy"]), forced=forced)
+    assert rel_fro(f64(r["dw13"]), o["dw13"]) <= TOL
+    assert rel_fro(f64(r["dx"]), o["dx"]) <= TOL

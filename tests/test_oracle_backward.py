@@ -83,6 +83,16 @@ def test_one_expert_router_gets_no_gradient():
     assert np.allclose(g["dx"], g["dx_experts"])
 
 
+def test_single_renormalised_slot_gives_no_router_gradient():
+    """K = 1 with renormalisation: the weight w = p_e / p_e is 1 whatever the
+    logits, so the router gets no gradient although E > 1."""
+    x, w_gate, b, w13, w2, dy = _problem(8, E=4, K=1)
+    g = _B.moe_backward(x, w_gate, b, w13, w2, 1, True, dy)
+    assert np.max(np.abs(g["dlogits"])) == 0.0
+    assert np.max(np.abs(g["dw_gate"])) == 0.0 and np.max(np.abs(g["dbias"])) == 0.0
+    assert np.max(np.abs(g["dw"])) > 0.0  # the slot weight's own gradient is not zero
+
+
 def test_pairs_of_one_token_sum_in_dx():
     """The permute backward adds the K slot rows of a token: with K copies of
     the same expert impossible, check dx_experts against a per-pair sum."""
