@@ -165,58 +165,67 @@ __global__ void __launch_bounds__(BT) router_bwd_kernel(const float *__restrict_
 
 // Partial dW_gate over one token range: part[z][h][e] = sum over t in
 // [z*tc, min(n, (z+1)*tc)) of x[t][h] dlogits[t][e], ascending t, float32.
-// A block computes 64 h x 64 e (each thread 4 x 4); the tokens pass through
-// shared memory 32 at a time (x rows as 128-byte bf16 pieces, dlogits rows
-// coalesced over e).
-constexpr int GW_T = 32;
+// A block computes 128 h x 64 e (each thread 8 h x 4 e: three 16-byte
+// shared-memory loads per 32 FMAs); the tokens pass through shared memory 32
+// at a time (x rows as 16-byte bf16 pieces, dlogits rows coalesced over e),
+// the next chunk's global loads in flight while the current one is used.
+constexpr int GW_T = 32, GW_H = 128, GW_E = 64;
 __global__ void __launch_bounds__(BT) dw_gate_kernel(const __nv_bfloat16 *__restrict__ x,
                                                      const float *__restrict__ dl,
                                                      float *__restrict__ part, int n, int H,
                                                      int E, int tc) {
   pdl_enter();
-  __shared__ __align__(16) float xs[GW_T][64];
-  __shared__ __align__(16) float ds[GW_T][64];
-  const int h0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
+  __shared__ __align__(16) float xs[GW_T][GW_H];
+  __shared__ __align__(16) float ds[GW_T][GW_E];
+  const int h0 = blockIdx.x * GW_H, e0 = blockIdx.y * GW_E;
   const int t0 = blockIdx.z * tc, t1 = min(n, t0 + tc);
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  float acc[4][4] = {};
-  // this thread's share of a chunk (32 tokens x 64 h of x: one 16-byte piece;
-  // 32 tokens x 64 e of dlogits: 8 values), loaded one chunk ahead
-  const int xr = tid >> 3, xc = tid & 7;
-  uint4 xv_next = make_uint4(0u, 0u, 0u, 0u);
-  float dv_next[GW_T * 64 / BT];
+  float acc[8][4] = {};
+  // this thread's share of a chunk: 2 of the 512 16-byte pieces of x (32
+  // tokens x 128 h) and 8 of the 2048 dlogits values (32 tokens x 64 e)
+  constexpr int XP = GW_T * GW_H / 8 / BT, DP = GW_T * GW_E / BT;
+  uint4 xv_next[XP];
+  float dv_next[DP];
   auto fetch = [&](int tb) {
-    xv_next = tb + xr < t1
-                  ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(tb + xr) * H + h0 + xc * 8))
-                  : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int q = 0; q < GW_T * 64 / BT; ++q) {
+    for (int q = 0; q < XP; ++q) {
+      const int i = tid + q * BT, r = i >> 4, c = i & 15;
+      xv_next[q] = tb + r < t1 ? __ldg(reinterpret_cast<const uint4 *>(
+                                     x + (size_t)(tb + r) * H + h0 + c * 8))
+                               : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int q = 0; q < DP; ++q) {
       const int i = tid + q * BT, r = i >> 6, c = i & 63;
       dv_next[q] = (tb + r < t1 && e0 + c < E) ? __ldg(dl + (size_t)(tb + r) * E + e0 + c) : 0.f;
     }
   };
   if (t0 < t1) fetch(t0);
   for (int tb = t0; tb < t1; tb += GW_T) {
-    {
-      float f[8];
-      bf16x8_to_f32(xv_next, f);
-      *reinterpret_cast<float4 *>(&xs[xr][xc * 8]) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4 *>(&xs[xr][xc * 8 + 4]) = make_float4(f[4], f[5], f[6], f[7]);
 #pragma unroll
-      for (int q = 0; q < GW_T * 64 / BT; ++q) {
-        const int i = tid + q * BT;
-        ds[i >> 6][i & 63] = dv_next[q];
-      }
+    for (int q = 0; q < XP; ++q) {
+      const int i = tid + q * BT, r = i >> 4, c = i & 15;
+      float f[8];
+      bf16x8_to_f32(xv_next[q], f);
+      *reinterpret_cast<float4 *>(&xs[r][c * 8]) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4 *>(&xs[r][c * 8 + 4]) = make_float4(f[4], f[5], f[6], f[7]);
+    }
+#pragma unroll
+    for (int q = 0; q < DP; ++q) {
+      const int i = tid + q * BT;
+      ds[i >> 6][i & 63] = dv_next[q];
     }
     __syncthreads();
     if (tb + GW_T < t1) fetch(tb + GW_T);  // in flight while this chunk is used
-#pragma unroll 8
+#pragma unroll 4
     for (int tt = 0; tt < GW_T; ++tt) {
-      const float4 xv = *reinterpret_cast<const float4 *>(&xs[tt][ty * 4]);
+      const float4 x0 = *reinterpret_cast<const float4 *>(&xs[tt][ty * 8]);
+      const float4 x1 = *reinterpret_cast<const float4 *>(&xs[tt][ty * 8 + 4]);
       const float4 dv = *reinterpret_cast<const float4 *>(&ds[tt][tx * 4]);
-      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+      const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const float da[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], da[j], acc[i][j]);
     }
@@ -224,11 +233,11 @@ __global__ void __launch_bounds__(BT) dw_gate_kernel(const __nv_bfloat16 *__rest
   }
   float *out = part + (size_t)blockIdx.z * H * E;
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = e0 + tx * 4 + j;
-      if (e < E) out[(size_t)(h0 + ty * 4 + i) * E + e] = acc[i][j];
+      if (e < E) out[(size_t)(h0 + ty * 8 + i) * E + e] = acc[i][j];
     }
 }
 
@@ -431,7 +440,7 @@ cudaError_t launch_router_bwd(const Desc &d, const void *x, const float *logits,
   // dW_gate[h][e] = sum_t x[t][h] dlogits[t][e]: the tokens split into
   // RB_SPLIT ranges (partials in dw_part), then added in order
   const int kc = (d.n + RB_SPLIT - 1) / RB_SPLIT;
-  e = launch_pdl(dw_gate_kernel, dim3(d.H / 64, (d.E + 63) / 64, RB_SPLIT), dim3(BT), 0, s,
+  e = launch_pdl(dw_gate_kernel, dim3(d.H / GW_H, (d.E + GW_E - 1) / GW_E, RB_SPLIT), dim3(BT), 0, s,
                  reinterpret_cast<const __nv_bfloat16 *>(x), (const float *)dlogits, dw_part, d.n,
                  d.H, d.E, kc);
   if (e != cudaSuccess) return e;
