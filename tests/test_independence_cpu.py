@@ -52,3 +52,16 @@ def test_cuda_sources_include_nothing_from_the_oracle():
             for line in open(os.path.join(csrc, f)):
                 if line.lstrip().startswith("#include"):
                     assert "oracle" not in line, (f, line)
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """No CPU fallback: without the built library every entry point raises."""
+    import pytest
+    from top_routing_dispatch_gb300 import _lib, api
+    monkeypatch.setattr(_lib, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libmoe_gb300.so"))
+    monkeypatch.setattr(_lib, "_LIB", None)
+    with pytest.raises(ImportError):
+        _lib.load()
+    desc = _lib.LayerDesc(n=8, H=256, I=128, E=8, K=2, dtype=1, norm_topk_prob=0)
+    with pytest.raises(ImportError):
+        api.moe_backward_workspace_size(desc)
