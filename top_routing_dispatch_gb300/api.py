@@ -241,12 +241,17 @@ class MoELayer:
 
 
 def moe_backward_workspace_size(desc) -> int:
+    """Bytes of device scratch moe_backward needs for this layer shape."""
     return int(_lib.load().moe_backward_workspace_size(ctypes.byref(desc)))
 
 
 def moe_backward(desc, x, w_gate, w13, w2, dy, logits, topk_idx, topk_w, offsets, inv_perm,
                  x_perm, h, y_perm, dx, dw_gate, dbias, dw13, dw2, ws, status_word=None,
                  stream=None):
+    """Gradients of the layer for dy (bf16 layers): dx (n,H) bf16 and the
+    float32 dw_gate (H,E), dbias (E, or None), dw13 (E,H,2I), dw2 (E,I,H),
+    from the forward's own intermediates (logits, topk_idx, topk_w, offsets,
+    inv_perm, x_perm, h and the unweighted y_perm of moe_expert_gemm2)."""
     nbytes = ws.numel() * ws.element_size()
     _check(_lib.load().moe_backward(
         ctypes.byref(desc), _p(x), _p(w_gate), _p(w13), _p(w2), _p(dy), _p(logits), _p(topk_idx),
