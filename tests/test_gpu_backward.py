@@ -27,6 +27,9 @@ CASES = [
               seed=45),
     MoEConfig("bwd_e20", n=300, H=512, I=384, E=20, K=3, dtype="bf16", norm_topk_prob=False,
               seed=46),
+    # E = 128: two 64-expert tiles in dW_gate and the router's tensor-core path
+    MoEConfig("bwd_e128", n=400, H=256, I=128, E=128, K=4, dtype="bf16", norm_topk_prob=True,
+              seed=49),
 ]
 TOL = 2e-2
 
