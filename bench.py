@@ -357,11 +357,21 @@ def run_ours(args, cfg):
         ("permute", lambda: M.moe_permute(desc, x, v["perm"], v["x_perm"], st, stream)),
         ("gemm1", lambda: M.moe_expert_gemm1_swiglu(desc, v["x_perm"], L["w13"], v["offsets"],
                                                     v["h"], 0, st, stream)),
-        ("gemm2", lambda: M.moe_expert_gemm2_weighted(desc, v["h"], L["w2"], v["offsets"],
-                                                      v["perm"], v["topk_w"], v["y_perm"], 0, st,
-                                                      stream)),
-        ("combine", lambda: M.moe_combine_slots(desc, v["y_perm"], y, stream)),
     ]
+    if cfg.dtype == "bf16":  # the rows the layer runs: weighting in GEMM2, slot-sum combine
+        phases += [
+            ("gemm2", lambda: M.moe_expert_gemm2_weighted(desc, v["h"], L["w2"], v["offsets"],
+                                                          v["perm"], v["topk_w"], v["y_perm"], 0,
+                                                          st, stream)),
+            ("combine", lambda: M.moe_combine_slots(desc, v["y_perm"], y, stream)),
+        ]
+    else:  # float32 layers: expert-ordered GEMM2, then the weighting gather-combine
+        phases += [
+            ("gemm2", lambda: M.moe_expert_gemm2(desc, v["h"], L["w2"], v["offsets"], v["y_perm"],
+                                                 0, st, stream)),
+            ("combine", lambda: M.moe_combine(desc, v["y_perm"], v["topk_w"], v["inv_perm"], y,
+                                              st, stream)),
+        ]
     T = Timer(torch, stream, dev)
 
     def phased_step(flush=True):
@@ -442,11 +452,12 @@ def run_ours(args, cfg):
 
     # an entry point the step does not call, timed alone on the same layout:
     # GEMM1 with the permute fused into its A loads (x_perm never written)
-    h_alt = torch.empty_like(v["h"])
-    fused = lambda: M.moe_expert_gemm1_swiglu_gather(desc, x, v["perm"], L["w13"], v["offsets"],
-                                                     h_alt, 0, st, stream)
-    T.measure(fused, 3)
-    per_phase["gemm1_gather"] = T.measure(fused, max(5, args.steps // 2))
+    if cfg.dtype == "bf16":  # the fused-gather GEMM1 exists for bf16 layers
+        h_alt = torch.empty_like(v["h"])
+        fused = lambda: M.moe_expert_gemm1_swiglu_gather(desc, x, v["perm"], L["w13"],
+                                                         v["offsets"], h_alt, 0, st, stream)
+        T.measure(fused, 3)
+        per_phase["gemm1_gather"] = T.measure(fused, max(5, args.steps // 2))
 
     counts = v["counts"].cpu().tolist()
     alg = algorithmic(cfg, counts)
@@ -534,7 +545,8 @@ def run_ours(args, cfg):
 def backward(args, torch, M, synth, cfg, dev, peaks, layer, L, x, v, st, stream, T):
     """moe_backward on the same layer: one C-ABI call per step (combine
     backward, two dgrad GEMMs, the SwiGLU-backward GEMM, two weight-gradient
-    GEMMs, router backward, dx gather), L2 flushed before each step."""
+    GEMMs, router backward, dx = the router term fused with the permute
+    backward), L2 flushed before each step."""
     n, H, I, E, K = cfg.n, cfg.H, cfg.I, cfg.E, cfg.K
     nK = n * K
     f32, bf = torch.float32, torch.bfloat16
