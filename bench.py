@@ -35,11 +35,6 @@ METRIC = "MoE-layer tokens/s and grouped-GEMM TFLOP/s (% BF16 peak), permute/com
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20          # > 129 MB L2
-# kernels of the library launched by one layer step (single stream, bf16 with
-# E % 64 == 0): router 2 (tensor-core logits + TopK, exact rescoring of the
-# flagged near ties) + layout 2 (count, scan + scatter) + permute 1 + GEMM1 1
-# + GEMM2 1 + combine 1
-KERNELS_PER_STEP = 8
 
 
 def parse_args():
@@ -56,6 +51,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-domino", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--extra-workloads", default="olmoe_skew_bf16,dsv3_bf16,tiny_fp32",
+                    help="other single-batch workloads timed after the headline (N=1 only); "
+                         "empty to skip")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -325,6 +323,157 @@ class Timer:
         return ts
 
 
+def kernel_rows(M, desc, cfg, x, y, L, v, st, lws, stream):
+    """The step as one C-ABI call per row of the layer (the rows the forward
+    runs for this dtype)."""
+    rows = [
+        ("router", lambda: M.moe_route_topk(desc, x, L["w_gate"], L["bias"], v["topk_idx"],
+                                            v["topk_w"], v["logits"], stream)),
+        ("layout", lambda: M.moe_dispatch_layout(desc, v["topk_idx"], v["counts"], v["offsets"],
+                                                 v["perm"], v["inv_perm"], st, lws, stream)),
+        ("permute", lambda: M.moe_permute(desc, x, v["perm"], v["x_perm"], st, stream)),
+        ("gemm1", lambda: M.moe_expert_gemm1_swiglu(desc, v["x_perm"], L["w13"], v["offsets"],
+                                                    v["h"], 0, st, stream)),
+    ]
+    if cfg.dtype == "bf16":  # the rows the layer runs: weighting in GEMM2, slot-sum combine
+        rows += [
+            ("gemm2", lambda: M.moe_expert_gemm2_weighted(desc, v["h"], L["w2"], v["offsets"],
+                                                          v["perm"], v["topk_w"], v["y_perm"], 0,
+                                                          st, stream)),
+            ("combine", lambda: M.moe_combine_slots(desc, v["y_perm"], y, stream)),
+        ]
+    else:  # float32 layers: expert-ordered GEMM2, then the weighting gather-combine
+        rows += [
+            ("gemm2", lambda: M.moe_expert_gemm2(desc, v["h"], L["w2"], v["offsets"], v["y_perm"],
+                                                 0, st, stream)),
+            ("combine", lambda: M.moe_combine(desc, v["y_perm"], v["topk_w"], v["inv_perm"], y,
+                                              st, stream)),
+        ]
+    return rows
+
+
+def kernel_table(cfg, per_phase, per_phase_warm, counts, peaks, rows):
+    """Per-kernel time, throughput and fraction of its own roofline."""
+    alg = algorithmic(cfg, counts)
+    kernels = {}
+    for name, ts in per_phase.items():
+        ms = statistics.mean(ts)
+        a = alg[name]
+        k = {"ms": ms, "gbs": a["bytes"] / (ms * 1e-3) / 1e9,
+             "in_step": any(name == p for p, _ in rows)}
+        k["frac_hbm"] = k["gbs"] / peaks["hbm_gbs"]
+        if a["flop"]:
+            k["tflops"] = a["flop"] / (ms * 1e-3) / 1e12
+        if name.startswith("gemm"):
+            k["frac_bf16"] = k["tflops"] / peaks["bf16_tflops"]
+        # the kernel's own roofline: the larger of its tensor time (bf16 GEMMs
+        # and the bf16 router) and its HBM time, over the measured time
+        on_tc = cfg.dtype == "bf16" and (name.startswith("gemm") or name == "router")
+        t_tensor = a["flop"] / (peaks["bf16_tflops"] * 1e12) if on_tc else 0.0
+        t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        k["roofline_bound"] = "tensor" if t_tensor >= t_hbm else "hbm"
+        k["frac_roofline"] = max(t_tensor, t_hbm) / (ms * 1e-3)
+        if name in per_phase_warm:
+            k["ms_warm"] = statistics.mean(per_phase_warm[name])
+        kernels[name] = k
+    return kernels
+
+
+def compact_kernels(kernels):
+    """Per kernel: ms, the fraction of its roofline and the bound, plus the
+    fraction of the bf16 peak (GEMMs) or of the HBM peak (everything else)."""
+    out = {}
+    for name, k in kernels.items():
+        c = {"ms": round(k["ms"], 5), "bound": k["roofline_bound"],
+             "frac_roofline": round(k["frac_roofline"], 4),
+             "frac_hbm": round(k["frac_hbm"], 4)}
+        if "frac_bf16" in k:
+            c["frac_bf16"] = round(k["frac_bf16"], 4)
+        out[name] = c
+    return out
+
+
+def measure_layer(args, torch, M, synth, cfg, dev, peaks, rank, steps, warmup, dist=None):
+    """Times one workload's layer: `steps` forward steps (one
+    moe_forward_microbatches call each, L2 flushed before each), then the same
+    step as one C-ABI call per row (flushed and warm).  Returns the context the
+    headline's extra measurements reuse."""
+    L = synth.make_layer(cfg, dev)
+    x = synth.make_x(cfg, dev, seed=rank_seed(cfg, rank))
+    desc = M.desc_for(cfg)
+    layer = M.MoELayer(desc, L["w_gate"], L["bias"], L["w13"], L["w2"])
+    v = {k: layer.view(k) for k in ("logits", "topk_idx", "topk_w", "counts", "offsets", "perm",
+                                    "inv_perm", "x_perm", "h", "y_perm")}
+    lws = torch.empty(max(M.moe_layout_workspace_size(desc), 1), dtype=torch.uint8, device=dev)
+    st = layer.status
+    y = torch.empty_like(x)
+    stream = torch.cuda.Stream(device=dev)
+    rows = kernel_rows(M, desc, cfg, x, y, L, v, st, lws, stream)
+    T = Timer(torch, stream, dev)
+
+    def phased_step(flush=True):
+        T.prep(flush)
+        evs = [T.event()]
+        for _, fn in rows:
+            fn()
+            evs.append(T.event())
+        return evs
+
+    def forward_step():  # the step as a user runs it: one C-ABI call
+        layer.forward([x], [y], compute=stream)
+
+    for _ in range(warmup):
+        phased_step()
+        T.measure(forward_step, 1)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    fwd_ms = T.measure(forward_step, steps)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    evs = [phased_step() for _ in range(steps)]
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    per_phase = {name: [s[i].elapsed_time(s[i + 1]) for s in evs]
+                 for i, (name, _) in enumerate(rows)}
+    warm = [phased_step(flush=False) for _ in range(steps)]
+    torch.cuda.synchronize()
+    per_phase_warm = {name: [s[i].elapsed_time(s[i + 1]) for s in warm]
+                      for i, (name, _) in enumerate(rows)}
+    phased_ms = [s[0].elapsed_time(s[-1]) for s in evs]
+    status = M.moe_check_status(st, stream)
+    return dict(L=L, x=x, y=y, desc=desc, layer=layer, v=v, st=st, stream=stream, T=T,
+                rows=rows, fwd_ms=fwd_ms, per_phase=per_phase, per_phase_warm=per_phase_warm,
+                phased_ms=phased_ms, clocks=clk, status=status)
+
+
+def extra_workloads(args, torch, M, synth, dev, peaks, rank):
+    """The other single-batch workloads, each in a short timed block: tokens/s,
+    ms per step and every kernel's fraction of its roofline."""
+    from workloads import BY_NAME
+    out = {}
+    for name in args.extra_workloads.split(","):
+        name = name.strip()
+        if not name or name == args.workload:
+            continue
+        cfg = BY_NAME[name]
+        r = measure_layer(args, torch, M, synth, cfg, dev, peaks, rank,
+                          steps=max(3, min(args.steps, 10)), warmup=3)
+        counts = r["v"]["counts"].cpu().tolist()
+        kern = kernel_table(cfg, r["per_phase"], r["per_phase_warm"], counts, peaks, r["rows"])
+        ms = statistics.mean(r["fwd_ms"])
+        out[name] = {"tokens_per_s": round(cfg.n / (ms * 1e-3), 1), "ms_per_step": round(ms, 5),
+                     "steps": len(r["fwd_ms"]), "device_status": r["status"],
+                     "clocks": r["clocks"], "kernels": compact_kernels(kern)}
+        del r
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, cfg):
     import torch
     import top_routing_dispatch_gb300 as M
@@ -339,83 +488,15 @@ def run_ours(args, cfg):
         dist.init_process_group("nccl")
     peaks, peak_src = load_peaks()
 
-    L = synth.make_layer(cfg, dev)
-    x = synth.make_x(cfg, dev, seed=rank_seed(cfg, rank))
-    desc = M.desc_for(cfg)
-    layer = M.MoELayer(desc, L["w_gate"], L["bias"], L["w13"], L["w2"])
-    v = {k: layer.view(k) for k in ("logits", "topk_idx", "topk_w", "counts", "offsets", "perm",
-                                    "inv_perm", "x_perm", "h", "y_perm")}
-    lws = torch.empty(max(M.moe_layout_workspace_size(desc), 1), dtype=torch.uint8, device=dev)
-    st = layer.status
-    y = torch.empty_like(x)
-    stream = torch.cuda.Stream(device=dev)
-    phases = [
-        ("router", lambda: M.moe_route_topk(desc, x, L["w_gate"], L["bias"], v["topk_idx"],
-                                            v["topk_w"], v["logits"], stream)),
-        ("layout", lambda: M.moe_dispatch_layout(desc, v["topk_idx"], v["counts"], v["offsets"],
-                                                 v["perm"], v["inv_perm"], st, lws, stream)),
-        ("permute", lambda: M.moe_permute(desc, x, v["perm"], v["x_perm"], st, stream)),
-        ("gemm1", lambda: M.moe_expert_gemm1_swiglu(desc, v["x_perm"], L["w13"], v["offsets"],
-                                                    v["h"], 0, st, stream)),
-    ]
-    if cfg.dtype == "bf16":  # the rows the layer runs: weighting in GEMM2, slot-sum combine
-        phases += [
-            ("gemm2", lambda: M.moe_expert_gemm2_weighted(desc, v["h"], L["w2"], v["offsets"],
-                                                          v["perm"], v["topk_w"], v["y_perm"], 0,
-                                                          st, stream)),
-            ("combine", lambda: M.moe_combine_slots(desc, v["y_perm"], y, stream)),
-        ]
-    else:  # float32 layers: expert-ordered GEMM2, then the weighting gather-combine
-        phases += [
-            ("gemm2", lambda: M.moe_expert_gemm2(desc, v["h"], L["w2"], v["offsets"], v["y_perm"],
-                                                 0, st, stream)),
-            ("combine", lambda: M.moe_combine(desc, v["y_perm"], v["topk_w"], v["inv_perm"], y,
-                                              st, stream)),
-        ]
-    T = Timer(torch, stream, dev)
-
-    def phased_step(flush=True):
-        T.prep(flush)
-        evs = [T.event()]
-        for _, fn in phases:
-            fn()
-            evs.append(T.event())
-        return evs
-
-    def forward_step():  # the step as a user runs it: one C-ABI call
-        layer.forward([x], [y], compute=stream)
-
-    for _ in range(args.warmup):
-        phased_step()
-        T.measure(forward_step, 1)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
     # timed: K steps, each one moe_forward_microbatches call (L2 flushed and
-    # the whole call enqueued before each step's events)
-    fwd_ms = T.measure(forward_step, args.steps)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    # the per-kernel breakdown: the same step as one C-ABI call per row, with
-    # an event between calls
-    steps = [phased_step() for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    per_phase = {name: [s[i].elapsed_time(s[i + 1]) for s in steps]
-                 for i, (name, _) in enumerate(phases)}
-    # the same without the L2 flush (each row finds its predecessor's output
-    # and, across steps, whatever of the weights L2 still holds)
-    warm_steps = [phased_step(flush=False) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    per_phase_warm = {name: [s[i].elapsed_time(s[i + 1]) for s in warm_steps]
-                      for i, (name, _) in enumerate(phases)}
-    phased_ms = [s[0].elapsed_time(s[-1]) for s in steps]
-    total_ms = max_over_ranks(sum(fwd_ms), dist, dev)
-    status = M.moe_check_status(st, stream)
+    # the whole call enqueued before each step's events); then the per-kernel
+    # breakdown as one C-ABI call per row with an event between calls
+    r = measure_layer(args, torch, M, synth, cfg, dev, peaks, rank, args.steps, args.warmup,
+                      dist)
+    L, x, y, desc, layer, v, st, stream, T = (r[k] for k in ("L", "x", "y", "desc", "layer", "v",
+                                                              "st", "stream", "T"))
+    total_ms = max_over_ranks(sum(r["fwd_ms"]), dist, dev)
+    per_phase, per_phase_warm, rows = r["per_phase"], r["per_phase_warm"], r["rows"]
 
     # end to end through the public C-ABI call on pinned host buffers
     # (moe_forward_host): each step copies x in, runs the layer and copies y
@@ -461,27 +542,7 @@ def run_ours(args, cfg):
 
     counts = v["counts"].cpu().tolist()
     alg = algorithmic(cfg, counts)
-    kernels = {}
-    for name, ts in per_phase.items():
-        ms = statistics.mean(ts)
-        a = alg[name]
-        k = {"ms": ms, "gbs": a["bytes"] / (ms * 1e-3) / 1e9,
-             "in_step": any(name == p for p, _ in phases)}
-        k["frac_hbm"] = k["gbs"] / peaks["hbm_gbs"]
-        if a["flop"]:
-            k["tflops"] = a["flop"] / (ms * 1e-3) / 1e12
-        if name.startswith("gemm"):
-            k["frac_bf16"] = k["tflops"] / peaks["bf16_tflops"]
-        # the kernel's own roofline: the larger of its tensor time (GEMMs and
-        # the tensor-core router) and its HBM time, over the measured time
-        on_tc = cfg.dtype == "bf16" and (name.startswith("gemm") or name == "router")
-        t_tensor = a["flop"] / (peaks["bf16_tflops"] * 1e12) if on_tc else 0.0
-        t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
-        k["roofline_bound"] = "tensor" if t_tensor >= t_hbm else "hbm"
-        k["frac_roofline"] = max(t_tensor, t_hbm) / (ms * 1e-3)
-        if name in per_phase_warm:
-            k["ms_warm"] = statistics.mean(per_phase_warm[name])
-        kernels[name] = k
+    kernels = kernel_table(cfg, per_phase, per_phase_warm, counts, peaks, rows)
     g1 = kernels["gemm1"]
     if g1["roofline_bound"] == "tensor":
         roofline = {"bound": "tensor", "achieved": g1["tflops"], "peak": peaks["bf16_tflops"],
@@ -498,7 +559,9 @@ def run_ours(args, cfg):
         "traffic": (recorded_traffic("gemm1_olmoe_bf16.md", GEMM_SOURCES)
                     if cfg.name == "olmoe_bf16" else None),
         "algorithmic_flop_per_launch": alg["gemm1"]["flop"],
-        "algorithmic_bytes_per_launch": alg["gemm1"]["bytes"]})
+        "algorithmic_bytes_per_launch": alg["gemm1"]["bytes"],
+        # every kernel of this workload's step (and the fused-gather GEMM1)
+        "kernels": compact_kernels(kernels)})
 
     out = {
         "metric": METRIC, "value": aggregate_tokens_per_s(cfg.n, args.steps, world, total_ms),
@@ -513,28 +576,37 @@ def run_ours(args, cfg):
                                        "kernels: the same rows as separate C-ABI calls"),
         "roofline": roofline,
         "kernels": kernels,
-        "phased_ms_per_step": statistics.mean(phased_ms),
+        "phased_ms_per_step": statistics.mean(r["phased_ms"]),
         "e2e": {"value": aggregate_tokens_per_s(cfg.n, args.steps, world, e2e_total), "unit": UNIT,
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
                 "d2h_bytes_per_step": y_h.numel() * y_h.element_size(),
                 "api": "moe_forward_host (pinned host x/y; copies overlap neighbouring steps)",
-                "l2": "not flushed: each step streams 805 MB of expert weights (> 129 MB L2)",
+                "l2": "not flushed: each step streams the expert weights (> 129 MB L2)",
                 "ms_per_step": e2e_total / args.steps},
         "e2e_serial": {"value": aggregate_tokens_per_s(cfg.n, args.steps, world, e2e_serial_total),
                        "unit": UNIT, "ms_per_step": e2e_serial_total / args.steps,
                        "note": "copy in, layer, copy out in order on one stream"},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
-        "clocks": clk,
-        "device_status": status,
+        "gpu_launches": M.kernels_per_forward(desc) * args.steps,
+        "clocks": r["clocks"],
+        "device_status": r["status"],
         "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,
     }
     if not args.no_domino:
-        out["domino"] = domino(args, torch, M, synth, DOMINO, dev, peaks)
+        dom = domino(args, torch, M, synth, DOMINO, dev, peaks)
+        out["domino"] = dom
+        roofline["overlap"] = {k: dom[k] for k in (
+            "hide_ratio_eligible", "hide_ratio_strict", "hide_ratio_eligible_runs",
+            "ms_compute_only_A", "ms_dispatch_combine_only_B", "ms_serial_C", "ms_overlapped_D",
+            "ms_edge_phases", "ms_eligible_phases", "bitwise_equal_to_single_stream")}
     if not args.no_backward and cfg.dtype == "bf16":
         out["backward"] = backward(args, torch, M, synth, cfg, dev, peaks, layer, L, x, v, st,
                                    stream, T)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg, L, x, args.cpu_sample, args.cpu_seconds)
+    if args.extra_workloads and world == 1:
+        del r, L, x, y, layer, v
+        torch.cuda.empty_cache()
+        roofline["workloads"] = extra_workloads(args, torch, M, synth, dev, peaks, rank)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist:
@@ -618,29 +690,42 @@ def domino(args, torch, M, synth, cfg, dev, peaks):
     layer.forward(xs, ys, compute=sc)
     torch.cuda.synchronize()
     ref = [y.clone() for y in ys]
-    t_a = med(lambda: (gemms(0), gemms(1)))
-    t_b = med(lambda: (front(0), front(1), back(0), back(1)))
-    t_edge = med(lambda: (front(0), back(1)))
-    t_elig = med(lambda: (front(1), back(0)))
-    t_c = med(lambda: layer.forward(xs, ys, compute=sc))
-    sweep = {}
-    for s in (0, 8, 16, 24, 32):
-        sweep[s] = med(lambda: layer.forward(xs, ys, sm_reserve=s, compute=sc, dispatch=sd))
-    best = min(sweep, key=sweep.get)
-    t_d = sweep[best]
+    # the four controls and the two phase groups, measured in REPS interleaved
+    # rounds; the hide ratios are taken per round and their median reported
+    REPS = 5
+    runs = []
+    sweep = {s: [] for s in (0, 8, 16, 24, 32)}
+    for _ in range(REPS):
+        t_a = med(lambda: (gemms(0), gemms(1)))
+        t_b = med(lambda: (front(0), front(1), back(0), back(1)))
+        t_edge = med(lambda: (front(0), back(1)))
+        t_elig = med(lambda: (front(1), back(0)))
+        t_c = med(lambda: layer.forward(xs, ys, compute=sc))
+        for s in sweep:
+            sweep[s].append(med(lambda: layer.forward(xs, ys, sm_reserve=s, compute=sc,
+                                                      dispatch=sd)))
+        t_d = sweep[0][-1]
+        runs.append(dict(A=t_a, B=t_b, C=t_c, D=t_d, edge=t_edge, elig=t_elig,
+                         strict=1.0 - (t_d - t_a) / t_b,
+                         elig_hide=1.0 - (t_d - t_a - t_edge) / t_elig))
+    sweep_med = {s: statistics.median(ts) for s, ts in sweep.items()}
+    best = min(sweep_med, key=sweep_med.get)
     layer.forward(xs, ys, sm_reserve=best, compute=sc, dispatch=sd)
     torch.cuda.synchronize()
     bitwise = all(torch.equal(a, b) for a, b in zip(ys, ref))
+    mk = lambda key: statistics.median(r[key] for r in runs)
     return {
         "workload": f"{cfg.name}: 2 x n={cfg.n}, seeds {list(cfg.mb_seeds)}",
-        "ms_compute_only_A": t_a, "ms_dispatch_combine_only_B": t_b,
-        "ms_serial_C": t_c, "ms_overlapped_D": t_d, "sm_reserve_best": best,
-        "ms_overlapped_by_sm_reserve": sweep,
-        "ms_edge_phases": t_edge, "ms_eligible_phases": t_elig,
-        "hide_ratio_strict": 1.0 - (t_d - t_a) / t_b,
-        "hide_ratio_eligible": 1.0 - (t_d - t_a - t_edge) / t_elig,
-        "speedup_D_vs_C": t_c / t_d,
-        "tokens_per_s_overlapped": 2 * cfg.n / (t_d * 1e-3),
+        "rounds": REPS, "reps_per_control": R,
+        "ms_compute_only_A": mk("A"), "ms_dispatch_combine_only_B": mk("B"),
+        "ms_serial_C": mk("C"), "ms_overlapped_D": mk("D"), "sm_reserve": 0,
+        "ms_overlapped_by_sm_reserve": sweep_med, "sm_reserve_best": best,
+        "ms_edge_phases": mk("edge"), "ms_eligible_phases": mk("elig"),
+        "hide_ratio_strict": mk("strict"),
+        "hide_ratio_eligible": mk("elig_hide"),
+        "hide_ratio_eligible_runs": [round(r["elig_hide"], 4) for r in runs],
+        "speedup_D_vs_C": mk("C") / mk("D"),
+        "tokens_per_s_overlapped": 2 * cfg.n / (mk("D") * 1e-3),
         "bitwise_equal_to_single_stream": bitwise,
     }
 

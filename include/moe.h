@@ -139,9 +139,10 @@ moe_status_t moe_dispatch_layout(const moe_layer_desc_t *desc, const int32_t *to
  *     itself allocates nothing.
  *   - Limit: n*K <= MOE_NOALLOC_MAX_PAIRS (and E <= 256 as everywhere);
  *     larger layouts return MOE_ERR_WORKSPACE before anything is enqueued.
- *   - The first call on a device looks up the array's device address (a
- *     cudaGetSymbolAddress, with that device current); make that first call
- *     before capturing a stream.
+ *   - Every call looks up the array's address on the current device
+ *     (cudaGetSymbolAddress, a host-side lookup), so the address stays valid
+ *     after a cudaDeviceReset.  The first call on a device may load the
+ *     library's device code: make that first call before capturing a stream.
  *   - All calls on a device share the array.  Calls must not overlap on the
  *     GPU: two of them running at once (e.g. on unordered streams) race on the
  *     scratch and give wrong layouts.  Calls ordered on one stream are safe.
@@ -279,6 +280,14 @@ moe_status_t moe_combine_slots(const moe_layer_desc_t *desc, const void *y_slot,
  * another (no result depends on grid size or stream timing).
  */
 size_t moe_workspace_size(const moe_layer_desc_t *desc);
+
+/*
+ * Kernel launches one micro-batch of moe_forward_microbatches enqueues for
+ * this layer (router, dispatch layout, permute, the two expert GEMMs, combine),
+ * for launch accounting; host-side, touches no device.  0 for an invalid
+ * descriptor.
+ */
+int moe_forward_launches(const moe_layer_desc_t *desc);
 moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
                                       const void *const *x, const void *w_gate, const float *bias,
                                       const void *w13, const void *w2, void *const *y, void *ws,
@@ -354,6 +363,9 @@ size_t moe_host_workspace_size(const moe_layer_desc_t *desc);
  * call, or synchronise copy_out).  The host never blocks.  Results are
  * bitwise those of moe_forward_microbatches on the same input.
  *   status_word: as for moe_forward_microbatches (NULL: a word inside ws).
+ * The library keeps six CUDA events per (device, ws) pipeline for at most 64
+ * pipelines; the 65th distinct ws replaces the least recently used one, after
+ * waiting on the host for that pipeline's last enqueued copies and layer.
  */
 moe_status_t moe_forward_host(const moe_layer_desc_t *desc, const void *x_host,
                               const void *w_gate, const float *bias, const void *w13,

@@ -16,7 +16,7 @@ SYMBOLS = (
     "moe_version", "moe_status_string", "moe_route_topk", "moe_layout_workspace_size",
     "moe_dispatch_layout", "moe_dispatch_layout_noalloc", "moe_permute", "moe_grouped_swiglu", "moe_expert_gemm1_swiglu",
     "moe_expert_gemm1_swiglu_gather", "moe_expert_gemm2", "moe_combine",
-    "moe_workspace_size", "moe_forward_microbatches", "moe_workspace_slot", "moe_check_status",
+    "moe_workspace_size", "moe_forward_launches", "moe_forward_microbatches", "moe_workspace_slot", "moe_check_status",
     "moe_host_workspace_size", "moe_forward_host", "moe_expert_gemm2_weighted",
     "moe_combine_slots", "moe_backward_workspace_size", "moe_backward",
 )
@@ -47,6 +47,7 @@ _st = ctypes.c_int
 def _declare(lib):
     sig = {
         "moe_version": (ctypes.c_char_p, []),
+        "moe_forward_launches": (ctypes.c_int, [_desc_p]),
         "moe_status_string": (ctypes.c_char_p, [_st]),
         "moe_route_topk": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
         "moe_layout_workspace_size": (ctypes.c_size_t, [_desc_p]),

@@ -141,6 +141,11 @@ def moe_combine(desc, y_perm, topk_w, inv_perm, y, status_word=None, stream=None
                                    _p(y), _p(status_word), _stream(stream)), "moe_combine")
 
 
+def kernels_per_forward(desc) -> int:
+    """Kernel launches one micro-batch of moe_forward_microbatches enqueues."""
+    return int(_lib.load().moe_forward_launches(ctypes.byref(desc)))
+
+
 def moe_workspace_size(desc) -> int:
     return int(_lib.load().moe_workspace_size(ctypes.byref(desc)))
 

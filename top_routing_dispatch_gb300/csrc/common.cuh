@@ -42,6 +42,8 @@ cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, cons
                           int32_t *topk_idx, float *topk_w, float *logits, int32_t *status,
                           cudaStream_t s);
 bool router_tc_supported(const Desc &d);
+// kernels launch_router enqueues for this layer
+int router_launches(const Desc &d);
 cudaError_t launch_router_tc(const Desc &d, const void *x, const void *w_gate, const float *bias,
                              int32_t *topk_idx, float *topk_w, float *logits, int32_t *status,
                              cudaStream_t s);

@@ -19,9 +19,8 @@
 // (zeroing the rows in place with a fence there cost about 2 us per tile).  A
 // tile of an expert without rows is written as zeros.  float32 output, written
 // by TMA tile stores from swizzled shared-memory staging buffers; one CTA per
-// SM, persistent, double-buffered TMEM accumulators as in gemm_tc.cu; CTA
-// pairs of a cluster compute neighbouring M tiles and share the B operand
-// through TMA multicast (wgrad_tc_kernel<CL> below).
+// SM, persistent, double-buffered TMEM accumulators as in gemm_tc.cu.  Every
+// CTA loads its own A and B boxes with plain (non-multicast) TMA copies.
 #include <cuda.h>
 
 #include <mutex>
@@ -81,15 +80,13 @@ struct WTile {
   int e, m0, n0, r0, rows, nkb;
 };
 
-// Work unit g of a cluster of CL CTAs: expert e, CL consecutive 128-row M
-// tiles (one per CTA: rank), one 256-column N tile.
-template <int CL>
-__device__ __forceinline__ WTile w_decode(const WTail &st, int g, int mt, int nt, int rank) {
+// Work unit g: expert e, one 128-row M tile, one 256-column N tile.
+__device__ __forceinline__ WTile w_decode(const WTail &st, int g, int mt, int nt) {
   WTile w;
-  const int per = (mt / CL) * nt;
+  const int per = mt * nt;
   w.e = g / per;
   const int rem = g - w.e * per;
-  w.m0 = ((rem / nt) * CL + rank) * WM;
+  w.m0 = (rem / nt) * WM;
   w.n0 = (rem % nt) * WN;
   w.r0 = st.off[w.e];
   w.rows = st.off[w.e + 1] - w.r0;
@@ -97,23 +94,8 @@ __device__ __forceinline__ WTile w_decode(const WTail &st, int g, int mt, int nt
   return w;
 }
 
-// One B box: local load (CL == 1) or multicast to every CTA of the cluster.
-template <int CL>
-__device__ __forceinline__ void w_load_b(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
-                                         int c1) {
-  if constexpr (CL == 1)
-    ptx::tma_load_2d(dst, map, bar, c0, c1);
-  else
-    ptx::tma_load_2d_multicast(dst, map, bar, c0, c1, (uint16_t)((1u << CL) - 1));
-}
-
-// CTAs of one cluster compute the tiles of CL consecutive M tiles that share
-// the expert, the N tile and hence every B operand block: each CTA loads its
-// own A boxes and 4/CL of the four B boxes, multicast to all CL CTAs, so the
-// B operand leaves L2 once per cluster.  A stage is refilled only after the
-// MMAs of every CTA of the cluster have read it (each CTA's MMA completion
-// arrives on the stage's empty barrier in all CL CTAs).
-template <int CL>
+// One persistent CTA per SM; work units are dealt round-robin.  A stage is
+// refilled once the MMAs that read it have completed.
 __global__ void __launch_bounds__(W_THREADS, 1)
     wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -124,8 +106,6 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmOut,
                     const int32_t *__restrict__ offsets, int E, int nK, int M, int N,
                     int32_t *status) {
-  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster of 1, 2 or 4 CTAs");
-  constexpr int BQ = 4 / CL;  // B boxes this CTA loads per block
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -136,13 +116,12 @@ __global__ void __launch_bounds__(W_THREADS, 1)
   WTail &st = *reinterpret_cast<WTail *>(smemE + 8 * W_EPI_BYTES);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = M / WM, nt = N / WN;
-  const int rank = CL > 1 ? (int)ptx::cluster_ctarank() : 0;
-  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
+  const int cid = blockIdx.x, ncl = gridDim.x;
 
   if (tid == 0) {
     for (int s = 0; s < WSTAGES; ++s) {
       ptx::mbar_init(&st.full[s], 1);
-      ptx::mbar_init(&st.empty[s], CL);
+      ptx::mbar_init(&st.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&st.tfull[a], 1);
@@ -162,9 +141,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     if (!ok && blockIdx.x == 0) flag_status(status, MOE_DEV_BAD_LAYOUT);
   }
   __syncthreads();
-  if (!st.ok) return;  // the same decision in every CTA of the cluster
-  // work units; the grid holds at most one cluster per unit
-  const int total = E * (mt / CL) * nt;
+  if (!st.ok) return;
+  // work units; the grid holds at most one CTA per unit
+  const int total = E * mt * nt;
 
   if (warp == 1) {
     ptx::tmem_alloc(&st.tmem_base, W_TMEM);
@@ -173,8 +152,6 @@ __global__ void __launch_bounds__(W_THREADS, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  // every CTA's barriers are initialised before any peer copies or arrives
-  if constexpr (CL > 1) ptx::cluster_sync();
   const uint32_t tmem = st.tmem_base;
   volatile int *abort_flag = &st.abort_flag;
 
@@ -190,7 +167,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       uint32_t phase = 0, used = 0, last_par = 0;
       bool stop = false;
       for (int g = cid; g < total && !stop; g += ncl) {
-        const WTile w = w_decode<CL>(st, g, mt, nt, rank);
+        const WTile w = w_decode(st, g, mt, nt);
         for (int kb = 0; kb < w.nkb; ++kb) {
           if (!w_wait(&st.empty[stage], phase ^ 1u, abort_flag, status)) {
             stop = true;
@@ -206,8 +183,8 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             for (int q = 0; q < 2; ++q)
               ptx::tma_load_2d(sa + q * WA_BOX, &tmA, &st.full[stage], w.m0 + q * 64, row);
 #pragma unroll
-            for (int q = rank * BQ; q < (rank + 1) * BQ; ++q)
-              w_load_b<CL>(sb + q * WB_BOX, &tmB, &st.full[stage], w.n0 + q * 64, row);
+            for (int q = 0; q < 4; ++q)
+              ptx::tma_load_2d(sb + q * WB_BOX, &tmB, &st.full[stage], w.n0 + q * 64, row);
           } else {
             // the segment's last rows: whole 16-row groups from the operands,
             // the partial group from the zero-padded tail rows of expert e
@@ -224,9 +201,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                 ptx::tma_load_2d(sa + q * WA_BOX + gr * W_GROUP_BYTES, ma, &st.full[stage],
                                  w.m0 + q * 64, r);
 #pragma unroll
-              for (int q = rank * BQ; q < (rank + 1) * BQ; ++q)
-                w_load_b<CL>(sb + q * WB_BOX + gr * W_GROUP_BYTES, mb, &st.full[stage],
-                             w.n0 + q * 64, r);
+              for (int q = 0; q < 4; ++q)
+                ptx::tma_load_2d(sb + q * WB_BOX + gr * W_GROUP_BYTES, mb, &st.full[stage],
+                                 w.n0 + q * 64, r);
             }
           }
           used |= 1u << stage;
@@ -237,19 +214,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
           }
         }
       }
-      // copies into this CTA's stages (its own and its peers') have landed
+      // never leave a TMA copy in flight: the last load of every stage has landed
       for (int s = 0; s < WSTAGES; ++s)
         if (used >> s & 1u) ptx::mbar_wait(&st.full[s], last_par >> s & 1u);
-      // and every CTA's MMAs have released every stage (their arrivals on
-      // this CTA's barriers are done before it may exit)
-      if (!stop && !*abort_flag)
-        for (int i = 0; i < WSTAGES; ++i) {
-          if (!w_wait(&st.empty[stage], phase ^ 1u, abort_flag, status)) break;
-          if (++stage == WSTAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
     }
   } else if (warp == 1) {
     // one thread issues the MMAs; the rest of the warp waits at the end
@@ -257,7 +224,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       for (int g = cid; g < total; g += ncl) {
-        const WTile w = w_decode<CL>(st, g, mt, nt, rank);
+        const WTile w = w_decode(st, g, mt, nt);
         if (!w_wait(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * WN);
@@ -278,10 +245,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             const uint64_t bdesc = ptx::smem_desc(b0 + kk * W_GROUP_BYTES, WB_BOX, 1024);
             ptx::mma_bf16(d, adesc, bdesc, W_IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
-          if constexpr (CL == 1)
-            ptx::mma_commit(&st.empty[stage]);
-          else
-            ptx::mma_commit_multicast(&st.empty[stage], (uint16_t)((1u << CL) - 1));
+          ptx::mma_commit(&st.empty[stage]);
           if (++stage == WSTAGES) {
             stage = 0;
             phase ^= 1u;
@@ -302,7 +266,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     int acc = 0, nstore = 0;
     uint32_t acc_phase = 0;
     for (int g = cid; g < total; g += ncl) {
-      const WTile w = w_decode<CL>(st, g, mt, nt, rank);
+      const WTile w = w_decode(st, g, mt, nt);
       if (!w_wait(&st.tfull[acc], acc_phase, abort_flag, status)) break;
       ptx::tc_fence_after();
       const uint32_t tb = tmem + (uint32_t)(acc * WN) + ((uint32_t)(q * 32) << 16);
@@ -348,8 +312,6 @@ __global__ void __launch_bounds__(W_THREADS, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  // no CTA leaves while a peer may still copy into it or arrive on it
-  if constexpr (CL > 1) ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     __syncwarp();
@@ -434,11 +396,6 @@ bool w_out_map(CUtensorMap *m, float *base, uint64_t cols, uint64_t rows) {
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// preferred cluster size (CTAs sharing the B operand); smaller when the M
-// tiles do not divide.  Measured at the OLMoE dW13 shape (GB300): 299 us with
-// pairs, 305 us with 4 CTAs, 311 us without clusters.
-constexpr int kWgradCluster = 2;
-
 struct WgradArgs {
   CUtensorMap mA, mB, mA16, mB16, mAt, mBt, mOut;
   const int32_t *offsets;
@@ -446,52 +403,24 @@ struct WgradArgs {
   int32_t *status;
 };
 
-// Persistent launch: as many clusters as fit on the device at once (cached
-// per device), at most one per work unit.
-template <int CL>
+// Persistent launch: one CTA per SM, at most one per work unit.
 cudaError_t wgrad_launch(const WgradArgs &p, cudaStream_t s) {
-  auto kernel = wgrad_tc_kernel<CL>;
-  static int clusters[64] = {0};
+  static int attr_set[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(W_THREADS);
-  cfg.dynamicSmemBytes = W_SMEM;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  int na = 0;
-  if (CL > 1) {
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = CL;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-  }
-  if (!clusters[dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W_SMEM);
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(wgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)W_SMEM);
     if (e != cudaSuccess) return e;
-    int nc = device_sm_count();
-    if (CL > 1) {
-      cfg.gridDim = dim3(CL * 16);
-      cfg.attrs = attr;
-      cfg.numAttrs = na;
-      e = cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg);
-      if (e != cudaSuccess) return e;
-    }
-    if (nc < 1) return cudaErrorInvalidConfiguration;
-    clusters[dev] = nc;
+    attr_set[dev] = 1;
   }
-  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[na].val.programmaticStreamSerializationAllowed = 1;
-  ++na;
-  cfg.attrs = attr;
-  cfg.numAttrs = na;
-  const int units = p.E * (p.M / WM / CL) * (p.N / WN);
-  cfg.gridDim = dim3((unsigned)(CL * (units < clusters[dev] ? units : clusters[dev])));
-  return cudaLaunchKernelEx(&cfg, kernel, p.mA, p.mB, p.mA16, p.mB16, p.mAt, p.mBt, p.mOut,
-                            p.offsets, p.E, p.nK, p.M, p.N, p.status);
+  const int units = p.E * (p.M / WM) * (p.N / WN);
+  const int sms = device_sm_count();
+  return launch_pdl(wgrad_tc_kernel, dim3((unsigned)(units < sms ? units : sms)), dim3(W_THREADS),
+                    W_SMEM, s, p.mA, p.mB, p.mA16, p.mB16, p.mAt, p.mBt, p.mOut, p.offsets, p.E,
+                    p.nK, p.M, p.N, p.status);
 }
 
 size_t wgrad_tail_bytes(const Desc &d, int M, int N) {
@@ -523,12 +452,8 @@ cudaError_t launch_wgrad_tc(const Desc &d, const void *a, int M, const void *b, 
                              (const __nv_bfloat16 *)a, M, (const __nv_bfloat16 *)b, N, offsets,
                              (int)nK, ta, tb);
   if (e != cudaSuccess) return e;
-  const int mt = M / WM;
-  const int cl = mt % kWgradCluster == 0 ? kWgradCluster : (mt % 2 == 0 ? 2 : 1);
   const WgradArgs args{mA, mB, mA16, mB16, mAt, mBt, mOut, offsets, d.E, (int)nK, M, N, status};
-  if (cl == 4) return wgrad_launch<4>(args, s);
-  if (cl == 2) return wgrad_launch<2>(args, s);
-  return wgrad_launch<1>(args, s);
+  return wgrad_launch(args, s);
 }
 
 }  // namespace moe

@@ -112,9 +112,25 @@ std::mutex g_pool_mu;
 // layer finished (x read, y written), y copied out
 struct HostEvents {
   cudaEvent_t in[2], layer[2], out[2];
+  unsigned long long last_use;
 };
+// At most kMaxHostPipelines pipelines keep their events; a new one replaces
+// the least recently used, whose recorded work is waited for first (so its
+// workspace's ordering is never lost while still in flight).
+constexpr size_t kMaxHostPipelines = 64;
 std::map<std::pair<int, const void *>, HostEvents> g_host_events;
+unsigned long long g_host_clock = 0;
 std::mutex g_host_mu;
+
+void destroy_host_events(HostEvents &h) {
+  for (int k = 0; k < 2; ++k) {
+    cudaEvent_t evs[3] = {h.in[k], h.layer[k], h.out[k]};
+    for (cudaEvent_t ev : evs) {
+      cudaEventSynchronize(ev);
+      cudaEventDestroy(ev);
+    }
+  }
+}
 
 }  // namespace
 }  // namespace moe
@@ -297,6 +313,14 @@ size_t moe_workspace_size(const moe_layer_desc_t *desc) {
   return mb_bytes(d);
 }
 
+int moe_forward_launches(const moe_layer_desc_t *desc) {
+  Desc d;
+  if (check_desc(desc, &d) != MOE_OK) return 0;
+  const bool pairs = d.nK() > 0;
+  // router | layout count + scan/scatter | permute | GEMM1, GEMM2 | combine
+  return router_launches(d) + (pairs ? 2 + 1 + 2 : 0) + (d.n > 0 ? 1 : 0);
+}
+
 void *moe_workspace_slot(const moe_layer_desc_t *desc, void *ws, int mb, int which) {
   Desc d;
   if (!ws || mb < 0 || which < 0 || which >= S_LAYOUT_WS) return nullptr;
@@ -472,7 +496,17 @@ moe_status_t moe_forward_host(const moe_layer_desc_t *desc, const void *x_host,
   std::lock_guard<std::mutex> lock(g_host_mu);
   auto it = g_host_events.find({dev, ws});
   if (it == g_host_events.end()) {
-    HostEvents h;
+    if (g_host_events.size() >= kMaxHostPipelines) {
+      auto lru = g_host_events.begin();
+      for (auto j = g_host_events.begin(); j != g_host_events.end(); ++j)
+        if (j->second.last_use < lru->second.last_use) lru = j;
+      int cur = dev;
+      if (lru->first.first != dev) cudaSetDevice(lru->first.first);
+      destroy_host_events(lru->second);
+      if (lru->first.first != dev) cudaSetDevice(cur);
+      g_host_events.erase(lru);
+    }
+    HostEvents h = {};
     for (int k = 0; k < 2; ++k) {
       if (cudaEventCreateWithFlags(&h.in[k], cudaEventDisableTiming) != cudaSuccess ||
           cudaEventCreateWithFlags(&h.layer[k], cudaEventDisableTiming) != cudaSuccess ||
@@ -482,6 +516,7 @@ moe_status_t moe_forward_host(const moe_layer_desc_t *desc, const void *x_host,
     it = g_host_events.emplace(std::make_pair(dev, (const void *)ws), h).first;
   }
   HostEvents &ev = it->second;
+  ev.last_use = ++g_host_clock;
   // copy in once the slot's previous layer has read its x
   cudaError_t e = cudaStreamWaitEvent(si, ev.layer[slot], 0);
   if (e == cudaSuccess) e = cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, si);
@@ -632,23 +667,15 @@ constexpr size_t kNoAllocScratchInts = (size_t)kNoAllocMaxChunks * (kMaxE + 1);
 
 static __device__ __align__(256) int32_t g_layout_scratch[kNoAllocScratchInts];
 
-// Device address of g_layout_scratch per device, looked up once per device.
-void *g_scratch_addr[64] = {nullptr};
-std::mutex g_scratch_mu;
-
+// Device address of g_layout_scratch on the current device.  It is looked up
+// on every call (a host-side table lookup once the module is loaded), so it
+// stays right after cudaDeviceReset, which unloads the module and may place
+// the array elsewhere when it is loaded again.
 cudaError_t layout_scratch_address(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_layout_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_layout_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

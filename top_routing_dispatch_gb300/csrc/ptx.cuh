@@ -121,40 +121,16 @@ __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Four rows (r0..r3) of a 2-D tensor, each box[0] elements wide from column
-// c0, written as one 4-row tile (the tensor map's box is one row high).
-// Rows outside the tensor read the fill value (zero).
+// The tensor map's box (box[0] x box[1] x 1 elements) at coordinates
+// (c0, c1, c2) of a 3-D tensor, written to shared memory at dst; the
+// transaction bytes complete on `bar`.  Elements outside the tensor read the
+// fill value (zero).
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int c0, int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// The same box written to every CTA of the cluster named in cta_mask, at the
-// same shared-memory offset; each receiving CTA's mbarrier at `bar`'s offset
-// gets the transaction bytes.  Used only inside one GPU's own memory.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *map,
-                                                      uint64_t *bar, int c0, int c1,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
-// As tma_load_2d_multicast, for a 3-D tensor map.
-__device__ __forceinline__ void tma_load_3d_multicast(void *dst, const CUtensorMap *map,
-                                                      uint64_t *bar, int c0, int c1, int c2,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 
@@ -233,16 +209,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// As mma_commit, arriving on the mbarrier at the same offset in every CTA of
-// the cluster named in cta_mask.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 

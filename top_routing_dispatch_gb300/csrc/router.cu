@@ -320,6 +320,11 @@ cudaError_t launch_topk_any(const Desc &d, const float *logits, const void *x, c
 
 }  // namespace
 
+int router_launches(const Desc &d) {
+  if (d.n == 0) return 0;
+  return 2;  // tensor-core tile kernel + rescoring, or FMA logits + TopK
+}
+
 cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, const float *bias,
                           int32_t *topk_idx, float *topk_w, float *logits, int32_t *status,
                           cudaStream_t s) {
