@@ -37,13 +37,21 @@ struct Desc {
 
 inline size_t elem_bytes(const Desc &d) { return d.bf16 ? 2 : 4; }
 
-// ---- router.cu (dispatches to router_tc.cu for bf16 layers with E % 64 == 0)
+// ---- router.cu (dispatches to router_mma.cu or router_tc.cu for bf16 layers)
+// guest: launch the configuration that fits beside a persistent GEMM CTA on
+// an SM (same results, shallower pipeline); only the warp-level MMA router has
+// one, the other routers ignore it
 cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, const float *bias,
                           int32_t *topk_idx, float *topk_w, float *logits, int32_t *status,
-                          cudaStream_t s);
+                          cudaStream_t s, bool guest = false);
 bool router_tc_supported(const Desc &d);
 // kernels launch_router enqueues for this layer
 int router_launches(const Desc &d);
+// router_mma.cu: warp-level MMA router (bf16, E = 64 or 128, K <= 8), one kernel
+bool router_mma_supported(const Desc &d);
+cudaError_t launch_router_mma(const Desc &d, const void *x, const void *w_gate, const float *bias,
+                              int32_t *topk_idx, float *topk_w, float *logits, bool guest,
+                              cudaStream_t s);
 cudaError_t launch_router_tc(const Desc &d, const void *x, const void *w_gate, const float *bias,
                              int32_t *topk_idx, float *topk_w, float *logits, int32_t *status,
                              cudaStream_t s);
@@ -52,13 +60,14 @@ cudaError_t launch_router_tc(const Desc &d, const void *x, const void *w_gate, c
 size_t layout_ws_bytes(const Desc &d);
 cudaError_t launch_layout(const Desc &d, const int32_t *topk_idx, int32_t *counts,
                           int32_t *offsets, int32_t *perm, int32_t *inv_perm, int32_t *status,
-                          void *ws, cudaStream_t s);
+                          void *ws, cudaStream_t s, bool guest = false);
 
 // ---- permute_combine.cu
 cudaError_t launch_permute(const Desc &d, const void *x, const int32_t *perm, void *x_perm,
-                           int32_t *status, cudaStream_t s);
+                           int32_t *status, cudaStream_t s, bool guest = false);
 cudaError_t launch_combine(const Desc &d, const void *y_perm, const float *topk_w,
-                           const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s);
+                           const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s,
+                           bool guest = false);
 
 // ---- gemm_tc.cu (bf16, tcgen05) and gemm_simt.cu (float32)
 cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
@@ -76,7 +85,8 @@ cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w
                                      const float *topk_w, void *y_slot, int sm_reserve,
                                      int32_t *status, cudaStream_t s);
 // y[t] = sum over k of y_slot[t*K + k] (float32, slot order, one rounding)
-cudaError_t launch_combine_slots(const Desc &d, const void *y_slot, void *y, cudaStream_t s);
+cudaError_t launch_combine_slots(const Desc &d, const void *y_slot, void *y, cudaStream_t s,
+                                 bool guest = false);
 // backward (backward.cu, gemm_tc.cu modes 5 and 6, gemm_wgrad.cu)
 constexpr int kRouterBwdSplit = 16;  // token ranges of the dW_gate reduction
 cudaError_t launch_combine_bwd(const Desc &d, const void *dy, const void *y_perm,
@@ -150,6 +160,36 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
+// Launch on the dispatch stream of the two-stream schedule, beside the
+// persistent GEMM of the other stream ("guest"): without programmatic stream
+// serialisation, so no CTA of the stream's next kernel sits resident on an SM
+// waiting for this one.  Otherwise as launch_pdl.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(bool guest, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                            size_t smem, cudaStream_t s, Args &&...args) {
+  if (!guest) return launch_pdl(kernel, grid, block, smem, s, static_cast<Args &&>(args)...);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
+// Prefer the largest shared-memory carveout for a kernel that may share an
+// SM with the grouped GEMM (whose CTA needs ~210 KB): an SM that starts one of
+// its CTAs then keeps the configuration the GEMM needs.  Set once per device.
+template <typename... KArgs>
+inline cudaError_t prefer_max_shared(void (*kernel)(KArgs...)) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
 }
 
 __device__ __forceinline__ void flag_status(int32_t *status, int bits) {

@@ -21,6 +21,9 @@ constexpr int LW = LT / 32;           // warps per block
 constexpr int SLICE = 256;            // pairs per warp
 constexpr int CH = LW * SLICE;        // pairs per block (2048)
 
+// GUEST: the instantiation launched beside the grouped GEMM (own carveout
+// preference, see prefer_max_shared)
+template <bool GUEST>
 __global__ void __launch_bounds__(LT) layout_count(const int32_t *__restrict__ idx, long long nK,
                                                    int E, int32_t *__restrict__ cnt,
                                                    int32_t *status) {
@@ -55,6 +58,7 @@ __global__ void __launch_bounds__(LT) layout_count(const int32_t *__restrict__ i
 // the lanes holding one expert find each other through a per-warp bit mask
 // per expert (atomicOr of the lane bit), a pair's rank is the number of lower
 // lanes with its expert, so the order inside an expert follows the flat index.
+template <bool GUEST>
 __global__ void __launch_bounds__(LT) layout_scan_scatter(const int32_t *__restrict__ idx,
                                                           long long nK, int E, int nb,
                                                           const int32_t *__restrict__ cnt,
@@ -170,7 +174,7 @@ size_t layout_ws_bytes(const Desc &d) {
 
 cudaError_t launch_layout(const Desc &d, const int32_t *topk_idx, int32_t *counts,
                           int32_t *offsets, int32_t *perm, int32_t *inv_perm, int32_t *status,
-                          void *ws, cudaStream_t s) {
+                          void *ws, cudaStream_t s, bool guest) {
   const long long nK = d.nK();
   const int nb = num_chunks(nK);
   if (nb == 0) {  // no tokens: all counts and offsets are zero
@@ -179,10 +183,21 @@ cudaError_t launch_layout(const Desc &d, const int32_t *topk_idx, int32_t *count
     return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d.E + 1), s);
   }
   int32_t *cnt = reinterpret_cast<int32_t *>(ws);
-  cudaError_t e = launch_pdl(layout_count, dim3(nb), dim3(LT), 0, s, topk_idx, nK, d.E, cnt, status);
+  if (guest) {
+    static bool carveout[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 && !carveout[dev]) {
+      cudaError_t e = prefer_max_shared(layout_count<true>);
+      if (e == cudaSuccess) e = prefer_max_shared(layout_scan_scatter<true>);
+      if (e != cudaSuccess) return e;
+      carveout[dev] = true;
+    }
+  }
+  cudaError_t e = launch_k(guest, guest ? layout_count<true> : layout_count<false>, dim3(nb),
+                           dim3(LT), 0, s, topk_idx, nK, d.E, cnt, status);
   if (e != cudaSuccess) return e;
-  return launch_pdl(layout_scan_scatter, dim3(nb), dim3(LT), 0, s, topk_idx, nK, d.E, nb, cnt,
-                    counts, offsets, perm, inv_perm);
+  return launch_k(guest, guest ? layout_scan_scatter<true> : layout_scan_scatter<false>, dim3(nb),
+                  dim3(LT), 0, s, topk_idx, nK, d.E, nb, cnt, counts, offsets, perm, inv_perm);
 }
 
 }  // namespace moe

@@ -353,26 +353,26 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
   cudaStream_t sd = dispatch ? dispatch : compute;
   const bool two = sd != sc;
 
-  auto route = [&](int j, cudaStream_t s) -> cudaError_t {
+  // guest: a dispatch-stream launch that runs beside the other stream's GEMM
+  // (see launch_k); every result is the same either way
+  auto route = [&](int j, cudaStream_t s, bool guest) -> cudaError_t {
     return launch_router(d, x[j], w_gate, bias, (int32_t *)slot_ptr(d, ws, j, S_TOPK_IDX),
                          (float *)slot_ptr(d, ws, j, S_TOPK_W),
-                         (float *)slot_ptr(d, ws, j, S_LOGITS), status, s);
+                         (float *)slot_ptr(d, ws, j, S_LOGITS), status, s, guest);
   };
-  auto layout_permute = [&](int j, cudaStream_t s) -> cudaError_t {
-    cudaError_t e = launch_layout(d, (const int32_t *)slot_ptr(d, ws, j, S_TOPK_IDX),
-                                  (int32_t *)slot_ptr(d, ws, j, S_COUNTS),
-                                  (int32_t *)slot_ptr(d, ws, j, S_OFFSETS),
-                                  (int32_t *)slot_ptr(d, ws, j, S_PERM),
-                                  (int32_t *)slot_ptr(d, ws, j, S_INV_PERM), status,
-                                  slot_ptr(d, ws, j, S_LAYOUT_WS), s);
-    if (e != cudaSuccess) return e;
-    return launch_permute(d, x[j], (int32_t *)slot_ptr(d, ws, j, S_PERM),
-                          slot_ptr(d, ws, j, S_X_PERM), status, s);
-  };
-  auto front = [&](int j, cudaStream_t s) -> cudaError_t {  // route + layout + permute
-    cudaError_t e = route(j, s);
-    if (e != cudaSuccess) return e;
-    return layout_permute(j, s);
+  auto front = [&](int j, cudaStream_t s, bool guest) -> cudaError_t {  // route, layout, permute
+    cudaError_t e = route(j, s, guest);
+    if (e == cudaSuccess)
+      e = launch_layout(d, (const int32_t *)slot_ptr(d, ws, j, S_TOPK_IDX),
+                        (int32_t *)slot_ptr(d, ws, j, S_COUNTS),
+                        (int32_t *)slot_ptr(d, ws, j, S_OFFSETS),
+                        (int32_t *)slot_ptr(d, ws, j, S_PERM),
+                        (int32_t *)slot_ptr(d, ws, j, S_INV_PERM), status,
+                        slot_ptr(d, ws, j, S_LAYOUT_WS), s, guest);
+    if (e == cudaSuccess)
+      e = launch_permute(d, x[j], (int32_t *)slot_ptr(d, ws, j, S_PERM),
+                         slot_ptr(d, ws, j, S_X_PERM), status, s, guest);
+    return e;
   };
   // bf16: GEMM2 applies the routing weights and writes each row to its
   // (token, slot) position (slot y_perm of the workspace), and the combine
@@ -393,19 +393,20 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
                                     (const float *)slot_ptr(d, ws, j, S_TOPK_W),
                                     slot_ptr(d, ws, j, S_Y_PERM), reserve, status, s);
   };
-  auto back = [&](int j, cudaStream_t s) -> cudaError_t {
-    if (d.bf16) return launch_combine_slots(d, slot_ptr(d, ws, j, S_Y_PERM), y[j], s);
+  auto back = [&](int j, cudaStream_t s, bool guest) -> cudaError_t {
+    if (d.bf16) return launch_combine_slots(d, slot_ptr(d, ws, j, S_Y_PERM), y[j], s, guest);
     return launch_combine(d, slot_ptr(d, ws, j, S_Y_PERM),
                           (const float *)slot_ptr(d, ws, j, S_TOPK_W),
-                          (const int32_t *)slot_ptr(d, ws, j, S_INV_PERM), y[j], status, s);
+                          (const int32_t *)slot_ptr(d, ws, j, S_INV_PERM), y[j], status, s,
+                          guest);
   };
 
   if (!two) {
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), sc);
     for (int j = 0; j < num_mb && e == cudaSuccess; ++j) {
-      e = front(j, sc);
+      e = front(j, sc, false);
       if (e == cudaSuccess) e = experts(j, sc);
-      if (e == cudaSuccess) e = back(j, sc);
+      if (e == cudaSuccess) e = back(j, sc, false);
     }
     return cuda_status(e);
   }
@@ -421,40 +422,38 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
     pool.ready = true;
   }
   cudaEvent_t ev_start = pool.ev[3 * kMaxMB], ev_done = pool.ev[3 * kMaxMB + 1];
-  cudaEvent_t *ev_front = pool.ev, *ev_gemm = pool.ev + kMaxMB, *ev_route = pool.ev + 2 * kMaxMB;
+  cudaEvent_t *ev_front = pool.ev, *ev_gemm = pool.ev + kMaxMB;
 
-  // Schedule (D = dispatch stream, C = compute stream):
-  //   D: route(0) | layout+permute(0) | layout+permute(1) | combine(0) | layout+permute(2) | ...
-  //   C:          | route(1)  | GEMMs(0)                  | route(2) | GEMMs(1)           | ...
-  // The router of micro-batch j+1 runs on C right before GEMMs(j), beside
-  // micro-batch j's layout and permute; j+1's layout and permute run beside
-  // GEMMs(j) and combine(j) beside GEMMs(j+1).  Only the router's tile kernel
-  // cannot share an SM with a GEMM CTA (both need most of the shared memory),
-  // so it is placed where the other stream runs memory-bound kernels.
+  // Schedule (D = dispatch stream, C = compute stream; front = route, layout
+  // and permute):
+  //   D: front(0) | front(1)        | combine(0) front(2) | ... | combine(last)
+  //   C:          | GEMMs(0)        | GEMMs(1)            | ...
+  // front(j+1) and combine(j-1) run on D while GEMMs(j) run on C.  They are
+  // launched as guests: at most one CTA per SM, each small enough (registers,
+  // shared memory, no TMEM) to sit beside the persistent GEMM CTA, and without
+  // programmatic serialisation, so no CTA of the next kernel on D waits
+  // resident on an SM.  front(0) and the last combine have no GEMM to hide
+  // under and run at full width.
   cudaError_t e = cudaEventRecord(ev_start, sc);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_start, 0);
   if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), sd);
-  if (e == cudaSuccess) e = route(0, sd);
-  if (e == cudaSuccess) e = cudaEventRecord(ev_route[0], sd);
+  if (e == cudaSuccess) e = front(0, sd, false);
+  if (e == cudaSuccess) e = cudaEventRecord(ev_front[0], sd);
   for (int j = 0; j < num_mb && e == cudaSuccess; ++j) {
-    if (j + 1 < num_mb) {                                        // route of j+1 on C
-      e = cudaStreamWaitEvent(sc, ev_route[j], 0);
-      if (e == cudaSuccess) e = route(j + 1, sc);
-      if (e == cudaSuccess) e = cudaEventRecord(ev_route[j + 1], sc);
-    }
-    if (e == cudaSuccess && j > 0) e = cudaStreamWaitEvent(sd, ev_route[j], 0);
-    if (e == cudaSuccess) e = layout_permute(j, sd);             // rest of j's dispatch
-    if (e == cudaSuccess) e = cudaEventRecord(ev_front[j], sd);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, ev_front[j], 0);
-    if (e == cudaSuccess) e = experts(j, sc);                    // experts of j
+    e = cudaStreamWaitEvent(sc, ev_front[j], 0);                   // GEMMs of j on C
+    if (e == cudaSuccess) e = experts(j, sc);
     if (e == cudaSuccess) e = cudaEventRecord(ev_gemm[j], sc);
-    if (j > 0) {                                                 // combine of j-1
+    if (j > 0) {                                                   // combine of j-1 on D
       if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_gemm[j - 1], 0);
-      if (e == cudaSuccess) e = back(j - 1, sd);
+      if (e == cudaSuccess) e = back(j - 1, sd, true);
+    }
+    if (j + 1 < num_mb) {                                          // front of j+1 on D
+      if (e == cudaSuccess) e = front(j + 1, sd, true);
+      if (e == cudaSuccess) e = cudaEventRecord(ev_front[j + 1], sd);
     }
   }
   if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_gemm[num_mb - 1], 0);
-  if (e == cudaSuccess) e = back(num_mb - 1, sd);
+  if (e == cudaSuccess) e = back(num_mb - 1, sd, false);
   if (e == cudaSuccess) e = cudaEventRecord(ev_done, sd);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, ev_done, 0);
   return cuda_status(e);

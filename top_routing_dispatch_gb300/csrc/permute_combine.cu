@@ -23,6 +23,9 @@ constexpr int PU = 8;     // 16-byte vectors in flight per lane
 // streaming (evict-first) cache hint, so the written rows do not push x,
 // which is re-read K times, out of L2 (measured: 30.5 -> 27.3 us at the
 // OLMoE shape, 134.6 -> 126.9 us for the skewed layer).
+// GUEST: the instantiation launched beside the grouped GEMM (its own kernel,
+// so that its shared-memory carveout preference does not touch the other).
+template <bool GUEST>
 __global__ void __launch_bounds__(PT) permute_kernel(const uint4 *__restrict__ x,
                                                      const int32_t *__restrict__ perm,
                                                      uint4 *__restrict__ xp, long long nK, int K,
@@ -90,7 +93,7 @@ constexpr int CV = 64;  // vectors per combine item
 
 // SLOTS: the rows of token t are t*K .. t*K+K-1 of an already weighted,
 // slot-ordered array (GEMM2's weighted epilogue), added with weight 1.
-template <bool BF16, int KM, bool SLOTS = false>
+template <bool BF16, int KM, bool SLOTS, bool GUEST>
 __global__ void __launch_bounds__(PT) combine_kernel(const uint4 *__restrict__ yp,
                                                      const float *__restrict__ tw,
                                                      const int32_t *__restrict__ inv,
@@ -166,8 +169,10 @@ __global__ void __launch_bounds__(PT) combine_kernel(const uint4 *__restrict__ y
   }
 }
 
-// blocks of the kernel that fit on the device at once (all CTAs in one wave)
-template <auto Kernel>
+// Blocks of the kernel that fit on the device at once (all CTAs in one wave);
+// for the guest instantiation, one per SM, and the first call on a device sets
+// its shared-memory carveout preference (see prefer_max_shared).
+template <auto Kernel, bool GUEST>
 int resident_grid() {
   static int cache[64] = {0};
   int dev = 0;
@@ -175,62 +180,76 @@ int resident_grid() {
   int &c = cache[dev >= 0 && dev < 64 ? dev : 0];
   if (c == 0) {
     int per_sm = 0;
+    if (GUEST) prefer_max_shared(Kernel);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, Kernel, PT, 0) != cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
-    c = per_sm * device_sm_count();
+    c = GUEST ? device_sm_count() : per_sm * device_sm_count();
   }
   return c;
 }
 
-template <bool BF16, int KM, bool SLOTS = false>
-cudaError_t combine_k(const Desc &d, const void *y_perm, const float *topk_w,
+template <bool BF16, int KM, bool SLOTS, bool GUEST>
+cudaError_t combine_g(const Desc &d, const void *y_perm, const float *topk_w,
                       const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s) {
   const int V = (int)((size_t)d.H * elem_bytes(d) / 16);
   const long long items = (long long)d.n * ((V + CV - 1) / CV);
-  const long long res = resident_grid<combine_kernel<BF16, KM, SLOTS>>();
+  const long long res = resident_grid<combine_kernel<BF16, KM, SLOTS, GUEST>, GUEST>();
   const long long want = (items + (PT / 32) - 1) / (PT / 32);
   const int grid = (int)(want < res ? want : res);
-  return launch_pdl(combine_kernel<BF16, KM, SLOTS>, dim3(grid), dim3(PT), 0, s,
-                    reinterpret_cast<const uint4 *>(y_perm), topk_w, inv_perm,
-                    reinterpret_cast<uint4 *>(y), d.n, d.K, V, d.nK(), status);
+  return launch_k(GUEST, combine_kernel<BF16, KM, SLOTS, GUEST>, dim3(grid), dim3(PT), 0, s,
+                  reinterpret_cast<const uint4 *>(y_perm), topk_w, inv_perm,
+                  reinterpret_cast<uint4 *>(y), d.n, d.K, V, d.nK(), status);
+}
+
+template <bool BF16, int KM, bool SLOTS = false>
+cudaError_t combine_k(const Desc &d, const void *y_perm, const float *topk_w,
+                      const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s,
+                      bool guest) {
+  return guest ? combine_g<BF16, KM, SLOTS, true>(d, y_perm, topk_w, inv_perm, y, status, s)
+               : combine_g<BF16, KM, SLOTS, false>(d, y_perm, topk_w, inv_perm, y, status, s);
 }
 
 template <bool BF16, bool SLOTS = false>
 cudaError_t combine_dispatch_k(const Desc &d, const void *y_perm, const float *topk_w,
                                const int32_t *inv_perm, void *y, int32_t *status,
-                               cudaStream_t s) {
-  if (d.K <= 2) return combine_k<BF16, 2, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s);
-  if (d.K <= 4) return combine_k<BF16, 4, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s);
-  if (d.K <= 8) return combine_k<BF16, 8, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s);
-  return combine_k<BF16, kMaxK, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s);
+                               cudaStream_t s, bool guest) {
+  if (d.K <= 2) return combine_k<BF16, 2, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s, guest);
+  if (d.K <= 4) return combine_k<BF16, 4, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s, guest);
+  if (d.K <= 8) return combine_k<BF16, 8, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s, guest);
+  return combine_k<BF16, kMaxK, SLOTS>(d, y_perm, topk_w, inv_perm, y, status, s, guest);
 }
 
 }  // namespace
 
 cudaError_t launch_permute(const Desc &d, const void *x, const int32_t *perm, void *x_perm,
-                           int32_t *status, cudaStream_t s) {
+                           int32_t *status, cudaStream_t s, bool guest) {
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
   const int V = (int)((size_t)d.H * elem_bytes(d) / 16);
-  const long long res = resident_grid<permute_kernel>();
+  const long long res =
+      guest ? resident_grid<permute_kernel<true>, true>() : resident_grid<permute_kernel<false>, false>();
   const long long want = (nK + (PT / 32) - 1) / (PT / 32);
-  return launch_pdl(permute_kernel, dim3((int)(want < res ? want : res)), dim3(PT), 0, s,
-                    reinterpret_cast<const uint4 *>(x), perm, reinterpret_cast<uint4 *>(x_perm),
-                    nK, d.K, V, status);
+  return launch_k(guest, guest ? permute_kernel<true> : permute_kernel<false>,
+                  dim3((int)(want < res ? want : res)), dim3(PT), 0, s,
+                  reinterpret_cast<const uint4 *>(x), perm, reinterpret_cast<uint4 *>(x_perm), nK,
+                  d.K, V, status);
 }
 
-cudaError_t launch_combine_slots(const Desc &d, const void *y_slot, void *y, cudaStream_t s) {
+cudaError_t launch_combine_slots(const Desc &d, const void *y_slot, void *y, cudaStream_t s,
+                                 bool guest) {
   if (d.n == 0) return cudaSuccess;
-  if (d.bf16) return combine_dispatch_k<true, true>(d, y_slot, nullptr, nullptr, y, nullptr, s);
-  return combine_dispatch_k<false, true>(d, y_slot, nullptr, nullptr, y, nullptr, s);
+  if (d.bf16)
+    return combine_dispatch_k<true, true>(d, y_slot, nullptr, nullptr, y, nullptr, s, guest);
+  return combine_dispatch_k<false, true>(d, y_slot, nullptr, nullptr, y, nullptr, s, guest);
 }
 
 cudaError_t launch_combine(const Desc &d, const void *y_perm, const float *topk_w,
-                           const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s) {
+                           const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s,
+                           bool guest) {
   if (d.n == 0) return cudaSuccess;
-  if (d.bf16) return combine_dispatch_k<true>(d, y_perm, topk_w, inv_perm, y, status, s);
-  return combine_dispatch_k<false>(d, y_perm, topk_w, inv_perm, y, status, s);
+  if (d.bf16) return combine_dispatch_k<true>(d, y_perm, topk_w, inv_perm, y, status, s, guest);
+  return combine_dispatch_k<false>(d, y_perm, topk_w, inv_perm, y, status, s, guest);
 }
 
 }  // namespace moe

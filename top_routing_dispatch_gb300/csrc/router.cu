@@ -322,13 +322,19 @@ cudaError_t launch_topk_any(const Desc &d, const float *logits, const void *x, c
 
 int router_launches(const Desc &d) {
   if (d.n == 0) return 0;
+  if (router_mma_supported(d)) return 1;  // one kernel: logits, TopK, near-tie rescoring
   return 2;  // tensor-core tile kernel + rescoring, or FMA logits + TopK
 }
 
 cudaError_t launch_router(const Desc &d, const void *x, const void *w_gate, const float *bias,
                           int32_t *topk_idx, float *topk_w, float *logits, int32_t *status,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool guest) {
   if (d.n == 0) return cudaSuccess;
+  if (router_mma_supported(d)) {
+    // warp-level MMA logits with softmax, TopK and near-tie rescoring in one
+    // kernel that fits beside a persistent GEMM CTA on an SM
+    return launch_router_mma(d, x, w_gate, bias, topk_idx, topk_w, logits, guest, s);
+  }
   if (router_tc_supported(d)) {
     // tensor-core logits with softmax, TopK and near-tie rescoring fused
     return launch_router_tc(d, x, w_gate, bias, topk_idx, topk_w, logits, status, s);
