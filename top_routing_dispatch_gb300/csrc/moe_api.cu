@@ -101,8 +101,17 @@ uint8_t *slot_ptr(const Desc &d, void *ws, int mb, int which) {
 // most recent record at the time it is enqueued, so reuse across calls is
 // safe; the mutex serialises enqueueing from several host threads.
 constexpr int kMaxMB = 64;
+constexpr int kPoolEvents = 4 * kMaxMB + 3;
+// Per device: the events of moe_forward_microbatches and the library's own
+// dispatch stream, created at the highest stream priority.  The two-stream
+// schedule runs its dispatch-side kernels there: the block scheduler then
+// serves their CTAs before CTAs of the compute stream's next GEMM, which a
+// programmatic launch makes pending while the current GEMM still holds every
+// SM (at equal priority those pending GEMM CTAs hold back the small dispatch
+// kernels until the GEMM ends).
 struct EventPool {
-  cudaEvent_t ev[3 * kMaxMB + 2];
+  cudaEvent_t ev[kPoolEvents];
+  cudaStream_t hi = nullptr;
   bool ready = false;
 };
 EventPool g_pools[64];
@@ -350,7 +359,7 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
   int32_t *status = status_word ? status_word
                                 : reinterpret_cast<int32_t *>(slot_ptr(d, ws, 0, S_STATUS));
   cudaStream_t sc = compute;
-  cudaStream_t sd = dispatch ? dispatch : compute;
+  cudaStream_t sd = dispatch ? dispatch : compute;  // replaced by the library's stream below
   const bool two = sd != sc;
 
   // guest: a dispatch-stream launch that runs beside the other stream's GEMM
@@ -360,7 +369,7 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
                          (float *)slot_ptr(d, ws, j, S_TOPK_W),
                          (float *)slot_ptr(d, ws, j, S_LOGITS), status, s, guest);
   };
-  auto front = [&](int j, cudaStream_t s, bool guest) -> cudaError_t {  // route, layout, permute
+  auto route_layout = [&](int j, cudaStream_t s, bool guest) -> cudaError_t {
     cudaError_t e = route(j, s, guest);
     if (e == cudaSuccess)
       e = launch_layout(d, (const int32_t *)slot_ptr(d, ws, j, S_TOPK_IDX),
@@ -369,29 +378,42 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
                         (int32_t *)slot_ptr(d, ws, j, S_PERM),
                         (int32_t *)slot_ptr(d, ws, j, S_INV_PERM), status,
                         slot_ptr(d, ws, j, S_LAYOUT_WS), s, guest);
-    if (e == cudaSuccess)
-      e = launch_permute(d, x[j], (int32_t *)slot_ptr(d, ws, j, S_PERM),
-                         slot_ptr(d, ws, j, S_X_PERM), status, s, guest);
+    return e;
+  };
+  auto permute = [&](int j, cudaStream_t s, bool guest) -> cudaError_t {
+    return launch_permute(d, x[j], (int32_t *)slot_ptr(d, ws, j, S_PERM),
+                          slot_ptr(d, ws, j, S_X_PERM), status, s, guest);
+  };
+  auto front = [&](int j, cudaStream_t s, bool guest) -> cudaError_t {  // route, layout, permute
+    cudaError_t e = route_layout(j, s, guest);
+    if (e == cudaSuccess) e = permute(j, s, guest);
     return e;
   };
   // bf16: GEMM2 applies the routing weights and writes each row to its
   // (token, slot) position (slot y_perm of the workspace), and the combine
   // adds each token's K contiguous rows; float32: GEMM2 writes y_perm in
   // expert order and the combine gathers and weights
-  auto experts = [&](int j, cudaStream_t s) -> cudaError_t {
+  const int reserve = two ? sm_reserve : 0;
+  auto gemm1 = [&](int j, cudaStream_t s) -> cudaError_t {
     const int32_t *off = (const int32_t *)slot_ptr(d, ws, j, S_OFFSETS);
-    const int reserve = two ? sm_reserve : 0;
+    return d.bf16 ? launch_gemm1_tc(d, slot_ptr(d, ws, j, S_X_PERM), w13, off,
+                                    slot_ptr(d, ws, j, S_H), reserve, status, s)
+                  : launch_gemm1_simt(d, slot_ptr(d, ws, j, S_X_PERM), w13, off,
+                                      slot_ptr(d, ws, j, S_H), status, s);
+  };
+  auto gemm2 = [&](int j, cudaStream_t s) -> cudaError_t {
+    const int32_t *off = (const int32_t *)slot_ptr(d, ws, j, S_OFFSETS);
     if (!d.bf16)
-      return launch_experts(d, slot_ptr(d, ws, j, S_X_PERM), w13, w2, off,
-                            slot_ptr(d, ws, j, S_H), slot_ptr(d, ws, j, S_Y_PERM), reserve,
-                            status, s);
-    cudaError_t e = launch_gemm1_tc(d, slot_ptr(d, ws, j, S_X_PERM), w13, off,
-                                    slot_ptr(d, ws, j, S_H), reserve, status, s);
-    if (e != cudaSuccess) return e;
+      return launch_gemm2_simt(d, slot_ptr(d, ws, j, S_H), w2, off, slot_ptr(d, ws, j, S_Y_PERM),
+                               status, s);
     return launch_gemm2_tc_weighted(d, slot_ptr(d, ws, j, S_H), w2, off,
                                     (const int32_t *)slot_ptr(d, ws, j, S_PERM),
                                     (const float *)slot_ptr(d, ws, j, S_TOPK_W),
                                     slot_ptr(d, ws, j, S_Y_PERM), reserve, status, s);
+  };
+  auto experts = [&](int j, cudaStream_t s) -> cudaError_t {
+    cudaError_t e = gemm1(j, s);
+    return e == cudaSuccess ? gemm2(j, s) : e;
   };
   auto back = [&](int j, cudaStream_t s, bool guest) -> cudaError_t {
     if (d.bf16) return launch_combine_slots(d, slot_ptr(d, ws, j, S_Y_PERM), y[j], s, guest);
@@ -416,39 +438,53 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
   std::lock_guard<std::mutex> lock(g_pool_mu);
   EventPool &pool = g_pools[dev];
   if (!pool.ready) {
-    for (int i = 0; i < 3 * kMaxMB + 2; ++i)
+    for (int i = 0; i < kPoolEvents; ++i)
       if (cudaEventCreateWithFlags(&pool.ev[i], cudaEventDisableTiming) != cudaSuccess)
         return MOE_ERR_CUDA;
+    int lo = 0, hi = 0;
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&pool.hi, cudaStreamNonBlocking, hi) != cudaSuccess)
+      return MOE_ERR_CUDA;
     pool.ready = true;
   }
-  cudaEvent_t ev_start = pool.ev[3 * kMaxMB], ev_done = pool.ev[3 * kMaxMB + 1];
-  cudaEvent_t *ev_front = pool.ev, *ev_gemm = pool.ev + kMaxMB;
+  cudaEvent_t ev_start = pool.ev[4 * kMaxMB], ev_done = pool.ev[4 * kMaxMB + 1];
+  cudaEvent_t ev_caller = pool.ev[4 * kMaxMB + 2];
+  cudaEvent_t *ev_front = pool.ev, *ev_gemm = pool.ev + kMaxMB, *ev_g1 = pool.ev + 2 * kMaxMB;
+  cudaStream_t caller_d = sd;
+  sd = pool.hi;
 
-  // Schedule (D = dispatch stream, C = compute stream; front = route, layout
-  // and permute):
-  //   D: front(0) | front(1)        | combine(0) front(2) | ... | combine(last)
-  //   C:          | GEMMs(0)        | GEMMs(1)            | ...
-  // front(j+1) and combine(j-1) run on D while GEMMs(j) run on C.  They are
-  // launched as guests: at most one CTA per SM, each small enough (registers,
-  // shared memory, no TMEM) to sit beside the persistent GEMM CTA, and without
-  // programmatic serialisation, so no CTA of the next kernel on D waits
-  // resident on an SM.  front(0) and the last combine have no GEMM to hide
-  // under and run at full width.
+  // Schedule (D = the library's high-priority dispatch stream, joined to the
+  // caller's compute and dispatch streams by events; C = compute stream):
+  //   D: front(0) | route+layout(1)  permute(1) | combine(0) route+layout(2) ...
+  //   C:          | GEMM1(0)         GEMM2(0)   | GEMM1(1)   GEMM2(1)  ...
+  // Micro-batch j+1's route and layout run beside GEMM1(j), its permute (which
+  // writes x_perm, the largest stream of the dispatch) beside GEMM2(j), and
+  // combine(j-1) beside GEMMs(j).  They are launched as guests: at most one
+  // CTA per SM, each small enough (registers, shared memory, no TMEM) to sit
+  // beside the persistent GEMM CTA, and without programmatic serialisation, so
+  // no CTA of the next kernel on D waits resident on an SM.  front(0) and the
+  // last combine have no GEMM to hide under and run at full width.
   cudaError_t e = cudaEventRecord(ev_start, sc);
+  if (e == cudaSuccess) e = cudaEventRecord(ev_caller, caller_d);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_caller, 0);
   if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), sd);
   if (e == cudaSuccess) e = front(0, sd, false);
   if (e == cudaSuccess) e = cudaEventRecord(ev_front[0], sd);
   for (int j = 0; j < num_mb && e == cudaSuccess; ++j) {
     e = cudaStreamWaitEvent(sc, ev_front[j], 0);                   // GEMMs of j on C
-    if (e == cudaSuccess) e = experts(j, sc);
+    if (e == cudaSuccess) e = gemm1(j, sc);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_g1[j], sc);
+    if (e == cudaSuccess) e = gemm2(j, sc);
     if (e == cudaSuccess) e = cudaEventRecord(ev_gemm[j], sc);
     if (j > 0) {                                                   // combine of j-1 on D
       if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_gemm[j - 1], 0);
       if (e == cudaSuccess) e = back(j - 1, sd, true);
     }
     if (j + 1 < num_mb) {                                          // front of j+1 on D
-      if (e == cudaSuccess) e = front(j + 1, sd, true);
+      if (e == cudaSuccess) e = route_layout(j + 1, sd, true);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, ev_g1[j], 0);
+      if (e == cudaSuccess) e = permute(j + 1, sd, true);
       if (e == cudaSuccess) e = cudaEventRecord(ev_front[j + 1], sd);
     }
   }
@@ -456,6 +492,7 @@ moe_status_t moe_forward_microbatches(const moe_layer_desc_t *desc, int num_mb,
   if (e == cudaSuccess) e = back(num_mb - 1, sd, false);
   if (e == cudaSuccess) e = cudaEventRecord(ev_done, sd);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, ev_done, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(caller_d, ev_done, 0);
   return cuda_status(e);
 }
 
