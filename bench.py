@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-domino", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--weights", choices=["tiled", "row"], default="tiled",
+                    help="bf16 expert weights: tiled by moe_prepare_weights once, untimed "
+                         "(default), or read row-major")
     ap.add_argument("--extra-workloads", default="olmoe_skew_bf16,dsv3_bf16,tiny_fp32",
                     help="other single-batch workloads timed after the headline (N=1 only); "
                          "empty to skip")
@@ -180,7 +183,9 @@ def host_inputs_from_device(L, x, rows):
     import torch
     ri = torch.as_tensor(rows, device=x.device)
     f32 = lambda t: None if t is None else t.detach().to("cpu", torch.float32).numpy()
-    return (f32(x[ri]), f32(L["w_gate"]), f32(L["bias"]), f32(L["w13"]), f32(L["w2"]))
+    # the row-major weights (the device run may read their tiled copies)
+    return (f32(x[ri]), f32(L["w_gate"]), f32(L["bias"]), f32(L.get("w13_row", L["w13"])),
+            f32(L.get("w2_row", L["w2"])))
 
 
 def cpu_baseline(cfg, L, x, sample, seconds):
@@ -251,6 +256,7 @@ def algorithmic(cfg, counts=None):
         "router": {"flop": 2 * n * H * E, "bytes": n * H * b + H * E * b + 2 * n * E * 4 + 2 * nK * 4},
         "layout": {"flop": 0, "bytes": 2 * nK * 4 + 2 * nK * 4 + (2 * E + 1) * 4},
         "permute": {"flop": 0, "bytes": n * H * b + nK * H * b + nK * 4},
+        "permute_scatter": {"flop": 0, "bytes": n * H * b + nK * H * b + nK * 4},
         "gemm1": {"flop": 4 * nK * H * I, "bytes": nK * H * b + used * H * 2 * I * b + nK * I * b},
         # GEMM1 with the permute fused: x once (rows are re-read from L2),
         # perm, the used experts' W13, h
@@ -393,14 +399,25 @@ def compact_kernels(kernels):
     return out
 
 
+def tiled_weights(args, cfg):
+    return args.weights == "tiled" and cfg.dtype == "bf16"
+
+
 def measure_layer(args, torch, M, synth, cfg, dev, peaks, rank, steps, warmup, dist=None):
     """Times one workload's layer: `steps` forward steps (one
     moe_forward_microbatches call each, L2 flushed before each), then the same
     step as one C-ABI call per row (flushed and warm).  Returns the context the
-    headline's extra measurements reuse."""
+    headline's extra measurements reuse.  With tiled weights the expert
+    entry points read the moe_prepare_weights copies (prepared once, before
+    any timing); L keeps the row-major weights as well (the backward's)."""
     L = synth.make_layer(cfg, dev)
     x = synth.make_x(cfg, dev, seed=rank_seed(cfg, rank))
-    desc = M.desc_for(cfg)
+    tiled = tiled_weights(args, cfg)
+    desc = M.desc_for(cfg, tiled=tiled)
+    if tiled:
+        L["w13_row"], L["w2_row"] = L["w13"], L["w2"]
+        L["w13"], L["w2"] = M.moe_prepare_weights(M.desc_for(cfg), L["w13_row"], L["w2_row"])
+        torch.cuda.synchronize()
     layer = M.MoELayer(desc, L["w_gate"], L["bias"], L["w13"], L["w2"])
     v = {k: layer.view(k) for k in ("logits", "topk_idx", "topk_w", "counts", "offsets", "perm",
                                     "inv_perm", "x_perm", "h", "y_perm")}
@@ -445,6 +462,12 @@ def measure_layer(args, torch, M, synth, cfg, dev, peaks, rank, steps, warmup, d
     per_phase_warm = {name: [s[i].elapsed_time(s[i + 1]) for s in warm]
                       for i, (name, _) in enumerate(rows)}
     phased_ms = [s[0].elapsed_time(s[-1]) for s in evs]
+    # entry points the step does not call, timed alone on the same layout:
+    # the scatter form of the permute (x read once)
+    xp_alt = torch.empty_like(v["x_perm"])
+    scat = lambda: M.moe_permute_scatter(desc, x, v["inv_perm"], xp_alt, st, stream)
+    T.measure(scat, 3)
+    per_phase["permute_scatter"] = T.measure(scat, steps)
     status = M.moe_check_status(st, stream)
     return dict(L=L, x=x, y=y, desc=desc, layer=layer, v=v, st=st, stream=stream, T=T,
                 rows=rows, fwd_ms=fwd_ms, per_phase=per_phase, per_phase_warm=per_phase_warm,
@@ -577,6 +600,8 @@ def run_ours(args, cfg):
         "roofline": roofline,
         "kernels": kernels,
         "phased_ms_per_step": statistics.mean(r["phased_ms"]),
+        "weights": ("tiled by moe_prepare_weights (once, untimed)" if tiled_weights(args, cfg)
+                    else "row-major"),
         "e2e": {"value": aggregate_tokens_per_s(cfg.n, args.steps, world, e2e_total), "unit": UNIT,
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
                 "d2h_bytes_per_step": y_h.numel() * y_h.element_size(),
@@ -620,22 +645,25 @@ def backward(args, torch, M, synth, cfg, dev, peaks, layer, L, x, v, st, stream,
     GEMMs, router backward, dx = the router term fused with the permute
     backward), L2 flushed before each step."""
     n, H, I, E, K = cfg.n, cfg.H, cfg.I, cfg.E, cfg.K
+    # the backward reads row-major weights (the forward may have run on tiles)
+    w13, w2 = L.get("w13_row", L["w13"]), L.get("w2_row", L["w2"])
+    desc = M.desc_for(cfg)
     nK = n * K
     f32, bf = torch.float32, torch.bfloat16
     g = torch.Generator(device=dev)
     g.manual_seed(synth.sub_seed(cfg.seed, "dy"))
     dy = torch.randn((n, H), generator=g, device=dev).to(bf)
     yp = torch.empty((nK, H), dtype=bf, device=dev)  # unweighted Y rows
-    M.moe_expert_gemm2(layer.desc, v["h"], L["w2"], v["offsets"], yp, 0, st, stream)
+    M.moe_expert_gemm2(desc, v["h"], w2, v["offsets"], yp, 0, st, stream)
     dx = torch.empty_like(x)
     dwg = torch.empty((H, E), dtype=f32, device=dev)
     dbias = torch.empty(E, dtype=f32, device=dev)
     dw13 = torch.empty((E, H, 2 * I), dtype=f32, device=dev)
     dw2 = torch.empty((E, I, H), dtype=f32, device=dev)
-    ws = torch.empty(M.moe_backward_workspace_size(layer.desc), dtype=torch.uint8, device=dev)
+    ws = torch.empty(M.moe_backward_workspace_size(desc), dtype=torch.uint8, device=dev)
 
     def step():
-        M.moe_backward(layer.desc, x, L["w_gate"], L["w13"], L["w2"], dy, v["logits"],
+        M.moe_backward(desc, x, L["w_gate"], w13, w2, dy, v["logits"],
                        v["topk_idx"], v["topk_w"], v["offsets"], v["inv_perm"], v["x_perm"],
                        v["h"], yp, dx, dwg, dbias, dw13, dw2, ws, st, stream)
     T.measure(step, 3)
@@ -655,7 +683,9 @@ def domino(args, torch, M, synth, cfg, dev, peaks):
     hide ratio, strict and over the overlap-eligible phases."""
     L = synth.make_layer(cfg, dev)
     xs = synth.make_micro_batches(cfg, dev)
-    desc = M.desc_for(cfg)
+    desc = M.desc_for(cfg, tiled=tiled_weights(args, cfg))
+    if tiled_weights(args, cfg):
+        L["w13"], L["w2"] = M.moe_prepare_weights(M.desc_for(cfg), L["w13"], L["w2"])
     layer = M.MoELayer(desc, L["w_gate"], L["bias"], L["w13"], L["w2"], num_mb=2)
     ys = [torch.empty_like(x) for x in xs]
     sc, sd = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)

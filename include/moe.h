@@ -75,6 +75,17 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 
+/*
+ * Layout of the expert weights w13 (E,H,2I) and w2 (E,I,H) that the expert
+ * entry points read.
+ *   MOE_WEIGHTS_ROW_MAJOR: as stored by the caller, row-major (the layout of
+ *     the pages' code: W13[e] is H x 2I with the gate columns first).
+ *   MOE_WEIGHTS_TILED: the output of moe_prepare_weights -- the same values
+ *     regrouped into contiguous 64 x 64 tiles (bf16 layers only; not accepted
+ *     by moe_backward).  Results are bitwise those of the row-major layout.
+ */
+typedef enum { MOE_WEIGHTS_ROW_MAJOR = 0, MOE_WEIGHTS_TILED = 1 } moe_weight_layout_t;
+
 typedef struct {
   int32_t n;              /* tokens (may be 0) */
   int32_t H;              /* hidden size */
@@ -83,6 +94,7 @@ typedef struct {
   int32_t K;              /* experts per token */
   int32_t dtype;          /* moe_dtype_t */
   int32_t norm_topk_prob; /* nonzero: divide the K weights by their sum */
+  int32_t weight_layout;  /* moe_weight_layout_t of w13 and w2 */
 } moe_layer_desc_t;
 
 /* Library version string and a human-readable name of a status code. */
@@ -162,6 +174,19 @@ moe_status_t moe_dispatch_layout_noalloc(const moe_layer_desc_t *desc, const int
  */
 moe_status_t moe_permute(const moe_layer_desc_t *desc, const void *x, const int32_t *perm,
                          void *x_perm, int32_t *status_word, moe_stream_t stream);
+
+/*
+ * The same permute in scatter form: x_perm[inv_perm[t*K + k]] = x[t] for
+ * every token t and slot k (inv_perm from moe_dispatch_layout).  Each x row
+ * is read once and written to its K rows, so x leaves DRAM once whatever the
+ * L2 holds (the gather form re-reads each x row K times and relies on the L2
+ * for the re-reads).  x_perm is bitwise equal to moe_permute's.  An inv_perm
+ * entry outside [0, n*K) is skipped and sets MOE_DEV_BAD_LAYOUT (status_word
+ * may be NULL); the row it would have written is left as it was.
+ */
+moe_status_t moe_permute_scatter(const moe_layer_desc_t *desc, const void *x,
+                                 const int32_t *inv_perm, void *x_perm, int32_t *status_word,
+                                 moe_stream_t stream);
 
 /*
  * Grouped SwiGLU experts: Algorithm 2 steps 8-9 for every expert with a
@@ -372,6 +397,38 @@ moe_status_t moe_forward_host(const moe_layer_desc_t *desc, const void *x_host,
                               const void *w2, void *y_host, void *ws, size_t ws_bytes,
                               long long call, int32_t *status_word, moe_stream_t compute,
                               moe_stream_t copy_in, moe_stream_t copy_out);
+
+/*
+ * One-time weight transform (untimed, before the layers run; the counterpart
+ * of the weight pre-transform the pages describe for DeepGEMM's Mega MoE
+ * kernel, "大模型系统中的通算融合" §4.4).  Writes w13 and w2 (row-major, bf16)
+ * in MOE_WEIGHTS_TILED layout: each 64 x 64 block (64 rows of k, 64 columns)
+ * of every expert's matrix becomes one contiguous 8 KB run, ordered by
+ * expert, then row block, then column block:
+ *   w13_tiled[((e*(H/64) + kb)*(2I/64) + nb)*4096 + r*64 + c]
+ *     = w13[e][64 kb + r][64 nb + c]          (and likewise w2 with I, H)
+ * so every tile the grouped GEMMs load is one contiguous DRAM run instead of
+ * 64 runs of 128 bytes a matrix row apart.  w13_tiled and w2_tiled have the
+ * sizes of w13 and w2 and must not overlap them.  desc: bf16, H % 64 == 0,
+ * I % 128 == 0 (weight_layout is ignored).  Enqueued on `stream`.
+ */
+moe_status_t moe_prepare_weights(const moe_layer_desc_t *desc, const void *w13, const void *w2,
+                                 void *w13_tiled, void *w2_tiled, moe_stream_t stream);
+
+/*
+ * Test control for the device timeout path (failure detection without a
+ * fault): the number of SM clock cycles a pipeline wait of the tensor-core
+ * grouped GEMMs (moe_expert_gemm1_swiglu, moe_expert_gemm2,
+ * moe_expert_gemm2_weighted, moe_expert_gemm1_swiglu_gather, the forward and
+ * moe_backward's GEMMs) and weight-gradient GEMMs waits before it gives up.
+ * A wait that gives up ORs MOE_DEV_TIMEOUT into the status word; every role
+ * of the CTA then stops, waits (with the full limit) for the copies and MMAs
+ * it has in flight, frees its tensor memory and leaves, so the context stays
+ * usable.  0 restores the default (2^31 cycles, about a second at 2 GHz).
+ * Applies to launches enqueued after the call, from any host thread.
+ * Returns MOE_ERR_INVALID_ARG for a negative value.
+ */
+moe_status_t moe_set_pipeline_wait_limit(long long cycles);
 
 /*
  * Blocks until `stream` is idle, then reads *status_word and maps it to

@@ -214,3 +214,32 @@ def test_backward_workspace_and_argument_checks(lib):
     assert call(wsp=ctypes.c_void_p((1 << 20) + 16)) == 1    # ws not 256-byte aligned
     assert call(dx=ctypes.c_void_p((1 << 12) + 8)) == 1      # dx not 16-byte aligned
     assert call(nbytes=need - 1) == 3                        # MOE_ERR_WORKSPACE
+
+
+@needs_nvcc
+def test_pipeline_wait_limit_control(lib):
+    # host-only: a negative limit is rejected, 0 (the default) and a positive
+    # limit are accepted; no launch happens
+    assert lib.moe_set_pipeline_wait_limit(-1) == 1
+    assert lib.moe_set_pipeline_wait_limit(1000) == 0
+    assert lib.moe_set_pipeline_wait_limit(0) == 0
+
+
+@needs_nvcc
+def test_tiled_weights_rejected_where_unsupported(lib):
+    import top_routing_dispatch_gb300 as M
+    # float32 layers and the backward read row-major weights only
+    d = M.make_desc(16, 64, 32, 4, 2, "f32", True, tiled=True)
+    assert lib.moe_grouped_swiglu(ctypes.byref(d), None, None, None, None, None, None, 0, None,
+                                  None) == 2
+    d = M.make_desc(16, 256, 128, 8, 2, "bf16", True, tiled=True)
+    assert lib.moe_backward(ctypes.byref(d), *([None] * 19), 0, None, None) == 2
+    # an unknown layout is an invalid descriptor
+    d = M.make_desc(16, 256, 128, 8, 2, "bf16", True)
+    d.weight_layout = 7
+    assert lib.moe_workspace_size(ctypes.byref(d)) == 0
+    # moe_prepare_weights needs bf16 and the GEMM's shape rules
+    d = M.make_desc(16, 64, 32, 4, 2, "f32", True)
+    assert lib.moe_prepare_weights(ctypes.byref(d), None, None, None, None, None) == 2
+    d = M.make_desc(16, 256, 128, 8, 2, "bf16", True)
+    assert lib.moe_prepare_weights(ctypes.byref(d), None, None, None, None, None) == 1

@@ -96,6 +96,31 @@ def check_permute(run, sample_rows=None):
     assert np.array_equal(got, ref)
 
 
+def check_permute_scatter(run, sample_rows=None):
+    """The scatter form (x read once, written to the K rows inv_perm names)
+    against the oracle's gather, exactly; the destination starts as all-ones
+    bytes so a row the kernel misses cannot pass."""
+    import top_routing_dispatch_gb300 as M
+    xp = torch.full((run.cfg.nK, run.cfg.H), -1, dtype=torch.int16,
+                    device=run.dev).view(run.x.dtype) if run.x.dtype == torch.bfloat16 else \
+        torch.full((run.cfg.nK, run.cfg.H), float("nan"), dtype=run.x.dtype, device=run.dev)
+    st = torch.zeros(1, dtype=torch.int32, device=run.dev)
+    M.moe_permute_scatter(run.desc, run.x, run.view("inv_perm"), xp, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    perm = run.np("perm")
+    if sample_rows is None:
+        assert np.array_equal(f64(xp), O.permute(f64(run.x), perm, run.cfg.K))
+        return
+    r = np.asarray(sample_rows)
+    got = f64(xp[torch.as_tensor(r, device=xp.device)])
+    assert np.array_equal(got, O.permute(f64(run.x), perm[r], run.cfg.K))
+    # every row, against the gather form (itself checked against the oracle)
+    assert torch.equal(xp.view(torch.int16) if xp.dtype == torch.bfloat16 else xp,
+                       run_permute(run).view(torch.int16) if xp.dtype == torch.bfloat16
+                       else run_permute(run))
+
+
 def check_experts(run, sample_rows=None):
     """GPU h and the GEMM2 output against the oracle's SwiGLU: GEMM1 on the
     oracle's gather of x (Algorithm 2 step 7), GEMM2 on the GPU's (rounded) h.
@@ -216,6 +241,7 @@ def test_small_all_steps(cfg):
     check_router(run)
     check_layout(run)
     check_permute(run)
+    check_permute_scatter(run)
     check_experts(run)
     check_gather_fusion(run)
     check_unweighted_gemm2_and_combine(run)
@@ -231,6 +257,7 @@ def test_full_size(cfg):
     check_layout(run)
     rng = np.random.default_rng(0)
     check_permute(run, rng.choice(cfg.nK, size=4096, replace=False))
+    check_permute_scatter(run, rng.choice(cfg.nK, size=4096, replace=False))
     off = run.np("offsets")
     # rows at every expert-segment start/end and tile seams, plus random rows,
     # restricted to a few experts (the hottest, the coldest non-empty, random)

@@ -1,0 +1,50 @@
+"""The device timeout path of the tensor-core GEMMs, exercised without a GPU
+fault: the pipeline waits are given a limit of a few hundred cycles (far below
+the time a tile's first operands take to arrive), so they give up.  The call
+must report MOE_ERR_TIMEOUT through the status word, every CTA must leave
+cleanly (the drain waits keep their full limit), and the next call on the same
+device, with the default limit back, must compute the same result as before."""
+import pytest
+import torch
+
+from tests.gpu_helpers import Run
+from workloads import OLMOE
+
+pytestmark = pytest.mark.gpu
+
+MOE_ERR_TIMEOUT = 6
+
+
+def _gemm1(M, run, h, st):
+    v = run.view
+    M.moe_expert_gemm1_swiglu(run.desc, v("x_perm"), run.L["w13"], v("offsets"), h, 0, st)
+
+
+def test_pipeline_wait_timeout_reports_and_recovers():
+    import top_routing_dispatch_gb300 as M
+    run = Run(OLMOE, n=512)
+    assert run.status == 0
+    st = torch.zeros(1, dtype=torch.int32, device=run.dev)
+    ref = torch.empty_like(run.view("h"))
+    _gemm1(M, run, ref, st)
+    assert M.moe_check_status(st) == 0
+    try:
+        M.moe_set_pipeline_wait_limit(200)
+        h = torch.zeros_like(ref)
+        st.zero_()
+        _gemm1(M, run, h, st)
+        got = M.moe_check_status(st)
+    finally:
+        M.moe_set_pipeline_wait_limit(0)
+    assert got == MOE_ERR_TIMEOUT
+    # the context is usable and the default limit is back: same bits as before
+    st.zero_()
+    h2 = torch.empty_like(ref)
+    _gemm1(M, run, h2, st)
+    assert M.moe_check_status(st) == 0
+    assert torch.equal(h2.view(torch.int16), ref.view(torch.int16))
+    # and the whole layer still matches its first run
+    y = run.layer.forward([run.x])[0]
+    torch.cuda.synchronize()
+    assert int(run.layer.status.item()) == 0
+    assert torch.equal(y.view(torch.int16), run.y.view(torch.int16))

@@ -14,14 +14,16 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
 # C ABI symbols, in header order (tests check the library exports each one).
 SYMBOLS = (
     "moe_version", "moe_status_string", "moe_route_topk", "moe_layout_workspace_size",
-    "moe_dispatch_layout", "moe_dispatch_layout_noalloc", "moe_permute", "moe_grouped_swiglu", "moe_expert_gemm1_swiglu",
+    "moe_dispatch_layout", "moe_dispatch_layout_noalloc", "moe_permute", "moe_permute_scatter", "moe_grouped_swiglu", "moe_expert_gemm1_swiglu",
     "moe_expert_gemm1_swiglu_gather", "moe_expert_gemm2", "moe_combine",
     "moe_workspace_size", "moe_forward_launches", "moe_forward_microbatches", "moe_workspace_slot", "moe_check_status",
     "moe_host_workspace_size", "moe_forward_host", "moe_expert_gemm2_weighted",
     "moe_combine_slots", "moe_backward_workspace_size", "moe_backward",
+    "moe_set_pipeline_wait_limit", "moe_prepare_weights",
 )
 
 MOE_F32, MOE_BF16 = 0, 1
+MOE_WEIGHTS_ROW_MAJOR, MOE_WEIGHTS_TILED = 0, 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT",
           7: "MOE_ERR_BAD_LAYOUT"}
@@ -36,7 +38,7 @@ SLOT = dict(logits=0, topk_idx=1, topk_w=2, counts=3, offsets=4, perm=5, inv_per
 class LayerDesc(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("K", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("norm_topk_prob", ctypes.c_int32)]
+                ("norm_topk_prob", ctypes.c_int32), ("weight_layout", ctypes.c_int32)]
 
 
 _vp = ctypes.c_void_p
@@ -55,6 +57,7 @@ def _declare(lib):
                                       ctypes.c_size_t, _vp]),
         "moe_dispatch_layout_noalloc": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
         "moe_permute": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp]),
+        "moe_permute_scatter": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp]),
         "moe_grouped_swiglu": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                      _vp, _vp]),
         "moe_expert_gemm1_swiglu": (_st, [_desc_p, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp]),
@@ -68,6 +71,8 @@ def _declare(lib):
                                            ctypes.c_int, _vp, _vp, _vp]),
         "moe_workspace_slot": (_vp, [_desc_p, _vp, ctypes.c_int, ctypes.c_int]),
         "moe_check_status": (_st, [_vp, _vp]),
+        "moe_set_pipeline_wait_limit": (_st, [ctypes.c_longlong]),
+        "moe_prepare_weights": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp]),
         "moe_host_workspace_size": (ctypes.c_size_t, [_desc_p]),
         "moe_expert_gemm2_weighted": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                             _vp, _vp]),

@@ -42,18 +42,31 @@ def _stream(s):
     return ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
 
 
-def make_desc(n, H, I, E, K, dtype, norm_topk_prob) -> LayerDesc:
+def make_desc(n, H, I, E, K, dtype, norm_topk_prob, tiled=False) -> LayerDesc:
+    """tiled: the expert weights passed to the expert entry points are the
+    output of moe_prepare_weights (MOE_WEIGHTS_TILED)."""
     if isinstance(dtype, torch.dtype):
         dtype = _DT[dtype]
     elif isinstance(dtype, str):
         dtype = {"f32": MOE_F32, "bf16": MOE_BF16}[dtype]
-    return LayerDesc(int(n), int(H), int(I), int(E), int(K), int(dtype), int(bool(norm_topk_prob)))
+    return LayerDesc(int(n), int(H), int(I), int(E), int(K), int(dtype), int(bool(norm_topk_prob)),
+                     int(bool(tiled)))
 
 
-def desc_for(cfg, n=None) -> LayerDesc:
+def desc_for(cfg, n=None, tiled=False) -> LayerDesc:
     """LayerDesc of a workload config (anything with n, H, I, E, K, dtype, norm_topk_prob)."""
     return make_desc(cfg.n if n is None else n, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype,
-                     cfg.norm_topk_prob)
+                     cfg.norm_topk_prob, tiled)
+
+
+def moe_prepare_weights(desc, w13, w2, w13_tiled=None, w2_tiled=None, stream=None):
+    """w13 and w2 regrouped into contiguous 64 x 64 tiles (MOE_WEIGHTS_TILED);
+    returns (w13_tiled, w2_tiled), allocated here when not given."""
+    w13_tiled = torch.empty_like(w13) if w13_tiled is None else w13_tiled
+    w2_tiled = torch.empty_like(w2) if w2_tiled is None else w2_tiled
+    _check(_lib.load().moe_prepare_weights(ctypes.byref(desc), _p(w13), _p(w2), _p(w13_tiled),
+                                           _p(w2_tiled), _stream(stream)), "moe_prepare_weights")
+    return w13_tiled, w2_tiled
 
 
 def torch_dtype(desc: LayerDesc):
@@ -93,6 +106,13 @@ def moe_dispatch_layout_noalloc(desc, topk_idx, counts, offsets, perm, inv_perm,
 def moe_permute(desc, x, perm, x_perm, status_word=None, stream=None):
     _check(_lib.load().moe_permute(ctypes.byref(desc), _p(x), _p(perm), _p(x_perm),
                                    _p(status_word), _stream(stream)), "moe_permute")
+
+
+def moe_permute_scatter(desc, x, inv_perm, x_perm, status_word=None, stream=None):
+    """x_perm[inv_perm[t*K + k]] = x[t]: the permute with each x row read once."""
+    _check(_lib.load().moe_permute_scatter(ctypes.byref(desc), _p(x), _p(inv_perm), _p(x_perm),
+                                           _p(status_word), _stream(stream)),
+           "moe_permute_scatter")
 
 
 def moe_grouped_swiglu(desc, x_perm, w13, w2, offsets, h, y_perm, sm_reserve=0, status_word=None,
@@ -184,6 +204,12 @@ def moe_workspace_slot(desc, ws, mb, which) -> int:
     if not p:
         raise ValueError("bad workspace slot request")
     return int(p)
+
+
+def moe_set_pipeline_wait_limit(cycles):
+    """Test control: cycles a tensor-core GEMM pipeline wait waits before it
+    gives up with MOE_ERR_TIMEOUT (0: the default, about a second)."""
+    _check(_lib.load().moe_set_pipeline_wait_limit(int(cycles)), "moe_set_pipeline_wait_limit")
 
 
 def moe_check_status(status_word, stream=None) -> int:

@@ -32,6 +32,7 @@ struct Desc {
   int n, H, I, E, K;
   bool bf16;
   bool norm;
+  bool tiled;  // expert weights in MOE_WEIGHTS_TILED layout
   long long nK() const { return (long long)n * K; }
 };
 
@@ -65,6 +66,10 @@ cudaError_t launch_layout(const Desc &d, const int32_t *topk_idx, int32_t *count
 // ---- permute_combine.cu
 cudaError_t launch_permute(const Desc &d, const void *x, const int32_t *perm, void *x_perm,
                            int32_t *status, cudaStream_t s, bool guest = false);
+// x_perm[inv_perm[t*K + k]] = x[t]: x read once (bitwise equal to launch_permute)
+cudaError_t launch_permute_scatter(const Desc &d, const void *x, const int32_t *inv_perm,
+                                   void *x_perm, int32_t *status, cudaStream_t s,
+                                   bool guest = false);
 cudaError_t launch_combine(const Desc &d, const void *y_perm, const float *topk_w,
                            const int32_t *inv_perm, void *y, int32_t *status, cudaStream_t s,
                            bool guest = false);
@@ -126,8 +131,16 @@ inline cudaError_t launch_experts(const Desc &d, const void *x_perm, const void 
                 : launch_gemm2_simt(d, h, w2, offsets, y_perm, status, s);
 }
 
+// prepare.cu: w13 (E,H,2I) and w2 (E,I,H) into 64 x 64 tiles (MOE_WEIGHTS_TILED)
+cudaError_t launch_prepare_weights(const Desc &d, const void *w13, const void *w2, void *w13t,
+                                   void *w2t, cudaStream_t s);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// Cycles a pipeline wait of the tcgen05 GEMM kernels waits before it gives up
+// (moe_set_pipeline_wait_limit; default about a second).
+long long pipeline_wait_limit();
 
 }  // namespace moe
 

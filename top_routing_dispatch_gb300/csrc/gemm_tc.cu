@@ -74,14 +74,17 @@ constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/true);
 constexpr uint32_t IDESC_KB = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/false);
 
+// A pipeline wait: gives up after `limit` cycles (setting the abort flag and
+// MOE_DEV_TIMEOUT), or at once when another role has given up.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
-                                              volatile int *abort_flag, int32_t *status) {
+                                              volatile int *abort_flag, int32_t *status,
+                                              long long limit) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > ptx::kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       flag_status(status, MOE_DEV_TIMEOUT);
       return false;
@@ -187,7 +190,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                            const int32_t *__restrict__ perm, int Kslots,
                            const __nv_bfloat16 *__restrict__ xg,
                            const float *__restrict__ tw,
-                           const __nv_bfloat16 *__restrict__ aux) {
+                           const __nv_bfloat16 *__restrict__ aux, long long wait_limit,
+                           int b_nb) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -258,7 +262,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         const TileInfo ti = decode_tile(st, t, n_tiles, E);
         bool stop = false;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!wait_or_abort(&st.empty[stage], phase ^ 1u, abort_flag, status)) {
+          if (!wait_or_abort(&st.empty[stage], phase ^ 1u, abort_flag, status, wait_limit)) {
             stop = true;
             break;
           }
@@ -277,8 +281,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                 ncol = (q < 2 ? 0 : I) + ti.nt * 128 + (q & 1) * 64;
               else
                 ncol = ti.nt * UMMA_N + q * 64;
-              ptx::tma_load_3d(smemB + stage * B_STAGE_BYTES + q * B_BOX_BYTES, &tmB,
-                               &st.full[stage], ncol, kb * BK, ti.e);
+              uint8_t *dst = smemB + stage * B_STAGE_BYTES + q * B_BOX_BYTES;
+              if (b_nb > 0)  // tiled weights: the 64 x 64 tile is one contiguous run
+                ptx::tma_load_2d(dst, &tmB, &st.full[stage], 0,
+                                 ((ti.e * KB + kb) * b_nb + (ncol >> 6)) * 64);
+              else
+                ptx::tma_load_3d(dst, &tmB, &st.full[stage], ncol, kb * BK, ti.e);
             }
           }
           used |= 1u << stage;
@@ -301,12 +309,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        if (!wait_or_abort(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status)) break;
+        if (!wait_or_abort(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status, wait_limit)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * UMMA_N);
         bool stop = false;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!wait_or_abort(&st.full[stage], phase, abort_flag, status)) {
+          if (!wait_or_abort(&st.full[stage], phase, abort_flag, status, wait_limit)) {
             stop = true;
             break;
           }
@@ -350,7 +358,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const TileInfo ti = decode_tile(st, t, n_tiles, E);
-      if (!wait_or_abort(&st.tfull[acc], acc_phase, abort_flag, status)) break;
+      if (!wait_or_abort(&st.tfull[acc], acc_phase, abort_flag, status, wait_limit)) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + (uint32_t)(acc * UMMA_N) + ((uint32_t)(q * 32) << 16);
       // rows of this warp's 32-row slice that belong to the tile's expert
@@ -489,7 +497,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       bool stop = false;
       for (int kb = 0; kb < KB; ++kb) {
         int ok = 1;
-        if (lane == 0) ok = wait_or_abort(&st.empty[stage], phase ^ 1u, abort_flag, status);
+        if (lane == 0) ok = wait_or_abort(&st.empty[stage], phase ^ 1u, abort_flag, status, wait_limit);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           stop = true;
@@ -570,6 +578,21 @@ bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uin
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// B operand map of the expert weights w (E matrices of rows x cols, bf16) for
+// 64 x 64 boxes: a 3-D map over the row-major matrices, or, for tiled weights
+// (moe_prepare_weights), a 2-D map over the contiguous 64 x 64 tiles (64
+// columns, one 64-row box per tile).  *b_nb: tiles per tile row (cols / 64)
+// for tiled weights, 0 otherwise (the kernel's b_nb argument).
+bool weight_map(CUtensorMap *m, const void *w, const Desc &d, uint64_t rows, uint64_t cols,
+                int *b_nb) {
+  if (d.tiled) {
+    *b_nb = (int)(cols / 64);
+    return make_map_2d(m, w, 64, (uint64_t)d.E * rows * (cols / 64), 64, BK);
+  }
+  *b_nb = 0;
+  return make_map_3d(m, w, cols, rows, d.E, 64, BK);
+}
+
 template <int MODE>
 cudaError_t set_smem_attr() {
   static int done[64] = {0};
@@ -596,15 +619,15 @@ cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
   CUtensorMap mA, mB;
-  if (!make_map_2d(&mA, x_perm, d.H, nK, BK, BM) ||
-      !make_map_3d(&mB, w13, 2ull * d.I, d.H, d.E, 64, BK))
+  int BNB = 0;
+  if (!make_map_2d(&mA, x_perm, d.H, nK, BK, BM) || !weight_map(&mB, w13, d, d.H, 2ull * d.I, &BNB))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_attr<1>();
   if (e != cudaSuccess) return e;
   return launch_pdl(grouped_gemm_tc_kernel<1>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
                     SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
                     reinterpret_cast<__nv_bfloat16 *>(h), status, nullptr, 0, nullptr, nullptr,
-                    nullptr);
+                    nullptr, pipeline_wait_limit(), BNB);
 }
 
 cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *perm,
@@ -613,13 +636,14 @@ cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
   CUtensorMap mB;  // A is gathered with cp.async: no tensor map for x
-  if (!make_map_3d(&mB, w13, 2ull * d.I, d.H, d.E, 64, BK)) return cudaErrorInvalidValue;
+  int BNB = 0;
+  if (!weight_map(&mB, w13, d, d.H, 2ull * d.I, &BNB)) return cudaErrorInvalidValue;
   cudaError_t e = set_smem_attr<3>();
   if (e != cudaSuccess) return e;
   return launch_pdl(grouped_gemm_tc_kernel<3>, dim3(gemm_grid(sm_reserve)), dim3(threads_for(3)),
                     SMEM_BYTES, s, mB, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
                     reinterpret_cast<__nv_bfloat16 *>(h), status, perm, d.K,
-                    reinterpret_cast<const __nv_bfloat16 *>(x), nullptr, nullptr);
+                    reinterpret_cast<const __nv_bfloat16 *>(x), nullptr, nullptr, pipeline_wait_limit(), BNB);
 }
 
 cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const int32_t *offsets,
@@ -627,14 +651,15 @@ cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const 
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
   CUtensorMap mA, mB;
-  if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !make_map_3d(&mB, w2, d.H, d.I, d.E, 64, BK))
+  int BNB = 0;
+  if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !weight_map(&mB, w2, d, d.I, d.H, &BNB))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_attr<2>();
   if (e != cudaSuccess) return e;
   return launch_pdl(grouped_gemm_tc_kernel<2>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
                     SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
                     reinterpret_cast<__nv_bfloat16 *>(y_perm), status, nullptr, 0, nullptr,
-                    nullptr, nullptr);
+                    nullptr, nullptr, pipeline_wait_limit(), BNB);
 }
 
 cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w2,
@@ -644,14 +669,15 @@ cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
   CUtensorMap mA, mB;
-  if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !make_map_3d(&mB, w2, d.H, d.I, d.E, 64, BK))
+  int BNB = 0;
+  if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !weight_map(&mB, w2, d, d.I, d.H, &BNB))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_attr<4>();
   if (e != cudaSuccess) return e;
   return launch_pdl(grouped_gemm_tc_kernel<4>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
                     SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
                     reinterpret_cast<__nv_bfloat16 *>(y_slot), status, perm, d.K, nullptr,
-                    topk_w, nullptr);
+                    topk_w, nullptr, pipeline_wait_limit(), BNB);
 }
 
 cudaError_t launch_gemm_dgrad_tc(const Desc &d, const void *a, const void *w, int Kdim, int Nout,
@@ -669,7 +695,7 @@ cudaError_t launch_gemm_dgrad_tc(const Desc &d, const void *a, const void *w, in
   return launch_pdl(grouped_gemm_tc_kernel<5>, dim3(gemm_grid(0)), dim3(threads_for(5)),
                     SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, Kdim, 0, Nout,
                     reinterpret_cast<__nv_bfloat16 *>(out), status, nullptr, 0, nullptr, nullptr,
-                    nullptr);
+                    nullptr, pipeline_wait_limit(), 0);
 }
 
 cudaError_t launch_gemm1_swiglu_bwd_tc(const Desc &d, const void *x_perm, const void *w13,
@@ -686,7 +712,7 @@ cudaError_t launch_gemm1_swiglu_bwd_tc(const Desc &d, const void *x_perm, const 
   return launch_pdl(grouped_gemm_tc_kernel<6>, dim3(gemm_grid(0)), dim3(threads_for(6)),
                     SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, 2 * d.I,
                     reinterpret_cast<__nv_bfloat16 *>(dgu), status, nullptr, 0, nullptr, nullptr,
-                    reinterpret_cast<const __nv_bfloat16 *>(dh));
+                    reinterpret_cast<const __nv_bfloat16 *>(dh), pipeline_wait_limit(), 0);
 }
 
 }  // namespace moe

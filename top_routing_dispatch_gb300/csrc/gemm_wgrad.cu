@@ -62,13 +62,13 @@ static_assert(W_SMEM <= 232448, "wgrad shared memory above the per-block limit")
 constexpr uint32_t W_IDESC = ptx::idesc_bf16_f32(WM, WN, /*a_mn=*/true, /*b_mn=*/true);
 
 __device__ __forceinline__ bool w_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                       int32_t *status) {
+                                       int32_t *status, long long limit) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > ptx::kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       flag_status(status, MOE_DEV_TIMEOUT);
       return false;
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmBt,
                     const __grid_constant__ CUtensorMap tmOut,
                     const int32_t *__restrict__ offsets, int E, int nK, int M, int N,
-                    int32_t *status) {
+                    int32_t *status, long long wait_limit) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       for (int g = cid; g < total && !stop; g += ncl) {
         const WTile w = w_decode(st, g, mt, nt);
         for (int kb = 0; kb < w.nkb; ++kb) {
-          if (!w_wait(&st.empty[stage], phase ^ 1u, abort_flag, status)) {
+          if (!w_wait(&st.empty[stage], phase ^ 1u, abort_flag, status, wait_limit)) {
             stop = true;
             break;
           }
@@ -225,12 +225,12 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       uint32_t phase = 0, acc_phase = 0;
       for (int g = cid; g < total; g += ncl) {
         const WTile w = w_decode(st, g, mt, nt);
-        if (!w_wait(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status)) break;
+        if (!w_wait(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status, wait_limit)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * WN);
         bool stop = false;
         for (int kb = 0; kb < w.nkb; ++kb) {
-          if (!w_wait(&st.full[stage], phase, abort_flag, status)) {
+          if (!w_wait(&st.full[stage], phase, abort_flag, status, wait_limit)) {
             stop = true;
             break;
           }
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     uint32_t acc_phase = 0;
     for (int g = cid; g < total; g += ncl) {
       const WTile w = w_decode(st, g, mt, nt);
-      if (!w_wait(&st.tfull[acc], acc_phase, abort_flag, status)) break;
+      if (!w_wait(&st.tfull[acc], acc_phase, abort_flag, status, wait_limit)) break;
       ptx::tc_fence_after();
       const uint32_t tb = tmem + (uint32_t)(acc * WN) + ((uint32_t)(q * 32) << 16);
       // each 32-column chunk of this warp's 32 rows goes through a swizzled
@@ -420,7 +420,7 @@ cudaError_t wgrad_launch(const WgradArgs &p, cudaStream_t s) {
   const int sms = device_sm_count();
   return launch_pdl(wgrad_tc_kernel, dim3((unsigned)(units < sms ? units : sms)), dim3(W_THREADS),
                     W_SMEM, s, p.mA, p.mB, p.mA16, p.mB16, p.mAt, p.mBt, p.mOut, p.offsets, p.E,
-                    p.nK, p.M, p.N, p.status);
+                    p.nK, p.M, p.N, p.status, pipeline_wait_limit());
 }
 
 size_t wgrad_tail_bytes(const Desc &d, int M, int N) {

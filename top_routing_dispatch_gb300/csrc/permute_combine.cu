@@ -69,6 +69,54 @@ __global__ void __launch_bounds__(PT) permute_kernel(const uint4 *__restrict__ x
   }
 }
 
+// Scatter permute: warp w copies the tokens [w*n/W, (w+1)*n/W); for each
+// token the K destination rows come from inv_perm (lane k holds slot k's),
+// PU 16-byte vectors per lane are loaded once and stored to all K rows
+// (streaming stores, as the gather form).
+template <bool GUEST>
+__global__ void __launch_bounds__(PT) permute_scatter_kernel(const uint4 *__restrict__ x,
+                                                             const int32_t *__restrict__ inv,
+                                                             uint4 *__restrict__ xp, int n,
+                                                             int K, int V, long long nK,
+                                                             int32_t *status) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const long long W = ((long long)gridDim.x * PT) >> 5;
+  const long long wid = ((long long)blockIdx.x * PT + threadIdx.x) >> 5;
+  const long long t0 = wid * n / W, t1 = (wid + 1) * n / W;
+  bool bad = false;
+  for (long long t = t0; t < t1; ++t) {
+    int dst = 0;
+    bool ok = true;
+    if (lane < K) {
+      dst = __ldg(inv + t * K + lane);
+      ok = dst >= 0 && (long long)dst < nK;
+      bad |= !ok;
+    }
+    const unsigned okm = __ballot_sync(0xffffffffu, ok);
+    const uint4 *src = x + (size_t)t * V;
+    for (int v0 = 0; v0 < V; v0 += 32 * PU) {
+      uint4 buf[PU];
+#pragma unroll
+      for (int u = 0; u < PU; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < V) buf[u] = __ldcs(src + v);  // read once: no need to keep it in L2
+      }
+      for (int k = 0; k < K; ++k) {
+        const int r = __shfl_sync(0xffffffffu, dst, k);
+        if (!(okm >> k & 1u)) continue;  // warp-uniform
+        uint4 *d = xp + (size_t)r * V;
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < V) __stcs(d + v, buf[u]);
+        }
+      }
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(status, MOE_DEV_BAD_LAYOUT);
+}
+
 __device__ __forceinline__ void acc_vec(float (&a)[8], uint4 v, float w, bool bf16) {
   if (bf16) {
     const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&v);
@@ -234,6 +282,19 @@ cudaError_t launch_permute(const Desc &d, const void *x, const int32_t *perm, vo
                   dim3((int)(want < res ? want : res)), dim3(PT), 0, s,
                   reinterpret_cast<const uint4 *>(x), perm, reinterpret_cast<uint4 *>(x_perm), nK,
                   d.K, V, status);
+}
+
+cudaError_t launch_permute_scatter(const Desc &d, const void *x, const int32_t *inv_perm,
+                                   void *x_perm, int32_t *status, cudaStream_t s, bool guest) {
+  if (d.nK() == 0) return cudaSuccess;
+  const int V = (int)((size_t)d.H * elem_bytes(d) / 16);
+  const long long res = guest ? resident_grid<permute_scatter_kernel<true>, true>()
+                              : resident_grid<permute_scatter_kernel<false>, false>();
+  const long long want = ((long long)d.n + (PT / 32) - 1) / (PT / 32);
+  return launch_k(guest, guest ? permute_scatter_kernel<true> : permute_scatter_kernel<false>,
+                  dim3((int)(want < res ? want : res)), dim3(PT), 0, s,
+                  reinterpret_cast<const uint4 *>(x), inv_perm, reinterpret_cast<uint4 *>(x_perm),
+                  d.n, d.K, V, d.nK(), status);
 }
 
 cudaError_t launch_combine_slots(const Desc &d, const void *y_slot, void *y, cudaStream_t s,

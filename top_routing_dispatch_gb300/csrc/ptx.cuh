@@ -55,7 +55,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// About 2^31 SM cycles (~1 s at 2 GHz) before a wait gives up.
+// About 2^31 SM cycles (~1 s at 2 GHz) before a wait gives up: the limit of
+// the drain waits (a CTA waiting for its own copies and MMAs in flight before
+// it leaves) and the default of the pipeline waits, which a launch can lower
+// (see pipeline_wait_limit).
 constexpr long long kWaitLimitCycles = 1ll << 31;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
