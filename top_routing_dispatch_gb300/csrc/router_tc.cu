@@ -668,11 +668,13 @@ cudaError_t launch_router_tc(const Desc &d, const void *x, const void *w_gate, c
   uint32_t cols = 32;
   while (cols < (uint32_t)d.E) cols <<= 1;
   const int n_tiles = (d.n + RT_BM - 1) / RT_BM;
-  const int sms = device_sm_count();
   const uint32_t idesc = ptx::idesc_bf16_f32(RT_BM, d.E, false, true);
   const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
   const __nv_bfloat16 *wb = reinterpret_cast<const __nv_bfloat16 *>(w_gate);
-  const int rgrid = d.n < 2 * sms ? d.n : 2 * sms;
+  // one CTA per token: a CTA whose token is not flagged leaves after one load,
+  // and the flagged tokens (8 % at the DeepSeek-V3 size) are rescored in
+  // parallel across the SMs instead of several after one another in one CTA
+  const int rgrid = d.n;
   const float tau_rel = tie_margin_tc(d.H);
   // the tile kernel (clusters of RC CTAs), then the exact rescoring of the
   // tokens it flagged
