@@ -257,6 +257,7 @@ def algorithmic(cfg, counts=None):
         "layout": {"flop": 0, "bytes": 2 * nK * 4 + 2 * nK * 4 + (2 * E + 1) * 4},
         "permute": {"flop": 0, "bytes": n * H * b + nK * H * b + nK * 4},
         "permute_scatter": {"flop": 0, "bytes": n * H * b + nK * H * b + nK * 4},
+        "permute_gather": {"flop": 0, "bytes": n * H * b + nK * H * b + nK * 4},
         "gemm1": {"flop": 4 * nK * H * I, "bytes": nK * H * b + used * H * 2 * I * b + nK * I * b},
         # GEMM1 with the permute fused: x once (rows are re-read from L2),
         # perm, the used experts' W13, h
@@ -329,15 +330,28 @@ class Timer:
         return ts
 
 
+# x above this size is permuted in scatter form by the forward (the library's
+# choice in moe_forward_microbatches, mirrored here to label the rows)
+SCATTER_PERMUTE_BYTES = 32 << 20
+
+
+def scatter_permute(cfg):
+    return cfg.n * cfg.H * (2 if cfg.dtype == "bf16" else 4) > SCATTER_PERMUTE_BYTES
+
+
 def kernel_rows(M, desc, cfg, x, y, L, v, st, lws, stream):
     """The step as one C-ABI call per row of the layer (the rows the forward
-    runs for this dtype)."""
+    runs for this dtype and size)."""
+    if scatter_permute(cfg):
+        permute = lambda: M.moe_permute_scatter(desc, x, v["inv_perm"], v["x_perm"], st, stream)
+    else:
+        permute = lambda: M.moe_permute(desc, x, v["perm"], v["x_perm"], st, stream)
     rows = [
         ("router", lambda: M.moe_route_topk(desc, x, L["w_gate"], L["bias"], v["topk_idx"],
                                             v["topk_w"], v["logits"], stream)),
         ("layout", lambda: M.moe_dispatch_layout(desc, v["topk_idx"], v["counts"], v["offsets"],
                                                  v["perm"], v["inv_perm"], st, lws, stream)),
-        ("permute", lambda: M.moe_permute(desc, x, v["perm"], v["x_perm"], st, stream)),
+        ("permute", permute),
         ("gemm1", lambda: M.moe_expert_gemm1_swiglu(desc, v["x_perm"], L["w13"], v["offsets"],
                                                     v["h"], 0, st, stream)),
     ]
@@ -370,7 +384,7 @@ def kernel_table(cfg, per_phase, per_phase_warm, counts, peaks, rows):
         k["frac_hbm"] = k["gbs"] / peaks["hbm_gbs"]
         if a["flop"]:
             k["tflops"] = a["flop"] / (ms * 1e-3) / 1e12
-        if name.startswith("gemm"):
+        if name.startswith("gemm") and cfg.dtype == "bf16":
             k["frac_bf16"] = k["tflops"] / peaks["bf16_tflops"]
         # the kernel's own roofline: the larger of its tensor time (bf16 GEMMs
         # and the bf16 router) and its HBM time, over the measured time
@@ -463,11 +477,17 @@ def measure_layer(args, torch, M, synth, cfg, dev, peaks, rank, steps, warmup, d
                       for i, (name, _) in enumerate(rows)}
     phased_ms = [s[0].elapsed_time(s[-1]) for s in evs]
     # entry points the step does not call, timed alone on the same layout:
-    # the scatter form of the permute (x read once)
+    # the other form of the permute (gather: x re-read K times; scatter: x
+    # read once)
     xp_alt = torch.empty_like(v["x_perm"])
-    scat = lambda: M.moe_permute_scatter(desc, x, v["inv_perm"], xp_alt, st, stream)
-    T.measure(scat, 3)
-    per_phase["permute_scatter"] = T.measure(scat, steps)
+    if scatter_permute(cfg):
+        name = "permute_gather"
+        other = lambda: M.moe_permute(desc, x, v["perm"], xp_alt, st, stream)
+    else:
+        name = "permute_scatter"
+        other = lambda: M.moe_permute_scatter(desc, x, v["inv_perm"], xp_alt, st, stream)
+    T.measure(other, 3)
+    per_phase[name] = T.measure(other, steps)
     status = M.moe_check_status(st, stream)
     return dict(L=L, x=x, y=y, desc=desc, layer=layer, v=v, st=st, stream=stream, T=T,
                 rows=rows, fwd_ms=fwd_ms, per_phase=per_phase, per_phase_warm=per_phase_warm,
@@ -490,6 +510,7 @@ def extra_workloads(args, torch, M, synth, dev, peaks, rank):
         kern = kernel_table(cfg, r["per_phase"], r["per_phase_warm"], counts, peaks, r["rows"])
         ms = statistics.mean(r["fwd_ms"])
         out[name] = {"tokens_per_s": round(cfg.n / (ms * 1e-3), 1), "ms_per_step": round(ms, 5),
+                     "permute_form": "scatter" if scatter_permute(cfg) else "gather",
                      "steps": len(r["fwd_ms"]), "device_status": r["status"],
                      "clocks": r["clocks"], "kernels": compact_kernels(kern)}
         del r
