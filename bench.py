@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--weights", choices=["tiled", "row"], default="tiled",
                     help="bf16 expert weights: tiled by moe_prepare_weights once, untimed "
                          "(default), or read row-major")
+    ap.add_argument("--gemm-pairs", choices=["on", "off"], default="on",
+                    help="forward grouped GEMMs on CTA pairs (cta_group::2, the default) or on "
+                         "single CTAs (same results)")
     ap.add_argument("--extra-workloads", default="olmoe_skew_bf16,dsv3_bf16,tiny_fp32",
                     help="other single-batch workloads timed after the headline (N=1 only); "
                          "empty to skip")
@@ -526,6 +529,7 @@ def run_ours(args, cfg):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    M.moe_set_gemm_pairs(args.gemm_pairs == "on")
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -623,6 +627,8 @@ def run_ours(args, cfg):
         "phased_ms_per_step": statistics.mean(r["phased_ms"]),
         "weights": ("tiled by moe_prepare_weights (once, untimed)" if tiled_weights(args, cfg)
                     else "row-major"),
+        "gemm_tiles": ("CTA pairs (cta_group::2), 256 x 256" if args.gemm_pairs == "on"
+                       else "single CTAs, 128 x 256"),
         "e2e": {"value": aggregate_tokens_per_s(cfg.n, args.steps, world, e2e_total), "unit": UNIT,
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
                 "d2h_bytes_per_step": y_h.numel() * y_h.element_size(),

@@ -19,7 +19,7 @@ SYMBOLS = (
     "moe_workspace_size", "moe_forward_launches", "moe_forward_microbatches", "moe_workspace_slot", "moe_check_status",
     "moe_host_workspace_size", "moe_forward_host", "moe_expert_gemm2_weighted",
     "moe_combine_slots", "moe_backward_workspace_size", "moe_backward",
-    "moe_set_pipeline_wait_limit", "moe_prepare_weights",
+    "moe_set_pipeline_wait_limit", "moe_prepare_weights", "moe_set_gemm_pairs",
 )
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -72,6 +72,7 @@ def _declare(lib):
         "moe_workspace_slot": (_vp, [_desc_p, _vp, ctypes.c_int, ctypes.c_int]),
         "moe_check_status": (_st, [_vp, _vp]),
         "moe_set_pipeline_wait_limit": (_st, [ctypes.c_longlong]),
+        "moe_set_gemm_pairs": (_st, [ctypes.c_int]),
         "moe_prepare_weights": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp]),
         "moe_host_workspace_size": (ctypes.c_size_t, [_desc_p]),
         "moe_expert_gemm2_weighted": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,

@@ -212,6 +212,12 @@ def moe_set_pipeline_wait_limit(cycles):
     _check(_lib.load().moe_set_pipeline_wait_limit(int(cycles)), "moe_set_pipeline_wait_limit")
 
 
+def moe_set_gemm_pairs(enable):
+    """Tuning control: run the forward grouped GEMMs on CTA pairs (True, the
+    default) or on single CTAs (False); the results are the same."""
+    _check(_lib.load().moe_set_gemm_pairs(1 if enable else 0), "moe_set_gemm_pairs")
+
+
 def moe_check_status(status_word, stream=None) -> int:
     """Synchronises `stream` and returns the mapped status code (0 = OK)."""
     return int(_lib.load().moe_check_status(_p(status_word), _stream(stream)))

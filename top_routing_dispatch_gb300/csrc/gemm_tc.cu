@@ -28,6 +28,7 @@
 // operand with 128-byte swizzle.  A is K-major with 128-byte swizzle.
 #include <cuda.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -36,11 +37,25 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BK = 64, UMMA_N = 256, UMMA_K = 16, STAGES = 4;
+constexpr int BM = 128, BK = 64, UMMA_N = 256, UMMA_K = 16;
 constexpr int A_STAGE_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;            // 8 KB: 64 n x 64 k
-constexpr int B_STAGE_BYTES = 4 * B_BOX_BYTES;      // 32 KB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int kMaxStages = 6;
+
+// Operand pipeline of one CTA.  Single CTAs: four stages of A (128 rows) and
+// all four B boxes (256 n).  CTA pairs (PAIR): the pair computes a 256-row x
+// 256-column tile with cta_group::2 MMAs; each CTA holds its own 128 A rows
+// and half of B (two boxes, 128 n), so six 32 KB stages fit in the same
+// shared memory.
+template <bool PAIR>
+struct Pipe {
+  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int B_BOXES = PAIR ? 2 : 4;
+  static constexpr int B_STAGE = B_BOXES * B_BOX_BYTES;
+  static constexpr int STAGE = A_STAGE_BYTES + B_STAGE;
+  static constexpr int TILE_ROWS = PAIR ? 2 * BM : BM;  // rows of an m-tile (whole pair)
+};
+static_assert(Pipe<true>::STAGES <= kMaxStages && Pipe<false>::STAGES <= kMaxStages, "");
 // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue; MODE 3 adds
 // warps 6-9, which gather the A rows with cp.async
 constexpr int NUM_THREADS = 192;
@@ -54,8 +69,8 @@ constexpr int TMEM_COLS = 512;                      // two 256-column accumulato
 constexpr int EPI_ROW_BYTES = 80, EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
 
 struct SmemTail {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -63,16 +78,24 @@ struct SmemTail {
   int abort_flag;
   int ok;
   int total_mtiles;
+  int own_issued[kMaxStages];   // PAIR: phases this CTA's producer loaded, per stage
+  int peer_issued[kMaxStages];  // PAIR (leader): the odd CTA's own_issued
   int off[kMaxE + 1];
   int tp[kMaxE + 1];  // first m-tile of each expert (exclusive prefix)
   alignas(16) uint8_t epi[4][EPI_WARP_BYTES];  // per epilogue warp staging
 };
 
-constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES +
-                              sizeof(SmemTail);
+template <bool PAIR>
+constexpr size_t smem_bytes() {
+  return 1024 /*alignment slack*/ + (size_t)Pipe<PAIR>::STAGES * Pipe<PAIR>::STAGE +
+         sizeof(SmemTail);
+}
+constexpr size_t SMEM_BYTES = smem_bytes<false>();
+static_assert(smem_bytes<true>() <= 227 * 1024, "pair pipeline exceeds shared memory");
 
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/true);
 constexpr uint32_t IDESC_KB = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/false);
+constexpr uint32_t IDESC_PAIR = ptx::idesc_bf16_f32(2 * BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/true);
 
 // A pipeline wait: gives up after `limit` cycles (setting the abort flag and
 // MOE_DEV_TIMEOUT), or at once when another role has given up.
@@ -96,7 +119,12 @@ struct TileInfo {
   int e, row0, rows, nt;
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const SmemTail &s, int t, int n_tiles, int E) {
+// Tile t: expert, first row and stored rows of this CTA's 128-row part
+// (PAIR: rank 0 takes rows [0, 128) of the pair's 256-row window, rank 1 rows
+// [128, 256); rows may be <= 0 when the segment ends in the first half).
+template <bool PAIR = false>
+__device__ __forceinline__ TileInfo decode_tile(const SmemTail &s, int t, int n_tiles, int E,
+                                                int rank = 0) {
   TileInfo ti;
   const int mt = t / n_tiles;
   ti.nt = t - mt * n_tiles;
@@ -109,7 +137,7 @@ __device__ __forceinline__ TileInfo decode_tile(const SmemTail &s, int t, int n_
       hi = mid;
   }
   ti.e = lo;
-  ti.row0 = s.off[lo] + (mt - s.tp[lo]) * BM;
+  ti.row0 = s.off[lo] + (mt - s.tp[lo]) * Pipe<PAIR>::TILE_ROWS + rank * BM;
   const int left = s.off[lo + 1] - ti.row0;
   ti.rows = left < BM ? left : BM;
   return ti;
@@ -181,7 +209,17 @@ __host__ __device__ constexpr bool kmajor_b(int mode) { return mode == 5; }
 //         a tile are read straight from x (row perm[r] / K) by four gather
 //         warps with 16-byte cp.async, written in the same 128-byte swizzled
 //         layout the TMA produces; no x_perm exists.
-template <int MODE>
+//
+// PAIR (modes 1, 2 and 4): clusters of two CTAs on two SMs compute 256-row x
+// 256-column tiles with cta_group::2 MMAs.  The even CTA ("leader") issues the
+// MMAs and owns the operand-full barriers: both CTAs' TMA copies complete on
+// them, and it expects both CTAs' bytes.  Its MMA commits arrive on the
+// operand-empty and accumulator-full barriers of both CTAs (multicast); both
+// CTAs' epilogue warps arrive on the leader's accumulator-empty barriers.
+// Each CTA drains the accumulator rows in its own TMEM.  Before the pair
+// leaves, the leader settles every stage whose two halves were not both
+// issued (a side that gave up early) and waits until every copy has landed.
+template <int MODE, bool PAIR = false>
 __global__ void __launch_bounds__(threads_for(MODE), 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -192,17 +230,27 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                            const float *__restrict__ tw,
                            const __nv_bfloat16 *__restrict__ aux, long long wait_limit,
                            int b_nb) {
+  static_assert(!PAIR || MODE == 1 || MODE == 2 || MODE == 4, "CTA pairs: forward modes only");
+  using P = Pipe<PAIR>;
+  constexpr int STAGES = P::STAGES;
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *smemA = smem;
-  uint8_t *smemB = smem + STAGES * A_STAGE_BYTES;
-  SmemTail &st = *reinterpret_cast<SmemTail *>(smem + STAGES * STAGE_BYTES);
+  // single CTAs: A stages, then B stages; PAIR: B stages first, so that every
+  // operand read of a stage stays inside the CTA's operand area
+  uint8_t *smemA = PAIR ? smem + STAGES * P::B_STAGE : smem;
+  uint8_t *smemB = PAIR ? smem : smem + STAGES * A_STAGE_BYTES;
+  SmemTail &st = *reinterpret_cast<SmemTail *>(smem + STAGES * P::STAGE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = gemm1_mode(MODE) ? I / 128 : (Nout + UMMA_N - 1) / UMMA_N;
   const int KB = Kdim / BK;
+  // PAIR: rank in the pair; tiles are dealt per pair
+  const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
+  const bool leader = rank == 0;
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -213,15 +261,21 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&st.tfull[a], 1);
-      ptx::mbar_init(&st.tempty[a], 4);
+      ptx::mbar_init(&st.tempty[a], PAIR ? 8 : 4);  // the epilogue warps (of both CTAs)
     }
     ptx::mbar_init(&st.drain, 1);
+    for (int s = 0; s < kMaxStages; ++s) st.own_issued[s] = st.peer_issued[s] = 0;
     st.abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
   for (int c = tid; c <= E; c += NUM_THREADS) st.off[c] = offsets[c];
-  __syncthreads();
+  // PAIR: both CTAs' barriers are initialised before either copies to or
+  // arrives on the other's
+  if constexpr (PAIR)
+    ptx::cluster_sync();
+  else
+    __syncthreads();
   if (tid == 0) {
     bool ok = st.off[0] == 0 && st.off[E] <= nK;
     int run = 0;
@@ -229,7 +283,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       const int len = st.off[e + 1] - st.off[e];
       ok = ok && len >= 0;
       st.tp[e] = run;
-      run += len > 0 ? (len + BM - 1) / BM : 0;
+      run += len > 0 ? (len + P::TILE_ROWS - 1) / P::TILE_ROWS : 0;
     }
     st.tp[E] = run;
     st.total_mtiles = run;
@@ -237,13 +291,19 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     if (!ok && blockIdx.x == 0) flag_status(status, MOE_DEV_BAD_LAYOUT);
   }
   __syncthreads();
+  // both CTAs of a pair read the same offsets, so they take the same exits
   if (!st.ok) return;
   const int total = st.total_mtiles * n_tiles;
-  if ((int)blockIdx.x >= total) return;
+  if (unit >= total) return;
 
   if (warp == 1) {
-    ptx::tmem_alloc(&st.tmem_base, TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(&st.tmem_base, TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(&st.tmem_base, TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -251,14 +311,65 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   const uint32_t tmem = st.tmem_base;
   volatile int *abort_flag = &st.abort_flag;
 
-  if (warp == 0) {
+  if (warp == 0 && PAIR) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmB);
+      // the leader's operand-full barriers, as shared::cluster addresses
+      const uint32_t full0 = ptx::mapa_shared(ptx::smem_u32(&st.full[0]), 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = unit; t < total; t += units) {
+        const TileInfo ti = decode_tile<true>(st, t, n_tiles, E, rank);
+        bool stop = false;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_or_abort(&st.empty[stage], phase ^ 1u, abort_flag, status, wait_limit)) {
+            stop = true;
+            break;
+          }
+          if (leader) ptx::mbar_arrive_expect_tx(&st.full[stage], 2 * P::STAGE);
+          const uint32_t bar = full0 + 8u * (uint32_t)stage;
+          // a part with no rows of the expert (segment ends in the first
+          // half) loads the expert's first rows: computed, never stored
+          ptx::tma_load_2d_pair(smemA + stage * A_STAGE_BYTES, &tmA, bar, kb * BK,
+                                ti.rows > 0 ? ti.row0 : st.off[ti.e]);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            // this CTA's half of the 256 B columns: GEMM1 gate (rank 0) or up
+            // (rank 1) columns of the 128 h columns; GEMM2 columns 128 * rank
+            const int q = 2 * rank + j;
+            const int ncol = gemm1_mode(MODE) ? (q < 2 ? 0 : I) + ti.nt * 128 + (q & 1) * 64
+                                              : ti.nt * UMMA_N + q * 64;
+            uint8_t *dst = smemB + stage * P::B_STAGE + j * B_BOX_BYTES;
+            if (b_nb > 0)
+              ptx::tma_load_2d_pair(dst, &tmB, bar, 0, ((ti.e * KB + kb) * b_nb + (ncol >> 6)) * 64);
+            else
+              ptx::tma_load_3d_pair(dst, &tmB, bar, ncol, kb * BK, ti.e);
+          }
+          ++st.own_issued[stage];
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (stop) break;
+      }
+      // copies still in flight are settled by the leader before the pair
+      // leaves: it needs the odd CTA's counts
+      if (!leader) {
+        const uint32_t dst0 = ptx::mapa_shared(ptx::smem_u32(&st.peer_issued[0]), 0);
+        for (int s2 = 0; s2 < STAGES; ++s2)
+          ptx::st_cluster_u32(dst0 + 4u * s2, (uint32_t)st.own_issued[s2]);
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t used = 0, last_par = 0;  // per stage: ever used, parity of last issue
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      for (int t = unit; t < total; t += units) {
         const TileInfo ti = decode_tile(st, t, n_tiles, E);
         bool stop = false;
         for (int kb = 0; kb < KB; ++kb) {
@@ -266,12 +377,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             stop = true;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&st.full[stage], MODE == 3 ? B_STAGE_BYTES : STAGE_BYTES);
+          ptx::mbar_arrive_expect_tx(&st.full[stage], MODE == 3 ? P::B_STAGE : P::STAGE);
           if (MODE != 3)
             ptx::tma_load_2d(smemA + stage * A_STAGE_BYTES, &tmA, &st.full[stage], kb * BK,
                              ti.row0);
           if (kmajor_b(MODE)) {  // one box: 64 k x 256 n rows
-            ptx::tma_load_3d(smemB + stage * B_STAGE_BYTES, &tmB, &st.full[stage], kb * BK,
+            ptx::tma_load_3d(smemB + stage * P::B_STAGE, &tmB, &st.full[stage], kb * BK,
                              ti.nt * UMMA_N, ti.e);
           } else {
 #pragma unroll
@@ -281,7 +392,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                 ncol = (q < 2 ? 0 : I) + ti.nt * 128 + (q & 1) * 64;
               else
                 ncol = ti.nt * UMMA_N + q * 64;
-              uint8_t *dst = smemB + stage * B_STAGE_BYTES + q * B_BOX_BYTES;
+              uint8_t *dst = smemB + stage * P::B_STAGE + q * B_BOX_BYTES;
               if (b_nb > 0)  // tiled weights: the 64 x 64 tile is one contiguous run
                 ptx::tma_load_2d(dst, &tmB, &st.full[stage], 0,
                                  ((ti.e * KB + kb) * b_nb + (ncol >> 6)) * 64);
@@ -303,12 +414,13 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         if (used >> s & 1u) ptx::mbar_wait(&st.full[s], last_par >> s & 1u);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // PAIR: the leader alone issues the pair's MMAs
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      for (int t = unit; t < total; t += units) {
         if (!wait_or_abort(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status, wait_limit)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * UMMA_N);
@@ -324,7 +436,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           if (MODE == 3) ptx::fence_proxy_async_smem();
           ptx::tc_fence_after();
           const uint32_t a0 = ptx::smem_u32(smemA + stage * A_STAGE_BYTES);
-          const uint32_t b0 = ptx::smem_u32(smemB + stage * B_STAGE_BYTES);
+          const uint32_t b0 = ptx::smem_u32(smemB + stage * P::B_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             // A: K-major SW128, k step of 16 elements = 32 bytes inside the atom
@@ -333,22 +445,36 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             // or (mode 5) K-major SW128 like A, 256 n rows
             const uint64_t bdesc = kmajor_b(MODE) ? ptx::smem_desc(b0 + kk * 32, 16, 1024)
                                                   : ptx::smem_desc(b0 + kk * 2048, B_BOX_BYTES, 1024);
-            ptx::mma_bf16(d, adesc, bdesc, kmajor_b(MODE) ? IDESC_KB : IDESC,
-                          (kb | kk) != 0 ? 1u : 0u);
+            // PAIR: each CTA's half of B is two of these atoms (128 n)
+            if constexpr (PAIR)
+              ptx::mma_bf16_pair(d, adesc, bdesc, IDESC_PAIR, (kb | kk) != 0 ? 1u : 0u);
+            else
+              ptx::mma_bf16(d, adesc, bdesc, kmajor_b(MODE) ? IDESC_KB : IDESC,
+                            (kb | kk) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(&st.empty[stage]);
+          // the stage is free in both CTAs once these MMAs have read it
+          if constexpr (PAIR)
+            ptx::mma_commit_pair(&st.empty[stage], 0x3);
+          else
+            ptx::mma_commit(&st.empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (stop) break;
-        ptx::mma_commit(&st.tfull[acc]);
+        if constexpr (PAIR)
+          ptx::mma_commit_pair(&st.tfull[acc], 0x3);
+        else
+          ptx::mma_commit(&st.tfull[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       // wait until every MMA this thread issued has finished
-      ptx::mma_commit(&st.drain);
+      if constexpr (PAIR)
+        ptx::mma_commit_pair(&st.drain, 0x1);
+      else
+        ptx::mma_commit(&st.drain);
       ptx::mbar_wait(&st.drain, 0);
     }
   } else if (warp < 6) {
@@ -356,8 +482,10 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile(st, t, n_tiles, E);
+    // PAIR: the odd CTA's warps release the accumulator on the leader's barrier
+    const uint32_t tempty0 = PAIR ? ptx::mapa_shared(ptx::smem_u32(&st.tempty[0]), 0) : 0u;
+    for (int t = unit; t < total; t += units) {
+      const TileInfo ti = decode_tile<PAIR>(st, t, n_tiles, E, rank);
       if (!wait_or_abort(&st.tfull[acc], acc_phase, abort_flag, status, wait_limit)) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + (uint32_t)(acc * UMMA_N) + ((uint32_t)(q * 32) << 16);
@@ -459,7 +587,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&st.tempty[acc]);
+      if (lane == 0) {
+        if (PAIR && !leader)
+          ptx::mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
+        else
+          ptx::mbar_arrive(&st.tempty[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -522,11 +655,38 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if constexpr (PAIR) {
+    // every role of both CTAs is done (the leader's MMAs have completed) and
+    // the odd CTA's load counts are in the leader
+    ptx::cluster_sync();
+    if (leader && tid == 0) {
+      // Both producers follow the same empty barriers, so per stage their
+      // counts differ by at most one phase when one side gave up early: the
+      // leader completes that last phase for the side that never came (its
+      // bytes, or its own arrival), then waits until every copy has landed.
+      for (int s = 0; s < STAGES; ++s) {
+        const int own = st.own_issued[s], peer = st.peer_issued[s];
+        if (own == peer + 1)
+          ptx::mbar_complete_tx(&st.full[s], P::STAGE);
+        else if (peer == own + 1)
+          ptx::mbar_arrive_expect_tx(&st.full[s], P::STAGE);
+        const int last = own > peer ? own : peer;
+        if (last > 0) ptx::mbar_wait(&st.full[s], (uint32_t)(last - 1) & 1u);
+      }
+    }
+    // no copy into either CTA is still in flight
+    ptx::cluster_sync();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     __syncwarp();
-    ptx::tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (PAIR)
+      ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+    else
+      ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -593,15 +753,15 @@ bool weight_map(CUtensorMap *m, const void *w, const Desc &d, uint64_t rows, uin
   return make_map_3d(m, w, cols, rows, d.E, 64, BK);
 }
 
-template <int MODE>
+template <int MODE, bool PAIR = false>
 cudaError_t set_smem_attr() {
   static int done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>,
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, PAIR>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
+                                       (int)smem_bytes<PAIR>());
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
   return e;
 }
@@ -611,7 +771,78 @@ int gemm_grid(int sm_reserve) {
   return g < 1 ? 1 : g;
 }
 
+// 0: CTA pairs for the forward GEMMs, 1: single CTAs (moe_set_gemm_pairs)
+std::atomic<int> g_single_cta{0};
+
+// CTA pairs of MODE's kernel that can be resident at once (cached per device)
+template <int MODE>
+cudaError_t pair_clusters(int *out) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!cached[dev]) {
+    e = set_smem_attr<MODE, true>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 16);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem_bytes<true>();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int nc = 0;
+    e = cudaOccupancyMaxActiveClusters(&nc, grouped_gemm_tc_kernel<MODE, true>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (nc < 1) return cudaErrorInvalidConfiguration;
+    cached[dev] = nc;
+  }
+  *out = cached[dev];
+  return cudaSuccess;
+}
+
+// Persistent launch of a forward GEMM: one CTA per SM, or (pairs) as many
+// CTA pairs as are resident at once within the SMs sm_reserve leaves.
+template <int MODE, typename... Args>
+cudaError_t launch_forward_gemm(int sm_reserve, cudaStream_t s, Args &&...args) {
+  if (g_single_cta.load(std::memory_order_relaxed)) {
+    cudaError_t e = set_smem_attr<MODE>();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(grouped_gemm_tc_kernel<MODE>, dim3(gemm_grid(sm_reserve)),
+                      dim3(NUM_THREADS), SMEM_BYTES, s, static_cast<Args &&>(args)...);
+  }
+  int nc = 0;
+  cudaError_t e = pair_clusters<MODE>(&nc);
+  if (e != cudaSuccess) return e;
+  const int avail = gemm_grid(sm_reserve) / 2;
+  if (avail < nc) nc = avail < 1 ? 1 : avail;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * nc);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem_bytes<true>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<MODE, true>,
+                            static_cast<Args &&>(args)...);
+}
+
 }  // namespace
+
+void set_gemm_single_cta(bool single) { g_single_cta.store(single ? 1 : 0); }
+bool gemm_single_cta() { return g_single_cta.load() != 0; }
 
 cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
                             const int32_t *offsets, void *h, int sm_reserve, int32_t *status,
@@ -622,12 +853,11 @@ cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
   int BNB = 0;
   if (!make_map_2d(&mA, x_perm, d.H, nK, BK, BM) || !weight_map(&mB, w13, d, d.H, 2ull * d.I, &BNB))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_attr<1>();
-  if (e != cudaSuccess) return e;
-  return launch_pdl(grouped_gemm_tc_kernel<1>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
-                    SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
-                    reinterpret_cast<__nv_bfloat16 *>(h), status, nullptr, 0, nullptr, nullptr,
-                    nullptr, pipeline_wait_limit(), BNB);
+  return launch_forward_gemm<1>(sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
+                                reinterpret_cast<__nv_bfloat16 *>(h), status,
+                                (const int32_t *)nullptr, 0, (const __nv_bfloat16 *)nullptr,
+                                (const float *)nullptr, (const __nv_bfloat16 *)nullptr,
+                                pipeline_wait_limit(), BNB);
 }
 
 cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *perm,
@@ -654,12 +884,11 @@ cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const 
   int BNB = 0;
   if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !weight_map(&mB, w2, d, d.I, d.H, &BNB))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_attr<2>();
-  if (e != cudaSuccess) return e;
-  return launch_pdl(grouped_gemm_tc_kernel<2>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
-                    SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
-                    reinterpret_cast<__nv_bfloat16 *>(y_perm), status, nullptr, 0, nullptr,
-                    nullptr, nullptr, pipeline_wait_limit(), BNB);
+  return launch_forward_gemm<2>(sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
+                                reinterpret_cast<__nv_bfloat16 *>(y_perm), status,
+                                (const int32_t *)nullptr, 0, (const __nv_bfloat16 *)nullptr,
+                                (const float *)nullptr, (const __nv_bfloat16 *)nullptr,
+                                pipeline_wait_limit(), BNB);
 }
 
 cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w2,
@@ -672,12 +901,10 @@ cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w
   int BNB = 0;
   if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !weight_map(&mB, w2, d, d.I, d.H, &BNB))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_attr<4>();
-  if (e != cudaSuccess) return e;
-  return launch_pdl(grouped_gemm_tc_kernel<4>, dim3(gemm_grid(sm_reserve)), dim3(NUM_THREADS),
-                    SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
-                    reinterpret_cast<__nv_bfloat16 *>(y_slot), status, perm, d.K, nullptr,
-                    topk_w, nullptr, pipeline_wait_limit(), BNB);
+  return launch_forward_gemm<4>(sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
+                                reinterpret_cast<__nv_bfloat16 *>(y_slot), status, perm, d.K,
+                                (const __nv_bfloat16 *)nullptr, topk_w,
+                                (const __nv_bfloat16 *)nullptr, pipeline_wait_limit(), BNB);
 }
 
 cudaError_t launch_gemm_dgrad_tc(const Desc &d, const void *a, const void *w, int Kdim, int Nout,

@@ -719,6 +719,11 @@ moe_status_t moe_set_pipeline_wait_limit(long long cycles) {
   return MOE_OK;
 }
 
+moe_status_t moe_set_gemm_pairs(int enable) {
+  set_gemm_single_cta(enable == 0);
+  return MOE_OK;
+}
+
 moe_status_t moe_check_status(const int32_t *status_word, moe_stream_t stream) {
   if (!status_word) return MOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
