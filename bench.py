@@ -600,12 +600,13 @@ def run_ours(args, cfg):
                     "unit": "GB/s", "frac": g1["gbs"] / peaks["hbm_gbs"]}
     peak_kind = "bf16 burst" if roofline["bound"] == "tensor" else "HBM copy"
     roofline.update({
-        "kernel": "grouped_gemm_tc_kernel<1> (GEMM1 + SwiGLU)",
+        "kernel": ("grouped_gemm_tc_kernel<1> (GEMM1 + SwiGLU, "
+                   + ("CTA pairs)" if args.gemm_pairs == "on" else "single CTAs)")),
         "peak_source": f"{peak_src} {peak_kind}" + (" (of measured)" if peak_src == "measured"
                                                     else " (of fallback)"),
         # DRAM bytes per launch from the ncu capture of this workload's GEMM1
         "traffic": (recorded_traffic("gemm1_olmoe_bf16.md", GEMM_SOURCES)
-                    if cfg.name == "olmoe_bf16" else None),
+                    if cfg.name == "olmoe_bf16" and args.gemm_pairs == "on" else None),
         "algorithmic_flop_per_launch": alg["gemm1"]["flop"],
         "algorithmic_bytes_per_launch": alg["gemm1"]["bytes"],
         # every kernel of this workload's step (and the fused-gather GEMM1)

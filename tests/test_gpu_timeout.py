@@ -20,7 +20,10 @@ def _gemm1(M, run, h, st):
     M.moe_expert_gemm1_swiglu(run.desc, v("x_perm"), run.L["w13"], v("offsets"), h, 0, st)
 
 
-def test_pipeline_wait_timeout_reports_and_recovers():
+@pytest.mark.parametrize("pairs", [True, False], ids=["cta_pairs", "single_cta"])
+def test_pipeline_wait_timeout_reports_and_recovers(pairs):
+    """CTA pairs: both CTAs give up on their own; the leader settles the
+    stages whose two halves were not both loaded before the pair leaves."""
     import top_routing_dispatch_gb300 as M
     run = Run(OLMOE, n=512)
     assert run.status == 0
@@ -29,6 +32,7 @@ def test_pipeline_wait_timeout_reports_and_recovers():
     _gemm1(M, run, ref, st)
     assert M.moe_check_status(st) == 0
     try:
+        M.moe_set_gemm_pairs(pairs)
         M.moe_set_pipeline_wait_limit(200)
         h = torch.zeros_like(ref)
         st.zero_()
@@ -36,6 +40,7 @@ def test_pipeline_wait_timeout_reports_and_recovers():
         got = M.moe_check_status(st)
     finally:
         M.moe_set_pipeline_wait_limit(0)
+        M.moe_set_gemm_pairs(True)
     assert got == MOE_ERR_TIMEOUT
     # the context is usable and the default limit is back: same bits as before
     st.zero_()
