@@ -1,4 +1,4 @@
-"""The forward grouped GEMMs on CTA pairs (cta_group::2, 256-row tiles, the
+"""The grouped GEMMs on CTA pairs (cta_group::2, 256-row tiles, the
 default) and on single CTAs (128-row tiles, moe_set_gemm_pairs(False)) give the
 same results: GEMM1 + SwiGLU (h), GEMM2 (unweighted and weighted) and the whole
 layer, on the small parity shapes (one-row and ragged segments, empty experts,
@@ -69,3 +69,22 @@ def test_pairs_sm_reserve():
 @pytest.mark.parametrize("cfg", [OLMOE, SKEW, DSV3], ids=lambda c: c.name)
 def test_pairs_full_size(cfg):
     _check(cfg)
+
+
+@pytest.mark.parametrize("name", ["bwd_bf16", "bwd_skew_e64", "bwd_e128", "olmoe"])
+def test_pairs_backward(name):
+    """moe_backward's dgrad (K-major weight operand) and SwiGLU-backward GEMMs
+    on CTA pairs against single CTAs: every gradient bitwise equal."""
+    import top_routing_dispatch_gb300 as M
+    from tests.test_gpu_backward import CASES, _run
+    cfg = OLMOE if name == "olmoe" else next(c for c in CASES if c.name == name)
+    M.moe_set_gemm_pairs(True)
+    a = _run(cfg)
+    try:
+        M.moe_set_gemm_pairs(False)
+        b = _run(cfg)
+    finally:
+        M.moe_set_gemm_pairs(True)
+    assert a["status"] == 0 and b["status"] == 0
+    for k in ("dx", "dwg", "dbias", "dw13", "dw2"):
+        assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), k

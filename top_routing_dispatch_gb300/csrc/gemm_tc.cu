@@ -96,6 +96,7 @@ static_assert(smem_bytes<true>() <= 227 * 1024, "pair pipeline exceeds shared me
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/true);
 constexpr uint32_t IDESC_KB = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/false);
 constexpr uint32_t IDESC_PAIR = ptx::idesc_bf16_f32(2 * BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/true);
+constexpr uint32_t IDESC_PAIR_KB = ptx::idesc_bf16_f32(2 * BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/false);
 
 // A pipeline wait: gives up after `limit` cycles (setting the abort flag and
 // MOE_DEV_TIMEOUT), or at once when another role has given up.
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                            const float *__restrict__ tw,
                            const __nv_bfloat16 *__restrict__ aux, long long wait_limit,
                            int b_nb) {
-  static_assert(!PAIR || MODE == 1 || MODE == 2 || MODE == 4, "CTA pairs: forward modes only");
+  static_assert(!PAIR || MODE != 3, "CTA pairs: not with the cp.async gather of mode 3");
   using P = Pipe<PAIR>;
   constexpr int STAGES = P::STAGES;
   pdl_enter();
@@ -333,6 +334,10 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           // half) loads the expert's first rows: computed, never stored
           ptx::tma_load_2d_pair(smemA + stage * A_STAGE_BYTES, &tmA, bar, kb * BK,
                                 ti.rows > 0 ? ti.row0 : st.off[ti.e]);
+          if (kmajor_b(MODE)) {  // one box: 64 k x this CTA's 128 of the 256 n rows
+            ptx::tma_load_3d_pair(smemB + stage * P::B_STAGE, &tmB, bar, kb * BK,
+                                  ti.nt * UMMA_N + rank * (UMMA_N / 2), ti.e);
+          } else {
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             // this CTA's half of the 256 B columns: GEMM1 gate (rank 0) or up
@@ -345,6 +350,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
               ptx::tma_load_2d_pair(dst, &tmB, bar, 0, ((ti.e * KB + kb) * b_nb + (ncol >> 6)) * 64);
             else
               ptx::tma_load_3d_pair(dst, &tmB, bar, ncol, kb * BK, ti.e);
+          }
           }
           ++st.own_issued[stage];
           if (++stage == STAGES) {
@@ -447,7 +453,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                                                   : ptx::smem_desc(b0 + kk * 2048, B_BOX_BYTES, 1024);
             // PAIR: each CTA's half of B is two of these atoms (128 n)
             if constexpr (PAIR)
-              ptx::mma_bf16_pair(d, adesc, bdesc, IDESC_PAIR, (kb | kk) != 0 ? 1u : 0u);
+              ptx::mma_bf16_pair(d, adesc, bdesc, kmajor_b(MODE) ? IDESC_PAIR_KB : IDESC_PAIR,
+                                 (kb | kk) != 0 ? 1u : 0u);
             else
               ptx::mma_bf16(d, adesc, bdesc, kmajor_b(MODE) ? IDESC_KB : IDESC,
                             (kb | kk) != 0 ? 1u : 0u);
@@ -771,7 +778,8 @@ int gemm_grid(int sm_reserve) {
   return g < 1 ? 1 : g;
 }
 
-// 0: CTA pairs for the forward GEMMs, 1: single CTAs (moe_set_gemm_pairs)
+// 0: CTA pairs for the grouped GEMMs (all modes but 3), 1: single CTAs
+// (moe_set_gemm_pairs)
 std::atomic<int> g_single_cta{0};
 
 // CTA pairs of MODE's kernel that can be resident at once (cached per device)
@@ -806,11 +814,11 @@ cudaError_t pair_clusters(int *out) {
   return cudaSuccess;
 }
 
-// Persistent launch of a forward GEMM: one CTA per SM, or (pairs) as many
-// CTA pairs as are resident at once within the SMs sm_reserve leaves.
+// Persistent launch of a grouped GEMM: one CTA per SM, or (pairs) as many CTA
+// pairs as are resident at once within the SMs sm_reserve leaves.
 template <int MODE, typename... Args>
-cudaError_t launch_forward_gemm(int sm_reserve, cudaStream_t s, Args &&...args) {
-  if (g_single_cta.load(std::memory_order_relaxed)) {
+cudaError_t launch_gemm(bool pair, int sm_reserve, cudaStream_t s, Args &&...args) {
+  if (!pair) {
     cudaError_t e = set_smem_attr<MODE>();
     if (e != cudaSuccess) return e;
     return launch_pdl(grouped_gemm_tc_kernel<MODE>, dim3(gemm_grid(sm_reserve)),
@@ -853,7 +861,7 @@ cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
   int BNB = 0;
   if (!make_map_2d(&mA, x_perm, d.H, nK, BK, BM) || !weight_map(&mB, w13, d, d.H, 2ull * d.I, &BNB))
     return cudaErrorInvalidValue;
-  return launch_forward_gemm<1>(sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
+  return launch_gemm<1>(!gemm_single_cta(), sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
                                 reinterpret_cast<__nv_bfloat16 *>(h), status,
                                 (const int32_t *)nullptr, 0, (const __nv_bfloat16 *)nullptr,
                                 (const float *)nullptr, (const __nv_bfloat16 *)nullptr,
@@ -884,7 +892,7 @@ cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const 
   int BNB = 0;
   if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !weight_map(&mB, w2, d, d.I, d.H, &BNB))
     return cudaErrorInvalidValue;
-  return launch_forward_gemm<2>(sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
+  return launch_gemm<2>(!gemm_single_cta(), sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
                                 reinterpret_cast<__nv_bfloat16 *>(y_perm), status,
                                 (const int32_t *)nullptr, 0, (const __nv_bfloat16 *)nullptr,
                                 (const float *)nullptr, (const __nv_bfloat16 *)nullptr,
@@ -901,7 +909,7 @@ cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w
   int BNB = 0;
   if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !weight_map(&mB, w2, d, d.I, d.H, &BNB))
     return cudaErrorInvalidValue;
-  return launch_forward_gemm<4>(sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
+  return launch_gemm<4>(!gemm_single_cta(), sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
                                 reinterpret_cast<__nv_bfloat16 *>(y_slot), status, perm, d.K,
                                 (const __nv_bfloat16 *)nullptr, topk_w,
                                 (const __nv_bfloat16 *)nullptr, pipeline_wait_limit(), BNB);
@@ -913,16 +921,17 @@ cudaError_t launch_gemm_dgrad_tc(const Desc &d, const void *a, const void *w, in
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
   CUtensorMap mA, mB;
-  // A (nK, Kdim) K-major; W[e] (Nout, Kdim): rows n with k contiguous
+  // A (nK, Kdim) K-major; W[e] (Nout, Kdim): rows n with k contiguous, one box
+  // of 256 n rows per stage (CTA pairs: each CTA's 128)
+  const bool pair = !gemm_single_cta();  // read once: the box and the kernel must agree
+  const uint32_t box_n = pair ? UMMA_N / 2 : UMMA_N;
   if (!make_map_2d(&mA, a, Kdim, nK, BK, BM) ||
-      !make_map_3d(&mB, w, Kdim, Nout, d.E, BK, UMMA_N))
+      !make_map_3d(&mB, w, Kdim, Nout, d.E, BK, box_n))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_attr<5>();
-  if (e != cudaSuccess) return e;
-  return launch_pdl(grouped_gemm_tc_kernel<5>, dim3(gemm_grid(0)), dim3(threads_for(5)),
-                    SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, Kdim, 0, Nout,
-                    reinterpret_cast<__nv_bfloat16 *>(out), status, nullptr, 0, nullptr, nullptr,
-                    nullptr, pipeline_wait_limit(), 0);
+  return launch_gemm<5>(pair, 0, s, mA, mB, offsets, d.E, (int)nK, Kdim, 0, Nout,
+                        reinterpret_cast<__nv_bfloat16 *>(out), status, (const int32_t *)nullptr,
+                        0, (const __nv_bfloat16 *)nullptr, (const float *)nullptr,
+                        (const __nv_bfloat16 *)nullptr, pipeline_wait_limit(), 0);
 }
 
 cudaError_t launch_gemm1_swiglu_bwd_tc(const Desc &d, const void *x_perm, const void *w13,
@@ -934,12 +943,10 @@ cudaError_t launch_gemm1_swiglu_bwd_tc(const Desc &d, const void *x_perm, const 
   if (!make_map_2d(&mA, x_perm, d.H, nK, BK, BM) ||
       !make_map_3d(&mB, w13, 2ull * d.I, d.H, d.E, 64, BK))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_attr<6>();
-  if (e != cudaSuccess) return e;
-  return launch_pdl(grouped_gemm_tc_kernel<6>, dim3(gemm_grid(0)), dim3(threads_for(6)),
-                    SMEM_BYTES, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, 2 * d.I,
-                    reinterpret_cast<__nv_bfloat16 *>(dgu), status, nullptr, 0, nullptr, nullptr,
-                    reinterpret_cast<const __nv_bfloat16 *>(dh), pipeline_wait_limit(), 0);
+  return launch_gemm<6>(!gemm_single_cta(), 0, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, 2 * d.I,
+                        reinterpret_cast<__nv_bfloat16 *>(dgu), status, (const int32_t *)nullptr,
+                        0, (const __nv_bfloat16 *)nullptr, (const float *)nullptr,
+                        reinterpret_cast<const __nv_bfloat16 *>(dh), pipeline_wait_limit(), 0);
 }
 
 }  // namespace moe
