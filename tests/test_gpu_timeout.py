@@ -53,3 +53,28 @@ def test_pipeline_wait_timeout_reports_and_recovers(pairs):
     torch.cuda.synchronize()
     assert int(run.layer.status.item()) == 0
     assert torch.equal(y.view(torch.int16), run.y.view(torch.int16))
+
+
+@pytest.mark.parametrize("pairs", [True, False], ids=["cta_pairs", "single_cta"])
+def test_backward_timeout_reports_and_recovers(pairs):
+    """The backward's GEMMs (dgrad, SwiGLU backward, weight gradients) give up
+    the same way; a normal call afterwards gives the same bits as before."""
+    import top_routing_dispatch_gb300 as M
+    from tests.test_gpu_backward import CASES, _run
+    cfg = next(c for c in CASES if c.name == "bwd_skew_e64")  # M = H, I multiples of 256
+    M.moe_set_gemm_pairs(pairs)
+    try:
+        ref = _run(cfg)
+        assert ref["status"] == 0
+        M.moe_set_pipeline_wait_limit(200)
+        try:
+            got = _run(cfg)
+        finally:
+            M.moe_set_pipeline_wait_limit(0)
+        assert got["status"] & 4, got["status"]  # MOE_DEV_TIMEOUT
+        again = _run(cfg)
+    finally:
+        M.moe_set_gemm_pairs(True)
+    assert again["status"] == 0
+    for k in ("dx", "dwg", "dbias", "dw13", "dw2"):
+        assert torch.equal(again[k].view(torch.uint8), ref[k].view(torch.uint8)), k
