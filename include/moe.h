@@ -431,14 +431,16 @@ moe_status_t moe_prepare_weights(const moe_layer_desc_t *desc, const void *w13, 
 moe_status_t moe_set_pipeline_wait_limit(long long cycles);
 
 /*
- * Tuning control of the forward grouped GEMMs (moe_expert_gemm1_swiglu,
- * moe_expert_gemm2, moe_expert_gemm2_weighted and the forward's GEMMs, bf16):
- * enable != 0 (the default) runs them on CTA pairs -- clusters of two CTAs on
- * two SMs computing 256-row x 256-column tiles with cta_group::2 MMAs, each
- * CTA holding its own 128 rows of A and half of the weight tile, which gives
- * six operand stages instead of four; enable == 0 runs one CTA per SM with
- * 128-row tiles.  The results are the same either way.  Applies to launches
- * enqueued after the call, from any host thread.  Always returns MOE_OK.
+ * Tuning control of the tensor-core grouped GEMMs (bf16: moe_expert_gemm1_swiglu,
+ * moe_expert_gemm2, moe_expert_gemm2_weighted, the forward's GEMMs, and
+ * moe_backward's dgrad, SwiGLU-backward and weight-gradient GEMMs; not
+ * moe_expert_gemm1_swiglu_gather): enable != 0 (the default) runs them on CTA
+ * pairs -- clusters of two CTAs on two SMs computing 256-row x 256-column
+ * tiles with cta_group::2 MMAs, each CTA holding its own 128 rows of A and half
+ * of the B tile, which gives six operand stages instead of four; enable == 0
+ * runs one CTA per SM with 128-row tiles.  The results are bitwise the same
+ * either way.  Applies to launches enqueued after the call, from any host
+ * thread.  Always returns MOE_OK.
  */
 moe_status_t moe_set_gemm_pairs(int enable);
 

@@ -213,8 +213,9 @@ def moe_set_pipeline_wait_limit(cycles):
 
 
 def moe_set_gemm_pairs(enable):
-    """Tuning control: run the forward grouped GEMMs on CTA pairs (True, the
-    default) or on single CTAs (False); the results are the same."""
+    """Tuning control: run the tensor-core grouped GEMMs (forward and
+    backward) on CTA pairs (True, the default) or on single CTAs (False); the
+    results are bitwise the same."""
     _check(_lib.load().moe_set_gemm_pairs(1 if enable else 0), "moe_set_gemm_pairs")
 
 

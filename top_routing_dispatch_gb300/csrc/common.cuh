@@ -83,8 +83,9 @@ cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *
                                    int sm_reserve, int32_t *status, cudaStream_t s);
 cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const int32_t *offsets,
                             void *y_perm, int sm_reserve, int32_t *status, cudaStream_t s);
-// The forward GEMMs (modes 1, 2, 4) run on CTA pairs (cta_group::2, 256-row
-// tiles) unless single CTAs are selected (moe_set_gemm_pairs); same results.
+// The grouped GEMMs (every mode but the fused gather, and the weight
+// gradients) run on CTA pairs (cta_group::2, 256-row tiles) unless single CTAs
+// are selected (moe_set_gemm_pairs); bitwise the same results.
 void set_gemm_single_cta(bool single);
 bool gemm_single_cta();
 // GEMM2 with the routing weight applied and each row written to its

@@ -8,14 +8,19 @@
 // epilogue of the DeepGEMM Mega MoE kernel described in "大模型系统中的通算
 // 融合" §4 (one L1 GEMM produces gate and up, the epilogue applies SwiGLU).
 //
-// Design (one persistent CTA per SM, 6 warps):
+// Design (persistent, 6 warps per CTA):
 //   warp 0      TMA producer: A tile (128 rows x 64 k) of the activations and
-//               four B boxes (64 k x 64 n) of the expert's weights per stage.
-//   warp 1      TMEM allocator and MMA issuer: 4 x tcgen05.mma 128x256x16 per
-//               stage into one of two 256-column TMEM accumulators.
+//               the expert's weight boxes (64 k x 64 n) per stage.
+//   warp 1      TMEM allocator and MMA issuer: 4 x tcgen05.mma per stage into
+//               one of two 256-column TMEM accumulators.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
 //               SiLU(gate)*up (GEMM1) or plain conversion (GEMM2), bf16 stores
 //               of the rows that belong to the tile's expert.
+// Two forms, bitwise the same.  Single CTAs: one CTA per SM, 128x256x16 MMAs,
+// four 48 KB stages (A + four B boxes).  CTA pairs (PAIR, the default): one
+// cluster of two CTAs per two SMs, 256x256x16 cta_group::2 MMAs issued by the
+// even CTA, each CTA holding its own 128 A rows and half of the weight tile
+// (two B boxes), six 32 KB stages (see the kernel's comment for the protocol).
 // A tile is (m-tile, n-tile).  m-tiles are 128-row windows that start at each
 // expert's segment start, so every tile belongs to exactly one expert; its
 // rows past the segment end are computed but not stored (TMA zero-fills rows
