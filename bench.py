@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--weights", choices=["tiled", "row"], default="tiled",
                     help="bf16 expert weights: tiled by moe_prepare_weights once, untimed "
                          "(default), or read row-major")
+    ap.add_argument("--router-t", choices=["on", "off"], default="on",
+                    help="bf16 layers: the router weight transposed once by moe_prepare_router "
+                         "(untimed) for the near-tie rescoring, or read as stored (same results)")
     ap.add_argument("--gemm-pairs", choices=["on", "off"], default="on",
                     help="forward grouped GEMMs on CTA pairs (cta_group::2, the default) or on "
                          "single CTAs (same results)")
@@ -430,11 +433,13 @@ def measure_layer(args, torch, M, synth, cfg, dev, peaks, rank, steps, warmup, d
     L = synth.make_layer(cfg, dev)
     x = synth.make_x(cfg, dev, seed=rank_seed(cfg, rank))
     tiled = tiled_weights(args, cfg)
-    desc = M.desc_for(cfg, tiled=tiled)
+    if args.router_t == "on" and cfg.dtype == "bf16":
+        L["w_gate_t"] = M.moe_prepare_router(M.desc_for(cfg), L["w_gate"])
+    desc = M.desc_for(cfg, tiled=tiled, w_gate_t=L.get("w_gate_t"))
     if tiled:
         L["w13_row"], L["w2_row"] = L["w13"], L["w2"]
         L["w13"], L["w2"] = M.moe_prepare_weights(M.desc_for(cfg), L["w13_row"], L["w2_row"])
-        torch.cuda.synchronize()
+    torch.cuda.synchronize()
     layer = M.MoELayer(desc, L["w_gate"], L["bias"], L["w13"], L["w2"])
     v = {k: layer.view(k) for k in ("logits", "topk_idx", "topk_w", "counts", "offsets", "perm",
                                     "inv_perm", "x_perm", "h", "y_perm")}
@@ -628,6 +633,8 @@ def run_ours(args, cfg):
         "phased_ms_per_step": statistics.mean(r["phased_ms"]),
         "weights": ("tiled by moe_prepare_weights (once, untimed)" if tiled_weights(args, cfg)
                     else "row-major"),
+        "router_weight": ("also transposed by moe_prepare_router (once, untimed)"
+                          if "w_gate_t" in L else "as stored"),
         "gemm_tiles": ("CTA pairs (cta_group::2), 256 x 256" if args.gemm_pairs == "on"
                        else "single CTAs, 128 x 256"),
         "e2e": {"value": aggregate_tokens_per_s(cfg.n, args.steps, world, e2e_total), "unit": UNIT,
@@ -711,7 +718,9 @@ def domino(args, torch, M, synth, cfg, dev, peaks):
     hide ratio, strict and over the overlap-eligible phases."""
     L = synth.make_layer(cfg, dev)
     xs = synth.make_micro_batches(cfg, dev)
-    desc = M.desc_for(cfg, tiled=tiled_weights(args, cfg))
+    wgt = (M.moe_prepare_router(M.desc_for(cfg), L["w_gate"])
+           if args.router_t == "on" and cfg.dtype == "bf16" else None)
+    desc = M.desc_for(cfg, tiled=tiled_weights(args, cfg), w_gate_t=wgt)
     if tiled_weights(args, cfg):
         L["w13"], L["w2"] = M.moe_prepare_weights(M.desc_for(cfg), L["w13"], L["w2"])
     layer = M.MoELayer(desc, L["w_gate"], L["bias"], L["w13"], L["w2"], num_mb=2)

@@ -95,6 +95,13 @@ typedef struct {
   int32_t dtype;          /* moe_dtype_t */
   int32_t norm_topk_prob; /* nonzero: divide the K weights by their sum */
   int32_t weight_layout;  /* moe_weight_layout_t of w13 and w2 */
+  /* optional (bf16 layers): the router weight transposed, (E, H) bf16 device
+   * memory made by moe_prepare_router from the w_gate passed to the calls,
+   * or NULL.  The router's exact near-tie rescoring then reads each expert's
+   * column of w_gate as one contiguous row of this copy instead of H
+   * scattered values; the results are bitwise the same.  Ignored for float32
+   * layers. */
+  const void *w_gate_t;
 } moe_layer_desc_t;
 
 /* Library version string and a human-readable name of a status code. */
@@ -414,6 +421,15 @@ moe_status_t moe_forward_host(const moe_layer_desc_t *desc, const void *x_host,
  */
 moe_status_t moe_prepare_weights(const moe_layer_desc_t *desc, const void *w13, const void *w2,
                                  void *w13_tiled, void *w2_tiled, moe_stream_t stream);
+
+/*
+ * One-time transform of the router weight (bf16 layers): w_gate_t[e][h] =
+ * w_gate[h][e], (E, H) bf16, for moe_layer_desc_t.w_gate_t.  w_gate_t must
+ * not overlap w_gate.  Enqueued on `stream`.  MOE_ERR_UNSUPPORTED for float32
+ * layers; MOE_ERR_INVALID_ARG for NULL pointers.
+ */
+moe_status_t moe_prepare_router(const moe_layer_desc_t *desc, const void *w_gate,
+                                void *w_gate_t, moe_stream_t stream);
 
 /*
  * Test control for the device timeout path (failure detection without a

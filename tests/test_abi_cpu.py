@@ -243,3 +243,9 @@ def test_tiled_weights_rejected_where_unsupported(lib):
     assert lib.moe_prepare_weights(ctypes.byref(d), None, None, None, None, None) == 2
     d = M.make_desc(16, 256, 128, 8, 2, "bf16", True)
     assert lib.moe_prepare_weights(ctypes.byref(d), None, None, None, None, None) == 1
+    # moe_prepare_router: bf16 only, both pointers required
+    assert lib.moe_prepare_router(ctypes.byref(d), None, None, None) == 1
+    d = M.make_desc(16, 64, 32, 4, 2, "f32", True)
+    assert lib.moe_prepare_router(ctypes.byref(d), None, None, None) == 2
+    # the descriptor carries the optional transposed router weight pointer
+    assert M.LayerDesc.w_gate_t.offset == 32

@@ -20,6 +20,7 @@ SYMBOLS = (
     "moe_host_workspace_size", "moe_forward_host", "moe_expert_gemm2_weighted",
     "moe_combine_slots", "moe_backward_workspace_size", "moe_backward",
     "moe_set_pipeline_wait_limit", "moe_prepare_weights", "moe_set_gemm_pairs",
+    "moe_prepare_router",
 )
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -38,7 +39,8 @@ SLOT = dict(logits=0, topk_idx=1, topk_w=2, counts=3, offsets=4, perm=5, inv_per
 class LayerDesc(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("K", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("norm_topk_prob", ctypes.c_int32), ("weight_layout", ctypes.c_int32)]
+                ("norm_topk_prob", ctypes.c_int32), ("weight_layout", ctypes.c_int32),
+                ("w_gate_t", ctypes.c_void_p)]
 
 
 _vp = ctypes.c_void_p
@@ -74,6 +76,7 @@ def _declare(lib):
         "moe_set_pipeline_wait_limit": (_st, [ctypes.c_longlong]),
         "moe_set_gemm_pairs": (_st, [ctypes.c_int]),
         "moe_prepare_weights": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp]),
+        "moe_prepare_router": (_st, [_desc_p, _vp, _vp, _vp]),
         "moe_host_workspace_size": (ctypes.c_size_t, [_desc_p]),
         "moe_expert_gemm2_weighted": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                             _vp, _vp]),

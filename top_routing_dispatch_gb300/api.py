@@ -42,21 +42,23 @@ def _stream(s):
     return ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
 
 
-def make_desc(n, H, I, E, K, dtype, norm_topk_prob, tiled=False) -> LayerDesc:
+def make_desc(n, H, I, E, K, dtype, norm_topk_prob, tiled=False, w_gate_t=None) -> LayerDesc:
     """tiled: the expert weights passed to the expert entry points are the
-    output of moe_prepare_weights (MOE_WEIGHTS_TILED)."""
+    output of moe_prepare_weights (MOE_WEIGHTS_TILED).  w_gate_t: the router
+    weight transposed by moe_prepare_router (the caller keeps the tensor
+    alive while the descriptor is used), or None."""
     if isinstance(dtype, torch.dtype):
         dtype = _DT[dtype]
     elif isinstance(dtype, str):
         dtype = {"f32": MOE_F32, "bf16": MOE_BF16}[dtype]
     return LayerDesc(int(n), int(H), int(I), int(E), int(K), int(dtype), int(bool(norm_topk_prob)),
-                     int(bool(tiled)))
+                     int(bool(tiled)), _p(w_gate_t))
 
 
-def desc_for(cfg, n=None, tiled=False) -> LayerDesc:
+def desc_for(cfg, n=None, tiled=False, w_gate_t=None) -> LayerDesc:
     """LayerDesc of a workload config (anything with n, H, I, E, K, dtype, norm_topk_prob)."""
     return make_desc(cfg.n if n is None else n, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype,
-                     cfg.norm_topk_prob, tiled)
+                     cfg.norm_topk_prob, tiled, w_gate_t)
 
 
 def moe_prepare_weights(desc, w13, w2, w13_tiled=None, w2_tiled=None, stream=None):
@@ -67,6 +69,17 @@ def moe_prepare_weights(desc, w13, w2, w13_tiled=None, w2_tiled=None, stream=Non
     _check(_lib.load().moe_prepare_weights(ctypes.byref(desc), _p(w13), _p(w2), _p(w13_tiled),
                                            _p(w2_tiled), _stream(stream)), "moe_prepare_weights")
     return w13_tiled, w2_tiled
+
+
+def moe_prepare_router(desc, w_gate, w_gate_t=None, stream=None):
+    """w_gate (H, E) transposed into (E, H) for LayerDesc.w_gate_t; returns it
+    (allocated here when not given)."""
+    H, E = w_gate.shape
+    if w_gate_t is None:
+        w_gate_t = torch.empty((E, H), dtype=w_gate.dtype, device=w_gate.device)
+    _check(_lib.load().moe_prepare_router(ctypes.byref(desc), _p(w_gate), _p(w_gate_t),
+                                          _stream(stream)), "moe_prepare_router")
+    return w_gate_t
 
 
 def torch_dtype(desc: LayerDesc):
@@ -253,9 +266,15 @@ class MoELayer:
     device, bias (E,) float32 or None.
     """
 
-    def __init__(self, desc: LayerDesc, w_gate, bias, w13, w2, num_mb=1):
+    def __init__(self, desc: LayerDesc, w_gate, bias, w13, w2, num_mb=1, w_gate_t=None):
+        """w_gate_t: the router weight transposed (moe_prepare_router), kept
+        alive here and set in this layer's copy of the descriptor."""
+        if w_gate_t is not None:
+            desc = LayerDesc.from_buffer_copy(desc)
+            desc.w_gate_t = w_gate_t.data_ptr()
         self.desc = desc
         self.w_gate, self.bias, self.w13, self.w2 = w_gate, bias, w13, w2
+        self.w_gate_t = w_gate_t
         dev = w13.device
         self.num_mb = num_mb
         self.ws = torch.empty(moe_workspace_size(desc) * num_mb, dtype=torch.uint8, device=dev)

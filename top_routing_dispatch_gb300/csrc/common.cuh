@@ -33,6 +33,7 @@ struct Desc {
   bool bf16;
   bool norm;
   bool tiled;  // expert weights in MOE_WEIGHTS_TILED layout
+  const void *w_gate_t;  // optional (E, H) transposed router weight (bf16), or null
   long long nK() const { return (long long)n * K; }
 };
 
@@ -139,6 +140,9 @@ inline cudaError_t launch_experts(const Desc &d, const void *x_perm, const void 
 // prepare.cu: w13 (E,H,2I) and w2 (E,I,H) into 64 x 64 tiles (MOE_WEIGHTS_TILED)
 cudaError_t launch_prepare_weights(const Desc &d, const void *w13, const void *w2, void *w13t,
                                    void *w2t, cudaStream_t s);
+// prepare.cu: w_gate (H, E) bf16 transposed into w_gate_t (E, H)
+cudaError_t launch_prepare_router(const Desc &d, const void *w_gate, void *w_gate_t,
+                                  cudaStream_t s);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

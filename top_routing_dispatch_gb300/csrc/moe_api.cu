@@ -56,6 +56,7 @@ moe_status_t check_desc(const moe_layer_desc_t *d, Desc *out) {
   out->bf16 = bf16;
   out->norm = d->norm_topk_prob != 0;
   out->tiled = d->weight_layout == MOE_WEIGHTS_TILED;
+  out->w_gate_t = bf16 ? d->w_gate_t : nullptr;
   return MOE_OK;
 }
 
@@ -699,6 +700,16 @@ moe_status_t moe_backward(const moe_layer_desc_t *desc, const void *x, const voi
     e = launch_router_bwd(d, x, logits, topk_idx, topk_w, dwt, dl, dwp, dw_gate, dbias, s);
   if (e == cudaSuccess) e = launch_dx_final(d, dxp, dl, w_gate, inv_perm, dx, s);
   return cuda_status(e);
+}
+
+moe_status_t moe_prepare_router(const moe_layer_desc_t *desc, const void *w_gate,
+                                void *w_gate_t, moe_stream_t stream) {
+  Desc d;
+  moe_status_t st = check_desc(desc, &d);
+  if (st != MOE_OK) return st;
+  if (!d.bf16) return MOE_ERR_UNSUPPORTED;
+  if (!w_gate || !w_gate_t) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_prepare_router(d, w_gate, w_gate_t, stream));
 }
 
 moe_status_t moe_prepare_weights(const moe_layer_desc_t *desc, const void *w13, const void *w2,

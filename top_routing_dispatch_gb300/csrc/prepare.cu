@@ -1,11 +1,12 @@
-// One-time weight transform for the grouped GEMMs (the pre-transform of
+// One-time weight transforms.  For the grouped GEMMs (the pre-transform of
 // expert weights that the pages describe for DeepGEMM's Mega MoE kernel,
 // "大模型系统中的通算融合" §4.4): every 64 x 64 tile (64 rows of k, 64
 // columns) of each expert matrix becomes one contiguous 8 KB run, ordered by
 // expert, row block, column block.  The GEMMs then fetch each tile they stage
 // as a single DRAM run (the row-major layout gives 64 runs of 128 bytes, one
-// matrix row apart).  A pure copy: results are bitwise those of the row-major
-// weights.
+// matrix row apart).  For the router: w_gate transposed, so the exact
+// near-tie rescoring reads an expert's column as one contiguous row.  Pure
+// copies: results are bitwise those of the weights as stored.
 #include "common.cuh"
 
 namespace moe {
@@ -39,7 +40,35 @@ cudaError_t tile_one(const void *w, void *out, int E, int rows, int cols, cudaSt
                     cols);
 }
 
+// w_gate_t[e][h] = w_gate[h][e]: 32 x 32 blocks through shared memory (one
+// padding column keeps the column reads free of bank conflicts).
+__global__ void __launch_bounds__(256) transpose_gate_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                             __nv_bfloat16 *__restrict__ wt,
+                                                             int H, int E) {
+  pdl_enter();
+  __shared__ __nv_bfloat16 blk[32][33];
+  const int h0 = blockIdx.y * 32, e0 = blockIdx.x * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  for (int r = ty; r < 32; r += 8) {
+    const int h = h0 + r, e = e0 + tx;
+    if (h < H && e < E) blk[r][tx] = w[(size_t)h * E + e];
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int e = e0 + r, h = h0 + tx;
+    if (e < E && h < H) wt[(size_t)e * H + h] = blk[tx][r];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_prepare_router(const Desc &d, const void *w_gate, void *w_gate_t,
+                                  cudaStream_t s) {
+  dim3 grid((unsigned)((d.E + 31) / 32), (unsigned)((d.H + 31) / 32));
+  return launch_pdl(transpose_gate_kernel, grid, dim3(256), 0, s,
+                    reinterpret_cast<const __nv_bfloat16 *>(w_gate),
+                    reinterpret_cast<__nv_bfloat16 *>(w_gate_t), d.H, d.E);
+}
 
 cudaError_t launch_prepare_weights(const Desc &d, const void *w13, const void *w2, void *w13t,
                                    void *w2t, cudaStream_t s) {

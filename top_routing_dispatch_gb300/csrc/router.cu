@@ -119,8 +119,9 @@ constexpr int RU = 4;  // rows of W_gate per lane per step of that pass
 template <int EPL, bool BF16>
 __global__ void __launch_bounds__(TOPK_WARPS * 32) router_topk_kernel(
     const float *__restrict__ logits, const void *__restrict__ x, const void *__restrict__ wg,
-    const float *__restrict__ bias, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
-    int n, int H, int E, int K, int norm, int only_flagged) {
+    const __nv_bfloat16 *__restrict__ wgt, const float *__restrict__ bias,
+    int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int n, int H, int E, int K,
+    int norm, int only_flagged) {
   pdl_enter();
   __shared__ float s_hi[TOPK_WARPS][kMaxK];
   __shared__ float s_lo[TOPK_WARPS][kMaxK];
@@ -219,7 +220,10 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) router_topk_kernel(
           xv[u] = in ? ld_in<BF16>(x, (size_t)t * H + hh) : 0.f;
 #pragma unroll
           for (int c = 0; c < RG; ++c)
-            wv[u][c] = (in && ce[c] >= 0) ? ld_in<BF16>(wg, (size_t)hh * E + ce[c]) : 0.f;
+            // W_gate[hh][ce[c]]: from the transposed copy (bf16) when given
+            wv[u][c] = !(in && ce[c] >= 0) ? 0.f
+                       : (BF16 && wgt) ? __bfloat162float(wgt[(size_t)ce[c] * H + hh])
+                                       : ld_in<BF16>(wg, (size_t)hh * E + ce[c]);
         }
 #pragma unroll
         for (int u = 0; u < RU; ++u)
@@ -304,9 +308,11 @@ cudaError_t launch_topk(const Desc &d, const float *logits, const void *x, const
   dim3 grid((d.n + TOPK_WARPS - 1) / TOPK_WARPS);
   if (d.bf16)
     return launch_pdl(router_topk_kernel<EPL, true>, grid, dim3(TOPK_WARPS * 32), 0, s, logits, x,
-                      wg, bias, idx, w, d.n, d.H, d.E, d.K, d.norm, only_flagged);
+                      wg, reinterpret_cast<const __nv_bfloat16 *>(d.w_gate_t), bias, idx, w, d.n,
+                      d.H, d.E, d.K, d.norm, only_flagged);
   return launch_pdl(router_topk_kernel<EPL, false>, grid, dim3(TOPK_WARPS * 32), 0, s, logits, x,
-                    wg, bias, idx, w, d.n, d.H, d.E, d.K, d.norm, only_flagged);
+                    wg, (const __nv_bfloat16 *)nullptr, bias, idx, w, d.n, d.H, d.E, d.K, d.norm,
+                    only_flagged);
 }
 
 cudaError_t launch_topk_any(const Desc &d, const float *logits, const void *x, const void *wg,

@@ -88,6 +88,22 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// W_gate[h][e] for the rescoring is read at base[col(e) + h * stride]: from the
+// transposed copy when there is one (expert e's column is a contiguous row of
+// it: col = e * H, stride 1), else from W_gate itself (col = e, stride E).
+// The same value either way.
+// col(e) < 0 marks an unused entry.
+struct GateCols {
+  const __nv_bfloat16 *base;
+  int stride;
+  bool t;
+  __device__ __forceinline__ int col(int e, int H) const { return e < 0 ? -1 : t ? e * H : e; }
+};
+__device__ __forceinline__ GateCols gate_cols(const __nv_bfloat16 *wg, const __nv_bfloat16 *wgt,
+                                              int E) {
+  return wgt ? GateCols{wgt, 1, true} : GateCols{wg, E, false};
+}
+
 // An order-preserving map of float32 onto uint32 (-0 taken as +0): a larger
 // key is a larger value.
 __device__ __forceinline__ unsigned fkey(float v) {
@@ -302,7 +318,8 @@ __device__ __forceinline__ void tok_extend(Tok<NV> &s, const float *lrow, int tl
 template <int NV>
 __device__ __forceinline__ void warp_rescore(const Tok<NV> &s, float (&ex_hi)[NV], float (&ex_lo)[NV], int lane,
                              const __nv_bfloat16 *__restrict__ xr,
-                             const __nv_bfloat16 *__restrict__ wg, const float *__restrict__ bias,
+                             const __nv_bfloat16 *__restrict__ wg,
+                             const __nv_bfloat16 *__restrict__ wgt, const float *__restrict__ bias,
                              int E, int H) {
   constexpr int UG = RM_UG, RU = 8;
   for (int u0 = 0; u0 < s.U; u0 += UG) {
@@ -329,6 +346,10 @@ __device__ __forceinline__ void warp_rescore(const Tok<NV> &s, float (&ex_hi)[NV
     DF acc[UG];
 #pragma unroll
     for (int i = 0; i < UG; ++i) acc[i] = DF{0.f, 0.f};
+    const GateCols gc = gate_cols(wg, wgt, E);
+    int wcol[UG];
+#pragma unroll
+    for (int i = 0; i < UG; ++i) wcol[i] = gc.col(eu[i], H);
     for (int h0 = lane; h0 < H; h0 += 32 * RU) {
       float xv[RU], wv[RU][UG];
 #pragma unroll
@@ -338,7 +359,9 @@ __device__ __forceinline__ void warp_rescore(const Tok<NV> &s, float (&ex_hi)[NV
         xv[r] = in ? __bfloat162float(xr[hh]) : 0.f;
 #pragma unroll
         for (int i = 0; i < UG; ++i)
-          wv[r][i] = (in && eu[i] >= 0) ? __bfloat162float(wg[(size_t)hh * E + eu[i]]) : 0.f;
+          wv[r][i] = (in && wcol[i] >= 0)
+                         ? __bfloat162float(gc.base[(size_t)wcol[i] + (size_t)hh * gc.stride])
+                         : 0.f;
       }
 #pragma unroll
       for (int r = 0; r < RU; ++r)
@@ -377,6 +400,7 @@ __device__ __forceinline__ void tok_finish(const Tok<NV> &s, int t, int lane,
                                            const float *ex_hi_l, const float *ex_lo_l,
                                            const __nv_bfloat16 *__restrict__ x,
                                            const __nv_bfloat16 *__restrict__ wg,
+                                           const __nv_bfloat16 *__restrict__ wgt,
                                            const float *__restrict__ bias, int E, int H, int norm,
                                            int32_t *__restrict__ topk_idx,
                                            float *__restrict__ topk_w) {
@@ -403,7 +427,7 @@ __device__ __forceinline__ void tok_finish(const Tok<NV> &s, int t, int lane,
         nunc += __popc(s.ub[j]);
       }
     } else {
-      warp_rescore<NV>(s, ex_hi, ex_lo, lane, x + (size_t)t * H, wg, bias, E, H);
+      warp_rescore<NV>(s, ex_hi, ex_lo, lane, x + (size_t)t * H, wg, wgt, bias, E, H);
     }
     // an uncertain position moves inside its run by (members ranked above it
     // by the exact values) - (members before it)
@@ -474,6 +498,7 @@ __device__ __forceinline__ void tok_finish(const Tok<NV> &s, int t, int lane,
 template <int EG, int K, int MT, int S, int STAGES>
 __device__ __forceinline__ void route_tile(const __nv_bfloat16 *__restrict__ x,
                                            const __nv_bfloat16 *__restrict__ wg,
+                                           const __nv_bfloat16 *__restrict__ wgt,
                                            const float *__restrict__ bias,
                                            float *__restrict__ logits,
                                            int32_t *__restrict__ topk_idx,
@@ -485,7 +510,8 @@ __device__ __forceinline__ void route_tile(const __nv_bfloat16 *__restrict__ x,
 template <int EG, int K, int MT, int S, int STAGES>
 __global__ void __launch_bounds__(RM_THREADS)
     router_mma_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ wg,
-                      const float *__restrict__ bias, float *__restrict__ logits,
+                      const __nv_bfloat16 *__restrict__ wgt, const float *__restrict__ bias,
+                      float *__restrict__ logits,
                       int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int n, int H,
                       int norm, float tau_rel) {
   static_assert(STAGES >= 2 && S % 64 == 0, "stages of whole 128-byte x rows");
@@ -495,14 +521,15 @@ __global__ void __launch_bounds__(RM_THREADS)
   const int ntile = (n + TOK - 1) / TOK;
   for (int tile = blockIdx.x; tile < ntile; tile += gridDim.x) {
     if (tile != (int)blockIdx.x) __syncthreads();  // the previous tile is done with smem
-    route_tile<EG, K, MT, S, STAGES>(x, wg, bias, logits, topk_idx, topk_w, n, H, norm, tau_rel,
-                                     tile * TOK, rm_smem);
+    route_tile<EG, K, MT, S, STAGES>(x, wg, wgt, bias, logits, topk_idx, topk_w, n, H, norm,
+                                     tau_rel, tile * TOK, rm_smem);
   }
 }
 
 template <int EG, int K, int MT, int S, int STAGES>
 __device__ __forceinline__ void route_tile(const __nv_bfloat16 *__restrict__ x,
                                            const __nv_bfloat16 *__restrict__ wg,
+                                           const __nv_bfloat16 *__restrict__ wgt,
                                            const float *__restrict__ bias,
                                            float *__restrict__ logits,
                                            int32_t *__restrict__ topk_idx,
@@ -692,6 +719,14 @@ __device__ __forceinline__ void route_tile(const __nv_bfloat16 *__restrict__ x,
       DF a[RM_UG];
 #pragma unroll
       for (int i = 0; i < RM_UG; ++i) a[i] = DF{0.f, 0.f};
+      const GateCols gc = gate_cols(wg, wgt, E);
+      int wcol[RM_UG];
+      int my_e = -1;  // thread tid < RM_UG adds up entry d0 + tid below
+#pragma unroll
+      for (int i = 0; i < RM_UG; ++i) {
+        wcol[i] = gc.col(ee[i], H);
+        if (tid == i) my_e = ee[i];
+      }
       for (int h0 = 0; h0 < H; h0 += RM_THREADS * RM_RB) {
         float xv[RM_RB][RM_UG], wv[RM_RB][RM_UG];
 #pragma unroll
@@ -699,9 +734,10 @@ __device__ __forceinline__ void route_tile(const __nv_bfloat16 *__restrict__ x,
           const int h = h0 + rr * RM_THREADS + tid;
 #pragma unroll
           for (int i = 0; i < RM_UG; ++i) {
-            const bool in = h < H && ee[i] >= 0;
+            const bool in = h < H && wcol[i] >= 0;
             xv[rr][i] = in ? __bfloat162float(xr[i][h]) : 0.f;
-            wv[rr][i] = in ? __bfloat162float(wg[(size_t)h * E + ee[i]]) : 0.f;
+            wv[rr][i] = in ? __bfloat162float(gc.base[(size_t)wcol[i] + (size_t)h * gc.stride])
+                           : 0.f;
           }
         }
 #pragma unroll
@@ -722,12 +758,12 @@ __device__ __forceinline__ void route_tile(const __nv_bfloat16 *__restrict__ x,
         }
       }
       __syncthreads();
-      if (tid < RM_UG && ee[tid] >= 0) {  // the warps' partial sums in order, then the bias
+      if (tid < RM_UG && my_e >= 0) {  // the warps' partial sums in order, then the bias
         DF sum{0.f, 0.f};
         for (int w = 0; w < RM_WARPS; ++w)
           sum = df_add(sum, DF{part_hi[w * RM_UG + tid], part_lo[w * RM_UG + tid]});
         if (bias) {
-          const float bb = bias[ee[tid]];
+          const float bb = bias[my_e];
           sum = isinf(bb) ? DF{bb, 0.f} : df_add(sum, DF{bb, 0.f});
         }
         ex_hi[d0 + tid] = sum.hi;
@@ -739,7 +775,7 @@ __device__ __forceinline__ void route_tile(const __nv_bfloat16 *__restrict__ x,
 #pragma unroll
     for (int i = 0; i < 2; ++i)
       if (tl[i] < nvalid)
-        tok_finish<NV, K>(st[i], t0 + tl[i], lane, ex_hi, ex_lo, x, wg, bias, E, H, norm,
+        tok_finish<NV, K>(st[i], t0 + tl[i], lane, ex_hi, ex_lo, x, wg, wgt, bias, E, H, norm,
                           topk_idx, topk_w);
   }
 }
@@ -784,8 +820,9 @@ cudaError_t launch_cfg(const Desc &d, const void *x, const void *w_gate, const f
   const int grid = guest && tiles > sms ? sms : tiles;
   return launch_k(guest, kernel, dim3(grid), dim3(RM_THREADS), (size_t)smem, s,
                   reinterpret_cast<const __nv_bfloat16 *>(x),
-                  reinterpret_cast<const __nv_bfloat16 *>(w_gate), bias, logits, topk_idx, topk_w,
-                  d.n, d.H, d.norm ? 1 : 0, tie_margin_tc(d.H));
+                  reinterpret_cast<const __nv_bfloat16 *>(w_gate),
+                  reinterpret_cast<const __nv_bfloat16 *>(d.w_gate_t), bias, logits, topk_idx,
+                  topk_w, d.n, d.H, d.norm ? 1 : 0, tie_margin_tc(d.H));
 }
 
 template <int EG, int K>

@@ -123,7 +123,8 @@ __device__ __forceinline__ bool ranks_above(float v, int e, float w, int f) {
 template <int KM>
 __global__ void __launch_bounds__(RR_THREADS)
     router_rescore_kernel(const __nv_bfloat16 *__restrict__ x,
-                          const __nv_bfloat16 *__restrict__ wg, const float *__restrict__ bias,
+                          const __nv_bfloat16 *__restrict__ wg,
+                          const __nv_bfloat16 *__restrict__ wgt, const float *__restrict__ bias,
                           const float *__restrict__ logits, int32_t *__restrict__ topk_idx,
                           float *__restrict__ topk_w, int n, int H, int E, int norm,
                           float tau_rel) {
@@ -219,7 +220,10 @@ __global__ void __launch_bounds__(RR_THREADS)
       DF acc{0.f, 0.f};
       if (s_id < U) {
         const __nv_bfloat16 *xr = x + (size_t)t * H;
-        const __nv_bfloat16 *wc = wg + ue[s_id];
+        // expert ue[s_id]'s column of W_gate: a contiguous row of the
+        // transposed copy when there is one, else every E-th value of W_gate
+        const __nv_bfloat16 *wc = wgt ? wgt + (size_t)ue[s_id] * H : wg + ue[s_id];
+        const size_t ws = wgt ? 1 : (size_t)E;
         const int nrows = (H - g_id + G - 1) / G;  // rows g_id + i * G, i < nrows
         DF a4[4] = {DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}};
         float xv[8], wv[8];
@@ -228,7 +232,7 @@ __global__ void __launch_bounds__(RR_THREADS)
           const bool in = u < nrows;
           const int h = g_id + u * G;
           xv[u] = in ? __bfloat162float(xr[h]) : 0.f;
-          wv[u] = in ? __bfloat162float(wc[(size_t)h * E]) : 0.f;
+          wv[u] = in ? __bfloat162float(wc[(size_t)h * ws]) : 0.f;
         }
         for (int i0 = 0; i0 < nrows; i0 += 8) {
           float xn[8], wn[8];
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(RR_THREADS)
             const bool in = i < nrows;
             const int h = g_id + i * G;
             xn[u] = in ? __bfloat162float(xr[h]) : 0.f;
-            wn[u] = in ? __bfloat162float(wc[(size_t)h * E]) : 0.f;
+            wn[u] = in ? __bfloat162float(wc[(size_t)h * ws]) : 0.f;
           }
 #pragma unroll
           for (int u = 0; u < 8; ++u) a4[u & 3] = df_add(a4[u & 3], two_prod(xv[u], wv[u]));
@@ -699,8 +703,9 @@ cudaError_t launch_router_tc(const Desc &d, const void *x, const void *w_gate, c
     e = cudaLaunchKernelEx(&cfg, kernel, mX, mW, bias, logits, topk_idx, topk_w, d.n, d.H, d.E,
                            d.norm ? 1 : 0, idesc, cols, status);
     if (e != cudaSuccess) return e;
-    return launch_pdl(rescore, dim3(rgrid), dim3(RR_THREADS), 0, s, xb, wb, bias, logits, topk_idx,
-                      topk_w, d.n, d.H, d.E, d.norm ? 1 : 0, tau_rel);
+    return launch_pdl(rescore, dim3(rgrid), dim3(RR_THREADS), 0, s, xb, wb,
+                      reinterpret_cast<const __nv_bfloat16 *>(d.w_gate_t), bias, logits,
+                      topk_idx, topk_w, d.n, d.H, d.E, d.norm ? 1 : 0, tau_rel);
   };
 #define MOE_RT_CASE(KK)                                                                    \
   case KK:                                                                                 \
