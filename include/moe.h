@@ -99,8 +99,8 @@ typedef struct {
    * memory made by moe_prepare_router from the w_gate passed to the calls,
    * or NULL.  The router's exact near-tie rescoring then reads each expert's
    * column of w_gate as one contiguous row of this copy instead of H
-   * scattered values; the results are bitwise the same.  Ignored for float32
-   * layers. */
+   * scattered values; the results are bitwise the same.  16-byte aligned
+   * (else MOE_ERR_INVALID_ARG from every call).  Ignored for float32 layers. */
   const void *w_gate_t;
 } moe_layer_desc_t;
 
@@ -425,8 +425,9 @@ moe_status_t moe_prepare_weights(const moe_layer_desc_t *desc, const void *w13, 
 /*
  * One-time transform of the router weight (bf16 layers): w_gate_t[e][h] =
  * w_gate[h][e], (E, H) bf16, for moe_layer_desc_t.w_gate_t.  w_gate_t must
- * not overlap w_gate.  Enqueued on `stream`.  MOE_ERR_UNSUPPORTED for float32
- * layers; MOE_ERR_INVALID_ARG for NULL pointers.
+ * not overlap w_gate and must be 16-byte aligned.  Enqueued on `stream`.
+ * MOE_ERR_UNSUPPORTED for float32 layers; MOE_ERR_INVALID_ARG for NULL or
+ * misaligned pointers.
  */
 moe_status_t moe_prepare_router(const moe_layer_desc_t *desc, const void *w_gate,
                                 void *w_gate_t, moe_stream_t stream);

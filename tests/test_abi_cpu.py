@@ -247,5 +247,11 @@ def test_tiled_weights_rejected_where_unsupported(lib):
     assert lib.moe_prepare_router(ctypes.byref(d), None, None, None) == 1
     d = M.make_desc(16, 64, 32, 4, 2, "f32", True)
     assert lib.moe_prepare_router(ctypes.byref(d), None, None, None) == 2
-    # the descriptor carries the optional transposed router weight pointer
+    # the descriptor carries the optional transposed router weight pointer,
+    # 16-byte aligned
     assert M.LayerDesc.w_gate_t.offset == 32
+    d = M.make_desc(16, 256, 128, 8, 2, "bf16", True)
+    d.w_gate_t = 0x1008
+    assert lib.moe_workspace_size(ctypes.byref(d)) == 0
+    d.w_gate_t = 0x1000
+    assert lib.moe_workspace_size(ctypes.byref(d)) > 0

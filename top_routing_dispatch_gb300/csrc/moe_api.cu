@@ -44,6 +44,8 @@ moe_status_t check_desc(const moe_layer_desc_t *d, Desc *out) {
   if (d->weight_layout != MOE_WEIGHTS_ROW_MAJOR && d->weight_layout != MOE_WEIGHTS_TILED)
     return MOE_ERR_INVALID_ARG;
   if (d->E > kMaxE || d->K > kMaxK) return MOE_ERR_UNSUPPORTED;
+  // the transposed router weight is read in 16-byte pieces
+  if (d->w_gate_t && (reinterpret_cast<uintptr_t>(d->w_gate_t) & 15)) return MOE_ERR_INVALID_ARG;
   if ((long long)d->n * d->K > 0x7fffffffll) return MOE_ERR_UNSUPPORTED;
   const bool bf16 = d->dtype == MOE_BF16;
   // rows move as 16-byte vectors
@@ -708,7 +710,8 @@ moe_status_t moe_prepare_router(const moe_layer_desc_t *desc, const void *w_gate
   moe_status_t st = check_desc(desc, &d);
   if (st != MOE_OK) return st;
   if (!d.bf16) return MOE_ERR_UNSUPPORTED;
-  if (!w_gate || !w_gate_t) return MOE_ERR_INVALID_ARG;
+  if (!w_gate || !w_gate_t || (reinterpret_cast<uintptr_t>(w_gate_t) & 15))
+    return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_prepare_router(d, w_gate, w_gate_t, stream));
 }
 
