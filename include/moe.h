@@ -462,6 +462,24 @@ moe_status_t moe_set_pipeline_wait_limit(long long cycles);
 moe_status_t moe_set_gemm_pairs(int enable);
 
 /*
+ * Tuning control of the forward grouped GEMMs on CTA pairs
+ * (moe_expert_gemm1_swiglu, moe_expert_gemm2, moe_expert_gemm2_weighted and
+ * the forward's GEMMs; without effect on single CTAs and on the backward):
+ * "fused tails".  An expert whose segment ends 1..32 rows past a 256-row
+ * window boundary, after at least one full window, computes those rows inside
+ * its last full window's tiles, transposed: per k stage the pair adds
+ * M = 256, N = 32 MMAs that reuse the stage's weight columns as A and take
+ * the tail rows as B, instead of a 256-row window of their own (Algorithm 2
+ * steps 8-9 of "MoE 分布式推理基础（基于 vLLM）" §1.2 are unchanged: every row
+ * is multiplied by its expert's weights).  mode < 0 (the default) chooses per
+ * launch: on when the layer averages 192..384 rows per expert (n*K/E), where
+ * about half of the experts save a window; mode == 0 never, mode > 0 always.
+ * The results are bitwise the same either way.  Applies to launches enqueued
+ * after the call, from any host thread.  Always returns MOE_OK.
+ */
+moe_status_t moe_set_gemm_tails(int mode);
+
+/*
  * Blocks until `stream` is idle, then reads *status_word and maps it to
  * MOE_OK, MOE_ERR_BAD_ROUTING, MOE_ERR_BAD_LAYOUT or MOE_ERR_TIMEOUT (first
  * match in that order).  Intended for tests and debugging.

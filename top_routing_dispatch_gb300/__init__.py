@@ -14,4 +14,5 @@ from .api import (  # noqa: E402,F401
     moe_grouped_swiglu, moe_layout_workspace_size, moe_permute, moe_permute_scatter, moe_route_topk,
     moe_workspace_size, moe_workspace_slot, workspace_view, kernels_per_forward,
     moe_prepare_weights, moe_set_pipeline_wait_limit, moe_set_gemm_pairs, moe_prepare_router,
+    moe_set_gemm_tails,
 )

@@ -20,7 +20,7 @@ SYMBOLS = (
     "moe_host_workspace_size", "moe_forward_host", "moe_expert_gemm2_weighted",
     "moe_combine_slots", "moe_backward_workspace_size", "moe_backward",
     "moe_set_pipeline_wait_limit", "moe_prepare_weights", "moe_set_gemm_pairs",
-    "moe_prepare_router",
+    "moe_prepare_router", "moe_set_gemm_tails",
 )
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -75,6 +75,7 @@ def _declare(lib):
         "moe_check_status": (_st, [_vp, _vp]),
         "moe_set_pipeline_wait_limit": (_st, [ctypes.c_longlong]),
         "moe_set_gemm_pairs": (_st, [ctypes.c_int]),
+        "moe_set_gemm_tails": (_st, [ctypes.c_int]),
         "moe_prepare_weights": (_st, [_desc_p, _vp, _vp, _vp, _vp, _vp]),
         "moe_prepare_router": (_st, [_desc_p, _vp, _vp, _vp]),
         "moe_host_workspace_size": (ctypes.c_size_t, [_desc_p]),

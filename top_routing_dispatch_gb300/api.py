@@ -232,6 +232,14 @@ def moe_set_gemm_pairs(enable):
     _check(_lib.load().moe_set_gemm_pairs(1 if enable else 0), "moe_set_gemm_pairs")
 
 
+def moe_set_gemm_tails(mode):
+    """Tuning control of the forward pair GEMMs' fused tails: None (the
+    default) chooses per launch, False never, True always; the results are
+    bitwise the same."""
+    m = -1 if mode is None else (1 if mode else 0)
+    _check(_lib.load().moe_set_gemm_tails(m), "moe_set_gemm_tails")
+
+
 def moe_check_status(status_word, stream=None) -> int:
     """Synchronises `stream` and returns the mapped status code (0 = OK)."""
     return int(_lib.load().moe_check_status(_p(status_word), _stream(stream)))

@@ -89,6 +89,9 @@ cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const 
 // are selected (moe_set_gemm_pairs); bitwise the same results.
 void set_gemm_single_cta(bool single);
 bool gemm_single_cta();
+// Fused tails of the forward pair GEMMs (moe_set_gemm_tails): -1 automatic,
+// 0 off, 1 on.
+void set_gemm_tails(int mode);
 // GEMM2 with the routing weight applied and each row written to its
 // (token, slot) position: y_slot[perm[r]] = topk_w[perm[r]] * (h W2[e])[r]
 cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w2,

@@ -20,7 +20,9 @@
 // four 48 KB stages (A + four B boxes).  CTA pairs (PAIR, the default): one
 // cluster of two CTAs per two SMs, 256x256x16 cta_group::2 MMAs issued by the
 // even CTA, each CTA holding its own 128 A rows and half of the weight tile
-// (two B boxes), six 32 KB stages (see the kernel's comment for the protocol).
+// (two B boxes), six 32 KB stages (see the kernel's comment for the protocol);
+// in the forward modes optionally with fused tails (TAILS: an expert's last
+// 1..32 rows computed transposed inside its last full window's tiles).
 // A tile is (m-tile, n-tile).  m-tiles are 128-row windows that start at each
 // expert's segment start, so every tile belongs to exactly one expert; its
 // rows past the segment end are computed but not stored (TMA zero-fills rows
@@ -71,37 +73,73 @@ constexpr int threads_for(int mode) {
   return mode == 3 ? NUM_THREADS + 32 * GATHER_WARPS : NUM_THREADS;
 }
 constexpr int TMEM_COLS = 512;                      // two 256-column accumulators
+// epilogue staging per warp: 32 rows of 80 B (bf16 output rows)
 constexpr int EPI_ROW_BYTES = 80, EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
+// GEMM1 tails: a gate warp's 32 x 32 SiLU values for its up warp, 144-byte rows
+constexpr int XCH_ROW_BYTES = 144, XCH_WARP_BYTES = 32 * XCH_ROW_BYTES;
+
+// Fused tails (CTA pairs, forward modes 1, 2 and 4).  An expert whose
+// segment ends 1..TAIL_ROWS rows past a 256-row window boundary, after at
+// least one full window, computes those rows inside its last full window's
+// tiles, transposed: in every k stage, beside the tile's 256 x 256 MMAs, the
+// leader issues M = 256, N = TAIL_ROWS MMAs that take the same weight columns
+// (each CTA's 128, MN-major) as A and the tail rows (TAIL_HALF per CTA,
+// K-major) as B, accumulating D^T into the first TAIL_ROWS columns of the
+// other TMEM accumulator.  The tail adds MMAs (an N = 32 MMA takes about
+// 0.4 of an N = 256 one: it reads the same A) but no weight traffic, where a
+// window of its own would repeat the whole tile.  The epilogue releases each
+// accumulator's first TAIL_ROWS columns (its "head") apart from the rest, as
+// soon as it has read them, and drains a tail before its tile's own
+// accumulator, so a tile with a tail waits only for the head of the other
+// accumulator.  A kernel variant (TAILS); launches choose it by the layer's
+// rows per expert (tails_auto).
+constexpr int TAIL_ROWS = 32, TAIL_HALF = TAIL_ROWS / 2;
+constexpr int TAIL_BYTES = TAIL_HALF * BK * 2;  // 2 KB per CTA and stage
+__host__ __device__ constexpr bool tail_mode(int mode) {
+  return mode == 1 || mode == 2 || mode == 4;
+}
 
 struct SmemTail {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t hempty[2];  // TAILS: columns [0, TAIL_ROWS) of the accumulator read
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
   int ok;
   int total_mtiles;
   int own_issued[kMaxStages];   // PAIR: phases this CTA's producer loaded, per stage
+  int own_bytes[kMaxStages];    // PAIR: bytes per CTA of the last phase loaded, per stage
   int peer_issued[kMaxStages];  // PAIR (leader): the odd CTA's own_issued
+  int peer_bytes[kMaxStages];   // PAIR (leader): the odd CTA's own_bytes
+  int epi_ok[4];                // GEMM1 tails: each epilogue warp's go-ahead
   int off[kMaxE + 1];
   int tp[kMaxE + 1];  // first m-tile of each expert (exclusive prefix)
   alignas(16) uint8_t epi[4][EPI_WARP_BYTES];  // per epilogue warp staging
 };
 
-template <bool PAIR>
+// TAILS: the stages are followed by a TAIL_BYTES slot per stage for the fused
+// tail rows and the two gate warps' exchange buffers
+template <bool PAIR, bool TAILS = false>
+__host__ __device__ constexpr size_t tails_bytes() {
+  return TAILS ? (size_t)Pipe<PAIR>::STAGES * TAIL_BYTES + 2 * XCH_WARP_BYTES : 0;
+}
+template <bool PAIR, bool TAILS = false>
 constexpr size_t smem_bytes() {
   return 1024 /*alignment slack*/ + (size_t)Pipe<PAIR>::STAGES * Pipe<PAIR>::STAGE +
-         sizeof(SmemTail);
+         tails_bytes<PAIR, TAILS>() + sizeof(SmemTail);
 }
 constexpr size_t SMEM_BYTES = smem_bytes<false>();
-static_assert(smem_bytes<true>() <= 227 * 1024, "pair pipeline exceeds shared memory");
+static_assert(smem_bytes<true, true>() <= 227 * 1024, "pair pipeline exceeds shared memory");
 
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/true);
 constexpr uint32_t IDESC_KB = ptx::idesc_bf16_f32(BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/false);
 constexpr uint32_t IDESC_PAIR = ptx::idesc_bf16_f32(2 * BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/true);
 constexpr uint32_t IDESC_PAIR_KB = ptx::idesc_bf16_f32(2 * BM, UMMA_N, /*a_mn=*/false, /*b_mn=*/false);
+// fused tail: A = the weight columns (MN-major), B = the tail rows (K-major)
+constexpr uint32_t IDESC_TAIL = ptx::idesc_bf16_f32(2 * BM, TAIL_ROWS, /*a_mn=*/true, /*b_mn=*/false);
 
 // A pipeline wait: gives up after `limit` cycles (setting the abort flag and
 // MOE_DEV_TIMEOUT), or at once when another role has given up.
@@ -123,12 +161,28 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
 
 struct TileInfo {
   int e, row0, rows, nt;
+  int tail, t0;  // fused tail: its rows (0: none) and first row
 };
+
+// TAILS: the expert's rows past its last full window (1..TAIL_ROWS of them)
+// are fused into that window's tiles
+template <bool PAIR, bool TAILS>
+__host__ __device__ constexpr bool fused_tail(int len) {
+  return PAIR && TAILS && len > Pipe<PAIR>::TILE_ROWS && len % Pipe<PAIR>::TILE_ROWS != 0 &&
+         len % Pipe<PAIR>::TILE_ROWS <= TAIL_ROWS;
+}
+// m-tiles of an expert with len rows
+template <bool PAIR, bool TAILS>
+__host__ __device__ constexpr int mtiles_of(int len) {
+  return len > 0 ? (len + Pipe<PAIR>::TILE_ROWS - 1) / Pipe<PAIR>::TILE_ROWS -
+                       (fused_tail<PAIR, TAILS>(len) ? 1 : 0)
+                 : 0;
+}
 
 // Tile t: expert, first row and stored rows of this CTA's 128-row part
 // (PAIR: rank 0 takes rows [0, 128) of the pair's 256-row window, rank 1 rows
 // [128, 256); rows may be <= 0 when the segment ends in the first half).
-template <bool PAIR = false>
+template <bool PAIR = false, bool TAILS = false>
 __device__ __forceinline__ TileInfo decode_tile(const SmemTail &s, int t, int n_tiles, int E,
                                                 int rank = 0) {
   TileInfo ti;
@@ -143,10 +197,55 @@ __device__ __forceinline__ TileInfo decode_tile(const SmemTail &s, int t, int n_
       hi = mid;
   }
   ti.e = lo;
-  ti.row0 = s.off[lo] + (mt - s.tp[lo]) * Pipe<PAIR>::TILE_ROWS + rank * BM;
+  const int j = mt - s.tp[lo];
+  const int w0 = s.off[lo] + j * Pipe<PAIR>::TILE_ROWS;
+  ti.row0 = w0 + rank * BM;
   const int left = s.off[lo + 1] - ti.row0;
   ti.rows = left < BM ? left : BM;
+  ti.tail = 0;
+  ti.t0 = 0;
+  if constexpr (PAIR && TAILS) {
+    const int len = s.off[lo + 1] - s.off[lo];
+    if (fused_tail<PAIR, TAILS>(len) && j == len / Pipe<PAIR>::TILE_ROWS - 1) {
+      ti.t0 = w0 + Pipe<PAIR>::TILE_ROWS;
+      ti.tail = s.off[lo + 1] - ti.t0;
+    }
+  }
   return ti;
+}
+
+// Barrier of the gate warp q and the up warp q + 2 (q = 0, 1) in a GEMM1
+// tail's epilogue: named barrier 1 or 2, 64 threads.
+__device__ __forceinline__ void epi_pair_bar(int q) {
+  if (q & 1)
+    ptx::named_bar_sync<2, 64>();
+  else
+    ptx::named_bar_sync<1, 64>();
+}
+
+
+// One epilogue warp's arrival (lane 0) on accumulator barrier bars[a]; the odd
+// CTA of a pair arrives on the leader's (remote0: its bars[0] in the cluster).
+__device__ __forceinline__ void epi_arrive(uint64_t *bars, uint32_t remote0, int a, bool remote) {
+  if (remote)
+    ptx::mbar_arrive_cluster(remote0 + 8u * (uint32_t)a);
+  else
+    ptx::mbar_arrive(&bars[a]);
+}
+// The warp has read accumulator a's head (its first TAIL_ROWS columns).  The
+// arrival is relaxed: the reads are complete (tcgen05.wait::ld) and ordered
+// before it (tcgen05.fence::before_thread_sync), and no memory write of the
+// warp needs to reach the waiting MMA issuer.
+__device__ __forceinline__ void head_release(uint64_t *bars, uint32_t remote0, int a, bool remote,
+                                             int lane) {
+  ptx::tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    if (remote)
+      ptx::mbar_arrive_cluster_relaxed(remote0 + 8u * (uint32_t)a);
+    else
+      ptx::mbar_arrive_relaxed(&bars[a]);
+  }
 }
 
 // MODE 3: perm entry of tile row rr (0 past the segment: such rows are never
@@ -179,13 +278,9 @@ __device__ __forceinline__ float silu(float g) {
 
 // my_dst: the output row of this lane's tile row (-1: do not store); the
 // destination of tile row `row` is fetched from its lane.
-__device__ __forceinline__ void store_tile_chunk(uint8_t *wbuf, const uint32_t (&pk)[16], int lane,
-                                                 __nv_bfloat16 *out, size_t ld, int my_dst,
-                                                 int rows, int col0) {
-  uint4 *mine = reinterpret_cast<uint4 *>(wbuf + lane * EPI_ROW_BYTES);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) mine[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-  __syncwarp();
+// Stores the staged 32 rows x 64 B: row r goes to out[dst of lane r] at col0.
+__device__ __forceinline__ void store_staged(const uint8_t *wbuf, int lane, __nv_bfloat16 *out,
+                                             size_t ld, int my_dst, int rows, int col0) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int p = lane + 32 * i;
@@ -197,6 +292,29 @@ __device__ __forceinline__ void store_tile_chunk(uint8_t *wbuf, const uint32_t (
     }
   }
   __syncwarp();
+}
+
+__device__ __forceinline__ void store_tile_chunk(uint8_t *wbuf, const uint32_t (&pk)[16], int lane,
+                                                 __nv_bfloat16 *out, size_t ld, int my_dst,
+                                                 int rows, int col0) {
+  uint4 *mine = reinterpret_cast<uint4 *>(wbuf + lane * EPI_ROW_BYTES);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) mine[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+  __syncwarp();
+  store_staged(wbuf, lane, out, ld, my_dst, rows, col0);
+}
+
+// Fused tails: this lane holds one output column (col0 + lane) for 32
+// consecutive rows; staged as row i = those rows' 32 columns, then stored
+// like a row-major chunk.
+__device__ __forceinline__ void store_tile_chunk_t(uint8_t *wbuf, const float (&v)[32], int lane,
+                                                   __nv_bfloat16 *out, size_t ld, int my_dst,
+                                                   int rows, int col0) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    *reinterpret_cast<__nv_bfloat16 *>(wbuf + i * EPI_ROW_BYTES + lane * 2) = __float2bfloat16_rn(v[i]);
+  __syncwarp();
+  store_staged(wbuf, lane, out, ld, my_dst, rows, col0);
 }
 
 // modes whose B is W13's gate/up column pairs (n-tile = 128 h columns)
@@ -225,10 +343,11 @@ __host__ __device__ constexpr bool kmajor_b(int mode) { return mode == 5; }
 // Each CTA drains the accumulator rows in its own TMEM.  Before the pair
 // leaves, the leader settles every stage whose two halves were not both
 // issued (a side that gave up early) and waits until every copy has landed.
-template <int MODE, bool PAIR = false>
+template <int MODE, bool PAIR = false, bool TAILS = false>
 __global__ void __launch_bounds__(threads_for(MODE), 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmA2,
                            const int32_t *__restrict__ offsets, int E, int nK, int Kdim, int I,
                            int Nout, __nv_bfloat16 *__restrict__ out, int32_t *status,
                            const int32_t *__restrict__ perm, int Kslots,
@@ -237,6 +356,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                            const __nv_bfloat16 *__restrict__ aux, long long wait_limit,
                            int b_nb) {
   static_assert(!PAIR || MODE != 3, "CTA pairs: not with the cp.async gather of mode 3");
+  static_assert(!TAILS || (PAIR && tail_mode(MODE)), "fused tails: CTA pairs, forward modes");
   using P = Pipe<PAIR>;
   constexpr int STAGES = P::STAGES;
   pdl_enter();
@@ -247,7 +367,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   // operand read of a stage stays inside the CTA's operand area
   uint8_t *smemA = PAIR ? smem + STAGES * P::B_STAGE : smem;
   uint8_t *smemB = PAIR ? smem : smem + STAGES * A_STAGE_BYTES;
-  SmemTail &st = *reinterpret_cast<SmemTail *>(smem + STAGES * P::STAGE);
+  uint8_t *smemT = smem + STAGES * P::STAGE;  // TAILS: the fused tail rows, per stage
+  uint8_t *xch = smemT + STAGES * TAIL_BYTES;  // TAILS: the gate warps' exchange buffers
+  SmemTail &st = *reinterpret_cast<SmemTail *>(smemT + tails_bytes<PAIR, TAILS>());
+  // PAIR, GEMM1: each CTA's half of the weight tile is 64 gate columns and the
+  // 64 matching up columns (a tail's SwiGLU then stays inside the CTA)
+  constexpr bool SPLIT_GU = PAIR && MODE == 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = gemm1_mode(MODE) ? I / 128 : (Nout + UMMA_N - 1) / UMMA_N;
@@ -268,9 +393,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&st.tfull[a], 1);
       ptx::mbar_init(&st.tempty[a], PAIR ? 8 : 4);  // the epilogue warps (of both CTAs)
+      ptx::mbar_init(&st.hempty[a], PAIR ? 8 : 4);
     }
     ptx::mbar_init(&st.drain, 1);
-    for (int s = 0; s < kMaxStages; ++s) st.own_issued[s] = st.peer_issued[s] = 0;
+    for (int s = 0; s < kMaxStages; ++s)
+      st.own_issued[s] = st.peer_issued[s] = st.own_bytes[s] = st.peer_bytes[s] = 0;
     st.abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -289,7 +416,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       const int len = st.off[e + 1] - st.off[e];
       ok = ok && len >= 0;
       st.tp[e] = run;
-      run += len > 0 ? (len + P::TILE_ROWS - 1) / P::TILE_ROWS : 0;
+      run += mtiles_of<PAIR, TAILS>(len);
     }
     st.tp[E] = run;
     st.total_mtiles = run;
@@ -321,19 +448,22 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     if (lane == 0) {
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB);
+      if (TAILS) ptx::prefetch_tmap(&tmA2);
       // the leader's operand-full barriers, as shared::cluster addresses
       const uint32_t full0 = ptx::mapa_shared(ptx::smem_u32(&st.full[0]), 0);
       int stage = 0;
       uint32_t phase = 0;
       for (int t = unit; t < total; t += units) {
-        const TileInfo ti = decode_tile<true>(st, t, n_tiles, E, rank);
+        const TileInfo ti = decode_tile<true, TAILS>(st, t, n_tiles, E, rank);
+        // bytes each CTA loads per stage
+        const int bytes = P::STAGE + (ti.tail ? TAIL_BYTES : 0);
         bool stop = false;
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_or_abort(&st.empty[stage], phase ^ 1u, abort_flag, status, wait_limit)) {
             stop = true;
             break;
           }
-          if (leader) ptx::mbar_arrive_expect_tx(&st.full[stage], 2 * P::STAGE);
+          if (leader) ptx::mbar_arrive_expect_tx(&st.full[stage], 2 * bytes);
           const uint32_t bar = full0 + 8u * (uint32_t)stage;
           // a part with no rows of the expert (segment ends in the first
           // half) loads the expert's first rows: computed, never stored
@@ -345,11 +475,13 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           } else {
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            // this CTA's half of the 256 B columns: GEMM1 gate (rank 0) or up
+            // this CTA's half of the 256 B columns: GEMM1 (mode 1) 64 gate and
+            // the 64 matching up columns, (mode 6) the gate (rank 0) or up
             // (rank 1) columns of the 128 h columns; GEMM2 columns 128 * rank
             const int q = 2 * rank + j;
-            const int ncol = gemm1_mode(MODE) ? (q < 2 ? 0 : I) + ti.nt * 128 + (q & 1) * 64
-                                              : ti.nt * UMMA_N + q * 64;
+            const int ncol = SPLIT_GU ? j * I + ti.nt * 128 + rank * 64
+                             : gemm1_mode(MODE) ? (q < 2 ? 0 : I) + ti.nt * 128 + (q & 1) * 64
+                                                : ti.nt * UMMA_N + q * 64;
             uint8_t *dst = smemB + stage * P::B_STAGE + j * B_BOX_BYTES;
             if (b_nb > 0)
               ptx::tma_load_2d_pair(dst, &tmB, bar, 0, ((ti.e * KB + kb) * b_nb + (ncol >> 6)) * 64);
@@ -357,7 +489,13 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
               ptx::tma_load_3d_pair(dst, &tmB, bar, ncol, kb * BK, ti.e);
           }
           }
+          // fused tail: this CTA's TAIL_HALF of the tail rows (rows past the
+          // tensor read zeros; rows of the next expert are never stored)
+          if (TAILS && ti.tail)
+            ptx::tma_load_2d_pair(smemT + stage * TAIL_BYTES, &tmA2, bar, kb * BK,
+                                  ti.t0 + rank * TAIL_HALF);
           ++st.own_issued[stage];
+          st.own_bytes[stage] = bytes;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -369,8 +507,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       // leaves: it needs the odd CTA's counts
       if (!leader) {
         const uint32_t dst0 = ptx::mapa_shared(ptx::smem_u32(&st.peer_issued[0]), 0);
-        for (int s2 = 0; s2 < STAGES; ++s2)
+        const uint32_t dstb = ptx::mapa_shared(ptx::smem_u32(&st.peer_bytes[0]), 0);
+        for (int s2 = 0; s2 < STAGES; ++s2) {
           ptx::st_cluster_u32(dst0 + 4u * s2, (uint32_t)st.own_issued[s2]);
+          ptx::st_cluster_u32(dstb + 4u * s2, (uint32_t)st.own_bytes[s2]);
+        }
       }
     }
   } else if (warp == 0) {
@@ -430,11 +571,40 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
-      uint32_t acc_phase = 0;
+      // bit a: parity of the uses so far of accumulator a (uses), and of its
+      // head (huses: the tiles on a, and the fused tails put there); use u
+      // waits for the epilogue's release u - 1
+      uint32_t uses = 0, huses = 0;
+      constexpr uint32_t idesc = PAIR ? (kmajor_b(MODE) ? IDESC_PAIR_KB : IDESC_PAIR)
+                                      : (kmajor_b(MODE) ? IDESC_KB : IDESC);
+      int e_cur = 0;  // expert of the current tile (a CTA's tiles come in increasing order)
       for (int t = unit; t < total; t += units) {
-        if (!wait_or_abort(&st.tempty[acc], acc_phase ^ 1u, abort_flag, status, wait_limit)) break;
+        bool tail = false;
+        if constexpr (TAILS) {
+          const int mt = t / n_tiles;
+          while (e_cur + 1 < E && st.tp[e_cur + 1] <= mt) ++e_cur;
+          const int len = st.off[e_cur + 1] - st.off[e_cur];
+          tail = fused_tail<PAIR, TAILS>(len) && mt - st.tp[e_cur] == len / P::TILE_ROWS - 1;
+        }
+        if (!wait_or_abort(&st.tempty[acc], (uses >> acc & 1u) ^ 1u, abort_flag, status,
+                           wait_limit))
+          break;
+        uses ^= 1u << acc;
+        if (TAILS) {
+          if (!wait_or_abort(&st.hempty[acc], (huses >> acc & 1u) ^ 1u, abort_flag, status,
+                             wait_limit))
+            break;
+          huses ^= 1u << acc;
+          if (tail) {  // the tail's D^T goes to the other accumulator's head
+            if (!wait_or_abort(&st.hempty[acc ^ 1], (huses >> (acc ^ 1) & 1u) ^ 1u, abort_flag,
+                               status, wait_limit))
+              break;
+            huses ^= 1u << (acc ^ 1);
+          }
+        }
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * UMMA_N);
+        const uint32_t dt = tmem + (uint32_t)((acc ^ 1) * UMMA_N);  // the tail's D^T
         bool stop = false;
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_or_abort(&st.full[stage], phase, abort_flag, status, wait_limit)) {
@@ -450,19 +620,28 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           const uint32_t b0 = ptx::smem_u32(smemB + stage * P::B_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // A: K-major SW128, k step of 16 elements = 32 bytes inside the atom
-            const uint64_t adesc = ptx::smem_desc(a0 + kk * 32, 16, 1024);
-            // B: MN-major SW128, 64-wide n atoms 8 KB apart, k step = 16 rows;
-            // or (mode 5) K-major SW128 like A, 256 n rows
-            const uint64_t bdesc = kmajor_b(MODE) ? ptx::smem_desc(b0 + kk * 32, 16, 1024)
+            // the activation rows: K-major SW128, k step of 16 elements = 32
+            // bytes inside the atom
+            const uint64_t xdesc = ptx::smem_desc(a0 + kk * 32, 16, 1024);
+            // the weights: MN-major SW128, 64-wide n atoms 8 KB apart, k step
+            // = 16 rows; or (mode 5) K-major SW128 like the rows, 256 n rows
+            const uint64_t wdesc = kmajor_b(MODE) ? ptx::smem_desc(b0 + kk * 32, 16, 1024)
                                                   : ptx::smem_desc(b0 + kk * 2048, B_BOX_BYTES, 1024);
-            // PAIR: each CTA's half of B is two of these atoms (128 n)
+            // PAIR: each CTA's half of the weights is two of these atoms (128 n)
             if constexpr (PAIR)
-              ptx::mma_bf16_pair(d, adesc, bdesc, kmajor_b(MODE) ? IDESC_PAIR_KB : IDESC_PAIR,
-                                 (kb | kk) != 0 ? 1u : 0u);
+              ptx::mma_bf16_pair(d, xdesc, wdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
             else
-              ptx::mma_bf16(d, adesc, bdesc, kmajor_b(MODE) ? IDESC_KB : IDESC,
-                            (kb | kk) != 0 ? 1u : 0u);
+              ptx::mma_bf16(d, xdesc, wdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          if (TAILS && tail) {
+            // the same weight atoms as the 256-row A operand (MN-major), the
+            // tail rows (TAIL_HALF per CTA, K-major) as a TAIL_ROWS-column B
+            const uint32_t r0 = ptx::smem_u32(smemT + stage * TAIL_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk)
+              ptx::mma_bf16_pair(dt, ptx::smem_desc(b0 + kk * 2048, B_BOX_BYTES, 1024),
+                                 ptx::smem_desc(r0 + kk * 32, 16, 1024), IDESC_TAIL,
+                                 (kb | kk) != 0 ? 1u : 0u);
           }
           // the stage is free in both CTAs once these MMAs have read it
           if constexpr (PAIR)
@@ -480,7 +659,6 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         else
           ptx::mma_commit(&st.tfull[acc]);
         acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
       }
       // wait until every MMA this thread issued has finished
       if constexpr (PAIR)
@@ -493,18 +671,102 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     // epilogue warps 2..5 -> TMEM lane quarter (warp % 4)
     const int q = warp & 3;
     int acc = 0;
-    uint32_t acc_phase = 0;
+    uint32_t fills = 0;  // bit a: parity of the fills of accumulator a drained so far
     // PAIR: the odd CTA's warps release the accumulator on the leader's barrier
     const uint32_t tempty0 = PAIR ? ptx::mapa_shared(ptx::smem_u32(&st.tempty[0]), 0) : 0u;
+    const uint32_t hempty0 = PAIR ? ptx::mapa_shared(ptx::smem_u32(&st.hempty[0]), 0) : 0u;
     for (int t = unit; t < total; t += units) {
-      const TileInfo ti = decode_tile<PAIR>(st, t, n_tiles, E, rank);
-      if (!wait_or_abort(&st.tfull[acc], acc_phase, abort_flag, status, wait_limit)) break;
+      const TileInfo ti = decode_tile<PAIR, TAILS>(st, t, n_tiles, E, rank);
+      const bool tail = TAILS && ti.tail > 0;
+      bool ok = wait_or_abort(&st.tfull[acc], fills >> acc & 1u, abort_flag, status, wait_limit);
+      if (gemm1_mode(MODE) && tail) {
+        // the gate and up warps of a GEMM1 tail wait on each other below:
+        // they go on together or not at all
+        const int wok = __all_sync(0xffffffffu, ok) ? 1 : 0;
+        if (lane == 0) st.epi_ok[q] = wok;
+        epi_pair_bar(q);
+        const volatile int *eo = st.epi_ok;
+        ok = eo[q & 1] && eo[(q & 1) + 2];
+      }
+      if (!ok) break;
+      fills ^= 1u << acc;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + (uint32_t)(acc * UMMA_N) + ((uint32_t)(q * 32) << 16);
+      uint8_t *wbuf = st.epi[q];
+      if (TAILS && tail) {
+        // first the fused tail's D^T, in the other accumulator's head: lane =
+        // weight column, TMEM column i = tail row t0 + i
+        const uint32_t tt = tmem + (uint32_t)((acc ^ 1) * UMMA_N) + ((uint32_t)(q * 32) << 16);
+        const int r = lane < ti.tail ? ti.t0 + lane : -1;  // this lane's tail row
+        if (gemm1_mode(MODE)) {
+          // warps 4, 5 (lanes 0-63) hold this CTA's 64 gate columns, warps 2,
+          // 3 (lanes 64-127) the matching up columns: each gate warp passes
+          // SiLU(gate) to its up warp through an exchange buffer
+          float4 *xrow =
+              reinterpret_cast<float4 *>(xch + (q & 1) * XCH_WARP_BYTES + lane * XCH_ROW_BYTES);
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(tt, v);
+          ptx::tmem_ld_wait();
+          // the other accumulator's head is free again
+          head_release(st.hempty, hempty0, acc ^ 1, PAIR && !leader, lane);
+          if (q < 2) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              xrow[i] = make_float4(silu(__uint_as_float(v[4 * i])), silu(__uint_as_float(v[4 * i + 1])),
+                                    silu(__uint_as_float(v[4 * i + 2])), silu(__uint_as_float(v[4 * i + 3])));
+            epi_pair_bar(q);  // staged
+            epi_pair_bar(q);  // read by the up warp
+          } else {
+            epi_pair_bar(q);
+            float hv[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 sv = xrow[i];
+              hv[4 * i] = sv.x * __uint_as_float(v[4 * i]);
+              hv[4 * i + 1] = sv.y * __uint_as_float(v[4 * i + 1]);
+              hv[4 * i + 2] = sv.z * __uint_as_float(v[4 * i + 2]);
+              hv[4 * i + 3] = sv.w * __uint_as_float(v[4 * i + 3]);
+            }
+            epi_pair_bar(q);
+            store_tile_chunk_t(wbuf, hv, lane, out, (size_t)I, r, ti.tail,
+                               ti.nt * 128 + rank * 64 + (q - 2) * 32);
+          }
+        } else {
+          const bool live = ti.nt * UMMA_N + rank * 128 + q * 32 < Nout;  // uniform across the warp
+          uint32_t a[32];
+          if (live) {
+            ptx::tmem_ld_32x32b_x32(tt, a);
+            ptx::tmem_ld_wait();
+          }
+          head_release(st.hempty, hempty0, acc ^ 1, PAIR && !leader, lane);
+          if (live) {
+            // this lane's tail row: its output row and routing weight (MODE 4)
+            int dst = r;
+            float wt = 1.f;
+            if (MODE == 4 && r >= 0) {
+              const int f = __ldg(perm + r);
+              if ((unsigned)f < (unsigned)nK) {
+                dst = f;
+                wt = __ldg(tw + f);
+              } else {
+                dst = -1;
+                flag_status(status, MOE_DEV_BAD_LAYOUT);
+              }
+            }
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              v[i] = __uint_as_float(a[i]);
+              if (MODE == 4) v[i] *= __shfl_sync(0xffffffffu, wt, i);
+            }
+            store_tile_chunk_t(wbuf, v, lane, out, (size_t)Nout, dst, ti.tail,
+                               ti.nt * UMMA_N + rank * 128 + q * 32);
+          }
+        }
+      }
       // rows of this warp's 32-row slice that belong to the tile's expert
       const int wrows = ti.rows - q * 32;
       const int wrow0 = ti.row0 + q * 32;
-      uint8_t *wbuf = st.epi[q];
       // output row of this lane's tile row, and its routing weight (MODE 4)
       int my_dst = wrow0 + lane;
       float wscale = 1.f;
@@ -523,11 +785,16 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       if (gemm1_mode(MODE)) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
+          // SPLIT_GU: accumulator columns [128 r, 128 r + 64) are the gate and
+          // [128 r + 64, 128 r + 128) the up columns of h columns [64 r, 64 r + 64)
+          const int gc = SPLIT_GU ? (c >> 1) * 128 + (c & 1) * 32 : c * 32;
+          const int uc = SPLIT_GU ? gc + 64 : 128 + c * 32;
           uint32_t g[32], u[32];
-          ptx::tmem_ld_32x32b_x32(tbase + c * 32, g);
-          ptx::tmem_ld_32x32b_x32(tbase + 128 + c * 32, u);
+          ptx::tmem_ld_32x32b_x32(tbase + gc, g);
+          ptx::tmem_ld_32x32b_x32(tbase + uc, u);
           ptx::tmem_ld_wait();
-          const int col = ti.nt * 128 + c * 32;
+          if (TAILS && c == 0) head_release(st.hempty, hempty0, acc, PAIR && !leader, lane);
+          const int col = ti.nt * 128 + (SPLIT_GU ? (c >> 1) * 64 + (c & 1) * 32 : c * 32);
           if (MODE == 6) {
             // SwiGLU backward: dG = dh U s (1 + G (1 - s)), dU = dh G s, s = sigmoid(G)
             float dh[32];
@@ -583,6 +850,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           uint32_t a[32];
           ptx::tmem_ld_32x32b_x32(tbase + c * 32, a);
           ptx::tmem_ld_wait();
+          if (TAILS && c == 0) head_release(st.hempty, hempty0, acc, PAIR && !leader, lane);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -599,14 +867,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        if (PAIR && !leader)
-          ptx::mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
-        else
-          ptx::mbar_arrive(&st.tempty[acc]);
-      }
+      if (lane == 0) epi_arrive(st.tempty, tempty0, acc, PAIR && !leader);
       acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
     }
   } else if (MODE == 3) {
     // cp.async gatherers: warp g fills tile rows [32g, 32g + 32).  Lane =
@@ -679,10 +941,10 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       // bytes, or its own arrival), then waits until every copy has landed.
       for (int s = 0; s < STAGES; ++s) {
         const int own = st.own_issued[s], peer = st.peer_issued[s];
-        if (own == peer + 1)
-          ptx::mbar_complete_tx(&st.full[s], P::STAGE);
+        if (own == peer + 1)  // both load the same tile in a phase: the same bytes
+          ptx::mbar_complete_tx(&st.full[s], (uint32_t)st.own_bytes[s]);
         else if (peer == own + 1)
-          ptx::mbar_arrive_expect_tx(&st.full[s], P::STAGE);
+          ptx::mbar_arrive_expect_tx(&st.full[s], (uint32_t)st.peer_bytes[s]);
         const int last = own > peer ? own : peer;
         if (last > 0) ptx::mbar_wait(&st.full[s], (uint32_t)(last - 1) & 1u);
       }
@@ -765,15 +1027,15 @@ bool weight_map(CUtensorMap *m, const void *w, const Desc &d, uint64_t rows, uin
   return make_map_3d(m, w, cols, rows, d.E, 64, BK);
 }
 
-template <int MODE, bool PAIR = false>
+template <int MODE, bool PAIR = false, bool TAILS = false>
 cudaError_t set_smem_attr() {
   static int done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, PAIR>,
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, PAIR, TAILS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_bytes<PAIR>());
+                                       (int)smem_bytes<PAIR, TAILS>());
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
   return e;
 }
@@ -786,9 +1048,29 @@ int gemm_grid(int sm_reserve) {
 // 0: CTA pairs for the grouped GEMMs (all modes but 3), 1: single CTAs
 // (moe_set_gemm_pairs)
 std::atomic<int> g_single_cta{0};
+// fused tails of the forward pair GEMMs (moe_set_gemm_tails): -1 chosen per
+// launch (tails_auto), 0 never, 1 always
+std::atomic<int> g_tails{-1};
+
+// Fused tails pay where a typical expert holds about one 256-row window and a
+// remainder: then a tail of at most 32 rows saves a whole window in about
+// half of the experts (measured: the grouped GEMMs of the DeepSeek-V3-sized
+// layer, 256 rows per expert on average, 16 % faster).  With two or more
+// windows per expert the saving is a smaller share, and the fused-tail kernel
+// runs its windows without a tail a few per cent slower (measured on the
+// OLMoE-shaped layer, 512 rows per expert: 7 % slower overall), so it is not
+// used there.
+bool tails_auto(long long nK, int E) {
+  const long long a = E > 0 ? nK / E : 0;
+  return a >= 192 && a <= 384;
+}
+bool use_tails(long long nK, int E) {
+  const int m = g_tails.load();
+  return m < 0 ? tails_auto(nK, E) : m != 0;
+}
 
 // CTA pairs of MODE's kernel that can be resident at once (cached per device)
-template <int MODE>
+template <int MODE, bool TAILS = false>
 cudaError_t pair_clusters(int *out) {
   static int cached[64] = {0};
   int dev = 0;
@@ -796,12 +1078,12 @@ cudaError_t pair_clusters(int *out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!cached[dev]) {
-    e = set_smem_attr<MODE, true>();
+    e = set_smem_attr<MODE, true, TAILS>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 16);
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = smem_bytes<true>();
+    cfg.dynamicSmemBytes = smem_bytes<true, TAILS>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -810,7 +1092,7 @@ cudaError_t pair_clusters(int *out) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int nc = 0;
-    e = cudaOccupancyMaxActiveClusters(&nc, grouped_gemm_tc_kernel<MODE, true>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&nc, grouped_gemm_tc_kernel<MODE, true, TAILS>, &cfg);
     if (e != cudaSuccess) return e;
     if (nc < 1) return cudaErrorInvalidConfiguration;
     cached[dev] = nc;
@@ -819,25 +1101,19 @@ cudaError_t pair_clusters(int *out) {
   return cudaSuccess;
 }
 
-// Persistent launch of a grouped GEMM: one CTA per SM, or (pairs) as many CTA
-// pairs as are resident at once within the SMs sm_reserve leaves.
-template <int MODE, typename... Args>
-cudaError_t launch_gemm(bool pair, int sm_reserve, cudaStream_t s, Args &&...args) {
-  if (!pair) {
-    cudaError_t e = set_smem_attr<MODE>();
-    if (e != cudaSuccess) return e;
-    return launch_pdl(grouped_gemm_tc_kernel<MODE>, dim3(gemm_grid(sm_reserve)),
-                      dim3(NUM_THREADS), SMEM_BYTES, s, static_cast<Args &&>(args)...);
-  }
+// Launch of the pair kernel: as many CTA pairs as are resident at once within
+// the SMs sm_reserve leaves.
+template <int MODE, bool TAILS, typename... Args>
+cudaError_t launch_pairs(int sm_reserve, cudaStream_t s, Args &&...args) {
   int nc = 0;
-  cudaError_t e = pair_clusters<MODE>(&nc);
+  cudaError_t e = pair_clusters<MODE, TAILS>(&nc);
   if (e != cudaSuccess) return e;
   const int avail = gemm_grid(sm_reserve) / 2;
   if (avail < nc) nc = avail < 1 ? 1 : avail;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * nc);
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = smem_bytes<true>();
+  cfg.dynamicSmemBytes = smem_bytes<true, TAILS>();
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -848,13 +1124,30 @@ cudaError_t launch_gemm(bool pair, int sm_reserve, cudaStream_t s, Args &&...arg
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<MODE, true>,
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<MODE, true, TAILS>,
                             static_cast<Args &&>(args)...);
+}
+
+// Persistent launch of a grouped GEMM: one CTA per SM, or CTA pairs (with
+// fused tails in the forward modes when `tails`).
+template <int MODE, typename... Args>
+cudaError_t launch_gemm(bool pair, bool tails, int sm_reserve, cudaStream_t s, Args &&...args) {
+  if (!pair) {
+    cudaError_t e = set_smem_attr<MODE>();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(grouped_gemm_tc_kernel<MODE>, dim3(gemm_grid(sm_reserve)),
+                      dim3(NUM_THREADS), SMEM_BYTES, s, static_cast<Args &&>(args)...);
+  }
+  if constexpr (tail_mode(MODE)) {
+    if (tails) return launch_pairs<MODE, true>(sm_reserve, s, static_cast<Args &&>(args)...);
+  }
+  return launch_pairs<MODE, false>(sm_reserve, s, static_cast<Args &&>(args)...);
 }
 
 }  // namespace
 
 void set_gemm_single_cta(bool single) { g_single_cta.store(single ? 1 : 0); }
+void set_gemm_tails(int mode) { g_tails.store(mode < 0 ? -1 : (mode ? 1 : 0)); }
 bool gemm_single_cta() { return g_single_cta.load() != 0; }
 
 cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
@@ -862,11 +1155,13 @@ cudaError_t launch_gemm1_tc(const Desc &d, const void *x_perm, const void *w13,
                             cudaStream_t s) {
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mA2;
   int BNB = 0;
-  if (!make_map_2d(&mA, x_perm, d.H, nK, BK, BM) || !weight_map(&mB, w13, d, d.H, 2ull * d.I, &BNB))
+  if (!make_map_2d(&mA, x_perm, d.H, nK, BK, BM) ||
+      !make_map_2d(&mA2, x_perm, d.H, nK, BK, TAIL_HALF) ||
+      !weight_map(&mB, w13, d, d.H, 2ull * d.I, &BNB))
     return cudaErrorInvalidValue;
-  return launch_gemm<1>(!gemm_single_cta(), sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
+  return launch_gemm<1>(!gemm_single_cta(), use_tails(nK, d.E), sm_reserve, s, mA, mB, mA2, offsets, d.E, (int)nK, d.H, d.I, d.I,
                                 reinterpret_cast<__nv_bfloat16 *>(h), status,
                                 (const int32_t *)nullptr, 0, (const __nv_bfloat16 *)nullptr,
                                 (const float *)nullptr, (const __nv_bfloat16 *)nullptr,
@@ -884,7 +1179,7 @@ cudaError_t launch_gemm1_tc_gather(const Desc &d, const void *x, const int32_t *
   cudaError_t e = set_smem_attr<3>();
   if (e != cudaSuccess) return e;
   return launch_pdl(grouped_gemm_tc_kernel<3>, dim3(gemm_grid(sm_reserve)), dim3(threads_for(3)),
-                    SMEM_BYTES, s, mB, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
+                    SMEM_BYTES, s, mB, mB, mB, offsets, d.E, (int)nK, d.H, d.I, d.I,
                     reinterpret_cast<__nv_bfloat16 *>(h), status, perm, d.K,
                     reinterpret_cast<const __nv_bfloat16 *>(x), nullptr, nullptr, pipeline_wait_limit(), BNB);
 }
@@ -893,11 +1188,12 @@ cudaError_t launch_gemm2_tc(const Desc &d, const void *h, const void *w2, const 
                             void *y_perm, int sm_reserve, int32_t *status, cudaStream_t s) {
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mA2;
   int BNB = 0;
-  if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !weight_map(&mB, w2, d, d.I, d.H, &BNB))
+  if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !make_map_2d(&mA2, h, d.I, nK, BK, TAIL_HALF) ||
+      !weight_map(&mB, w2, d, d.I, d.H, &BNB))
     return cudaErrorInvalidValue;
-  return launch_gemm<2>(!gemm_single_cta(), sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
+  return launch_gemm<2>(!gemm_single_cta(), use_tails(nK, d.E), sm_reserve, s, mA, mB, mA2, offsets, d.E, (int)nK, d.I, d.I, d.H,
                                 reinterpret_cast<__nv_bfloat16 *>(y_perm), status,
                                 (const int32_t *)nullptr, 0, (const __nv_bfloat16 *)nullptr,
                                 (const float *)nullptr, (const __nv_bfloat16 *)nullptr,
@@ -910,11 +1206,12 @@ cudaError_t launch_gemm2_tc_weighted(const Desc &d, const void *h, const void *w
                                      int32_t *status, cudaStream_t s) {
   const long long nK = d.nK();
   if (nK == 0) return cudaSuccess;
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mA2;
   int BNB = 0;
-  if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !weight_map(&mB, w2, d, d.I, d.H, &BNB))
+  if (!make_map_2d(&mA, h, d.I, nK, BK, BM) || !make_map_2d(&mA2, h, d.I, nK, BK, TAIL_HALF) ||
+      !weight_map(&mB, w2, d, d.I, d.H, &BNB))
     return cudaErrorInvalidValue;
-  return launch_gemm<4>(!gemm_single_cta(), sm_reserve, s, mA, mB, offsets, d.E, (int)nK, d.I, d.I, d.H,
+  return launch_gemm<4>(!gemm_single_cta(), use_tails(nK, d.E), sm_reserve, s, mA, mB, mA2, offsets, d.E, (int)nK, d.I, d.I, d.H,
                                 reinterpret_cast<__nv_bfloat16 *>(y_slot), status, perm, d.K,
                                 (const __nv_bfloat16 *)nullptr, topk_w,
                                 (const __nv_bfloat16 *)nullptr, pipeline_wait_limit(), BNB);
@@ -933,7 +1230,7 @@ cudaError_t launch_gemm_dgrad_tc(const Desc &d, const void *a, const void *w, in
   if (!make_map_2d(&mA, a, Kdim, nK, BK, BM) ||
       !make_map_3d(&mB, w, Kdim, Nout, d.E, BK, box_n))
     return cudaErrorInvalidValue;
-  return launch_gemm<5>(pair, 0, s, mA, mB, offsets, d.E, (int)nK, Kdim, 0, Nout,
+  return launch_gemm<5>(pair, false, 0, s, mA, mB, mA, offsets, d.E, (int)nK, Kdim, 0, Nout,
                         reinterpret_cast<__nv_bfloat16 *>(out), status, (const int32_t *)nullptr,
                         0, (const __nv_bfloat16 *)nullptr, (const float *)nullptr,
                         (const __nv_bfloat16 *)nullptr, pipeline_wait_limit(), 0);
@@ -948,7 +1245,7 @@ cudaError_t launch_gemm1_swiglu_bwd_tc(const Desc &d, const void *x_perm, const 
   if (!make_map_2d(&mA, x_perm, d.H, nK, BK, BM) ||
       !make_map_3d(&mB, w13, 2ull * d.I, d.H, d.E, 64, BK))
     return cudaErrorInvalidValue;
-  return launch_gemm<6>(!gemm_single_cta(), 0, s, mA, mB, offsets, d.E, (int)nK, d.H, d.I, 2 * d.I,
+  return launch_gemm<6>(!gemm_single_cta(), false, 0, s, mA, mB, mA, offsets, d.E, (int)nK, d.H, d.I, 2 * d.I,
                         reinterpret_cast<__nv_bfloat16 *>(dgu), status, (const int32_t *)nullptr,
                         0, (const __nv_bfloat16 *)nullptr, (const float *)nullptr,
                         reinterpret_cast<const __nv_bfloat16 *>(dh), pipeline_wait_limit(), 0);

@@ -738,6 +738,11 @@ moe_status_t moe_set_gemm_pairs(int enable) {
   return MOE_OK;
 }
 
+moe_status_t moe_set_gemm_tails(int mode) {
+  set_gemm_tails(mode);
+  return MOE_OK;
+}
+
 moe_status_t moe_check_status(const int32_t *status_word, moe_stream_t stream) {
   if (!status_word) return MOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;

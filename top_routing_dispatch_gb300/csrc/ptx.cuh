@@ -170,6 +170,12 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// named barrier ID (1..15) among COUNT threads (whole warps) of the CTA
+template <int ID, int COUNT>
+__device__ __forceinline__ void named_bar_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
+}
+
 // address of the same shared-memory location in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -186,6 +192,18 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
 // a peer's), with release semantics at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+               : "memory");
+}
+// Arrivals without release semantics: for a barrier that only says "these
+// TMEM columns have been read" (the reads completed by tcgen05.wait::ld, then
+// ordered by tcgen05.fence::before_thread_sync); no memory write of the
+// thread needs to be visible to the waiter.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
                : "memory");
 }
 
