@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--gemm-pairs", choices=["on", "off"], default="on",
                     help="forward grouped GEMMs on CTA pairs (cta_group::2, the default) or on "
                          "single CTAs (same results)")
+    ap.add_argument("--gemm-tails", choices=["auto", "on", "off"], default="auto",
+                    help="fused tails of the forward pair GEMMs: chosen per launch (the default: "
+                         "on at 192..384 rows per expert), always, or never (same results)")
     ap.add_argument("--extra-workloads", default="olmoe_skew_bf16,dsv3_bf16,tiny_fp32",
                     help="other single-batch workloads timed after the headline (N=1 only); "
                          "empty to skip")
@@ -535,6 +538,7 @@ def run_ours(args, cfg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     M.moe_set_gemm_pairs(args.gemm_pairs == "on")
+    M.moe_set_gemm_tails({"auto": None, "on": True, "off": False}[args.gemm_tails])
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -611,7 +615,8 @@ def run_ours(args, cfg):
                                                     else " (of fallback)"),
         # DRAM bytes per launch from the ncu capture of this workload's GEMM1
         "traffic": (recorded_traffic("gemm1_olmoe_bf16.md", GEMM_SOURCES)
-                    if cfg.name == "olmoe_bf16" and args.gemm_pairs == "on" else None),
+                    if cfg.name == "olmoe_bf16" and args.gemm_pairs == "on"
+                    and args.gemm_tails != "on" else None),
         "algorithmic_flop_per_launch": alg["gemm1"]["flop"],
         "algorithmic_bytes_per_launch": alg["gemm1"]["bytes"],
         # every kernel of this workload's step (and the fused-gather GEMM1)
@@ -635,8 +640,10 @@ def run_ours(args, cfg):
                     else "row-major"),
         "router_weight": ("also transposed by moe_prepare_router (once, untimed)"
                           if "w_gate_t" in L else "as stored"),
-        "gemm_tiles": ("CTA pairs (cta_group::2), 256 x 256" if args.gemm_pairs == "on"
-                       else "single CTAs, 128 x 256"),
+        "gemm_tiles": ("CTA pairs (cta_group::2), 256 x 256; fused tails "
+                       + {"auto": "chosen per launch (on at 192..384 rows per expert)",
+                          "on": "always", "off": "never"}[args.gemm_tails]
+                       if args.gemm_pairs == "on" else "single CTAs, 128 x 256"),
         "e2e": {"value": aggregate_tokens_per_s(cfg.n, args.steps, world, e2e_total), "unit": UNIT,
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
                 "d2h_bytes_per_step": y_h.numel() * y_h.element_size(),
