@@ -98,6 +98,11 @@ constexpr int TAIL_BYTES = TAIL_HALF * BK * 2;  // 2 KB per CTA and stage
 __host__ __device__ constexpr bool tail_mode(int mode) {
   return mode == 1 || mode == 2 || mode == 4;
 }
+// compile-time flag for the k loops specialised on "this tile has a tail"
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
 
 struct SmemTail {
   uint64_t full[kMaxStages];
@@ -455,14 +460,14 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       uint32_t phase = 0;
       for (int t = unit; t < total; t += units) {
         const TileInfo ti = decode_tile<true, TAILS>(st, t, n_tiles, E, rank);
-        // bytes each CTA loads per stage
-        const int bytes = P::STAGE + (ti.tail ? TAIL_BYTES : 0);
-        bool stop = false;
+        // the k loop, compiled apart for tiles with a fused tail (TL): the
+        // per-stage path of the others stays as short as without tails
+        auto k_loop = [&](auto tl) {
+          constexpr bool TL = decltype(tl)::value;
+          constexpr int bytes = P::STAGE + (TL ? TAIL_BYTES : 0);  // per CTA and stage
         for (int kb = 0; kb < KB; ++kb) {
-          if (!wait_or_abort(&st.empty[stage], phase ^ 1u, abort_flag, status, wait_limit)) {
-            stop = true;
-            break;
-          }
+          if (!wait_or_abort(&st.empty[stage], phase ^ 1u, abort_flag, status, wait_limit))
+            return true;
           if (leader) ptx::mbar_arrive_expect_tx(&st.full[stage], 2 * bytes);
           const uint32_t bar = full0 + 8u * (uint32_t)stage;
           // a part with no rows of the expert (segment ends in the first
@@ -491,7 +496,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           }
           // fused tail: this CTA's TAIL_HALF of the tail rows (rows past the
           // tensor read zeros; rows of the next expert are never stored)
-          if (TAILS && ti.tail)
+          if constexpr (TL)
             ptx::tma_load_2d_pair(smemT + stage * TAIL_BYTES, &tmA2, bar, kb * BK,
                                   ti.t0 + rank * TAIL_HALF);
           ++st.own_issued[stage];
@@ -501,6 +506,9 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             phase ^= 1u;
           }
         }
+          return false;
+        };
+        const bool stop = ti.tail ? k_loop(BoolC<TAILS>{}) : k_loop(BoolC<false>{});
         if (stop) break;
       }
       // copies still in flight are settled by the leader before the pair
@@ -571,10 +579,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
-      // bit a: parity of the uses so far of accumulator a (uses), and of its
-      // head (huses: the tiles on a, and the fused tails put there); use u
-      // waits for the epilogue's release u - 1
+      // bit a: parity of the uses so far of accumulator a (uses: use u waits
+      // for the epilogue's release u - 1), and of the waits for its head's
+      // releases (huses)
       uint32_t uses = 0, huses = 0;
+      bool prev_tail = false;  // the previous tile put a tail in this tile's head
       constexpr uint32_t idesc = PAIR ? (kmajor_b(MODE) ? IDESC_PAIR_KB : IDESC_PAIR)
                                       : (kmajor_b(MODE) ? IDESC_KB : IDESC);
       int e_cur = 0;  // expert of the current tile (a CTA's tiles come in increasing order)
@@ -590,27 +599,34 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
                            wait_limit))
           break;
         uses ^= 1u << acc;
-        if (TAILS) {
-          if (!wait_or_abort(&st.hempty[acc], (huses >> acc & 1u) ^ 1u, abort_flag, status,
-                             wait_limit))
+        // Head releases come only around tails, each with one wait here: the
+        // drain of a tail releases the head it used (awaited by the next
+        // tile, whose accumulator that is), and the drain of a tile followed
+        // by a tile with a tail releases its own head after its first chunk
+        // (awaited by that tile, whose tail goes there).  The whole-accumulator
+        // release covers every other case.
+        if (TAILS && prev_tail) {
+          if (!wait_or_abort(&st.hempty[acc], huses >> acc & 1u, abort_flag, status, wait_limit))
             break;
           huses ^= 1u << acc;
-          if (tail) {  // the tail's D^T goes to the other accumulator's head
-            if (!wait_or_abort(&st.hempty[acc ^ 1], (huses >> (acc ^ 1) & 1u) ^ 1u, abort_flag,
-                               status, wait_limit))
-              break;
-            huses ^= 1u << (acc ^ 1);
-          }
         }
+        // the tail's D^T goes to the other accumulator's head (free before the
+        // unit's first tile)
+        if (TAILS && tail && t != unit) {
+          if (!wait_or_abort(&st.hempty[acc ^ 1], huses >> (acc ^ 1) & 1u, abort_flag, status,
+                             wait_limit))
+            break;
+          huses ^= 1u << (acc ^ 1);
+        }
+        prev_tail = tail;
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * UMMA_N);
         const uint32_t dt = tmem + (uint32_t)((acc ^ 1) * UMMA_N);  // the tail's D^T
-        bool stop = false;
+        // the k loop, compiled apart for tiles with a fused tail (TL)
+        auto k_loop = [&](auto tl) {
+          constexpr bool TL = decltype(tl)::value;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!wait_or_abort(&st.full[stage], phase, abort_flag, status, wait_limit)) {
-            stop = true;
-            break;
-          }
+          if (!wait_or_abort(&st.full[stage], phase, abort_flag, status, wait_limit)) return true;
           // MODE 3: A was written by cp.async (generic proxy); the barrier
           // made it visible to this thread, the proxy fence makes it visible
           // to the tensor cores' async-proxy reads issued below
@@ -633,7 +649,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             else
               ptx::mma_bf16(d, xdesc, wdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          if (TAILS && tail) {
+          if constexpr (TL) {
             // the same weight atoms as the 256-row A operand (MN-major), the
             // tail rows (TAIL_HALF per CTA, K-major) as a TAIL_ROWS-column B
             const uint32_t r0 = ptx::smem_u32(smemT + stage * TAIL_BYTES);
@@ -653,6 +669,9 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             phase ^= 1u;
           }
         }
+          return false;
+        };
+        const bool stop = tail ? k_loop(BoolC<TAILS>{}) : k_loop(BoolC<false>{});
         if (stop) break;
         if constexpr (PAIR)
           ptx::mma_commit_pair(&st.tfull[acc], 0x3);
@@ -678,6 +697,9 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     for (int t = unit; t < total; t += units) {
       const TileInfo ti = decode_tile<PAIR, TAILS>(st, t, n_tiles, E, rank);
       const bool tail = TAILS && ti.tail > 0;
+      // the next tile puts its tail in this tile's head: release it early
+      const bool next_tail = TAILS && t + units < total &&
+                             decode_tile<PAIR, TAILS>(st, t + units, n_tiles, E, rank).tail > 0;
       bool ok = wait_or_abort(&st.tfull[acc], fills >> acc & 1u, abort_flag, status, wait_limit);
       if (gemm1_mode(MODE) && tail) {
         // the gate and up warps of a GEMM1 tail wait on each other below:
@@ -793,7 +815,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           ptx::tmem_ld_32x32b_x32(tbase + gc, g);
           ptx::tmem_ld_32x32b_x32(tbase + uc, u);
           ptx::tmem_ld_wait();
-          if (TAILS && c == 0) head_release(st.hempty, hempty0, acc, PAIR && !leader, lane);
+          if (TAILS && next_tail && c == 0)
+            head_release(st.hempty, hempty0, acc, PAIR && !leader, lane);
           const int col = ti.nt * 128 + (SPLIT_GU ? (c >> 1) * 64 + (c & 1) * 32 : c * 32);
           if (MODE == 6) {
             // SwiGLU backward: dG = dh U s (1 + G (1 - s)), dU = dh G s, s = sigmoid(G)
@@ -850,7 +873,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           uint32_t a[32];
           ptx::tmem_ld_32x32b_x32(tbase + c * 32, a);
           ptx::tmem_ld_wait();
-          if (TAILS && c == 0) head_release(st.hempty, hempty0, acc, PAIR && !leader, lane);
+          if (TAILS && next_tail && c == 0)
+            head_release(st.hempty, hempty0, acc, PAIR && !leader, lane);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
