@@ -126,10 +126,12 @@ struct SmemTail {
 };
 
 // TAILS: the stages are followed by a TAIL_BYTES slot per stage for the fused
-// tail rows and the two gate warps' exchange buffers
+// tail rows, the two gate warps' exchange buffers and the expert order
+// the order in which the fused-tail variant walks the experts (uint16 each)
+constexpr int ORD_BYTES = ((kMaxE + 1) * 2 + 15) / 16 * 16;
 template <bool PAIR, bool TAILS = false>
 __host__ __device__ constexpr size_t tails_bytes() {
-  return TAILS ? (size_t)Pipe<PAIR>::STAGES * TAIL_BYTES + 2 * XCH_WARP_BYTES : 0;
+  return TAILS ? (size_t)Pipe<PAIR>::STAGES * TAIL_BYTES + 2 * XCH_WARP_BYTES + ORD_BYTES : 0;
 }
 template <bool PAIR, bool TAILS = false>
 constexpr size_t smem_bytes() {
@@ -188,12 +190,13 @@ __host__ __device__ constexpr int mtiles_of(int len) {
 // (PAIR: rank 0 takes rows [0, 128) of the pair's 256-row window, rank 1 rows
 // [128, 256); rows may be <= 0 when the segment ends in the first half).
 template <bool PAIR = false, bool TAILS = false>
+// ord (TAILS): the expert at each position of the walk; tp is per position.
 __device__ __forceinline__ TileInfo decode_tile(const SmemTail &s, int t, int n_tiles, int E,
-                                                int rank = 0) {
+                                                int rank = 0, const uint16_t *ord = nullptr) {
   TileInfo ti;
   const int mt = t / n_tiles;
   ti.nt = t - mt * n_tiles;
-  int lo = 0, hi = E;  // largest e with tp[e] <= mt
+  int lo = 0, hi = E;  // largest position p with tp[p] <= mt
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (s.tp[mid] <= mt)
@@ -201,19 +204,20 @@ __device__ __forceinline__ TileInfo decode_tile(const SmemTail &s, int t, int n_
     else
       hi = mid;
   }
-  ti.e = lo;
   const int j = mt - s.tp[lo];
-  const int w0 = s.off[lo] + j * Pipe<PAIR>::TILE_ROWS;
+  const int e = (TAILS && ord) ? (int)ord[lo] : lo;
+  ti.e = e;
+  const int w0 = s.off[e] + j * Pipe<PAIR>::TILE_ROWS;
   ti.row0 = w0 + rank * BM;
-  const int left = s.off[lo + 1] - ti.row0;
+  const int left = s.off[e + 1] - ti.row0;
   ti.rows = left < BM ? left : BM;
   ti.tail = 0;
   ti.t0 = 0;
   if constexpr (PAIR && TAILS) {
-    const int len = s.off[lo + 1] - s.off[lo];
+    const int len = s.off[e + 1] - s.off[e];
     if (fused_tail<PAIR, TAILS>(len) && j == len / Pipe<PAIR>::TILE_ROWS - 1) {
       ti.t0 = w0 + Pipe<PAIR>::TILE_ROWS;
-      ti.tail = s.off[lo + 1] - ti.t0;
+      ti.tail = s.off[e + 1] - ti.t0;
     }
   }
   return ti;
@@ -374,6 +378,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   uint8_t *smemB = PAIR ? smem : smem + STAGES * A_STAGE_BYTES;
   uint8_t *smemT = smem + STAGES * P::STAGE;  // TAILS: the fused tail rows, per stage
   uint8_t *xch = smemT + STAGES * TAIL_BYTES;  // TAILS: the gate warps' exchange buffers
+  // TAILS: the experts in walk order.  GEMM1 takes those with a fused tail
+  // first, so their heavier tiles are dealt evenly over the pairs (measured:
+  // DeepSeek-V3-sized GEMM1 3.01 -> 2.77 ms); GEMM2, whose tiles are half as
+  // long, keeps the index order (fused-first measured 3 % slower there).
+  uint16_t *ord = TAILS ? reinterpret_cast<uint16_t *>(xch + 2 * XCH_WARP_BYTES) : nullptr;
+  constexpr bool FUSED_FIRST = TAILS && MODE == 1;
   SmemTail &st = *reinterpret_cast<SmemTail *>(smemT + tails_bytes<PAIR, TAILS>());
   // PAIR, GEMM1: each CTA's half of the weight tile is 64 gate columns and the
   // 64 matching up columns (a tail's SwiGLU then stays inside the CTA)
@@ -417,11 +427,25 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   if (tid == 0) {
     bool ok = st.off[0] == 0 && st.off[E] <= nK;
     int run = 0;
-    for (int e = 0; e < E; ++e) {
-      const int len = st.off[e + 1] - st.off[e];
-      ok = ok && len >= 0;
-      st.tp[e] = run;
-      run += mtiles_of<PAIR, TAILS>(len);
+    if constexpr (TAILS) {
+      for (int e = 0; e < E; ++e) ok = ok && st.off[e + 1] - st.off[e] >= 0;
+      int pos = 0;
+      for (int pass = FUSED_FIRST ? 0 : 1; pass < 2; ++pass)
+        for (int e = 0; e < E; ++e) {
+          const int len = st.off[e + 1] - st.off[e];
+          if (ok && (!FUSED_FIRST || fused_tail<PAIR, TAILS>(len) == (pass == 0))) {
+            ord[pos] = (uint16_t)e;
+            st.tp[pos++] = run;
+            run += mtiles_of<PAIR, TAILS>(len);
+          }
+        }
+    } else {
+      for (int e = 0; e < E; ++e) {
+        const int len = st.off[e + 1] - st.off[e];
+        ok = ok && len >= 0;
+        st.tp[e] = run;
+        run += mtiles_of<PAIR, TAILS>(len);
+      }
     }
     st.tp[E] = run;
     st.total_mtiles = run;
@@ -459,7 +483,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int t = unit; t < total; t += units) {
-        const TileInfo ti = decode_tile<true, TAILS>(st, t, n_tiles, E, rank);
+        const TileInfo ti = decode_tile<true, TAILS>(st, t, n_tiles, E, rank, ord);
         // the k loop, compiled apart for tiles with a fused tail (TL): the
         // per-stage path of the others stays as short as without tails
         auto k_loop = [&](auto tl) {
@@ -586,14 +610,15 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       bool prev_tail = false;  // the previous tile put a tail in this tile's head
       constexpr uint32_t idesc = PAIR ? (kmajor_b(MODE) ? IDESC_PAIR_KB : IDESC_PAIR)
                                       : (kmajor_b(MODE) ? IDESC_KB : IDESC);
-      int e_cur = 0;  // expert of the current tile (a CTA's tiles come in increasing order)
+      int p_cur = 0;  // walk position of the current tile's expert (tiles come in order)
       for (int t = unit; t < total; t += units) {
         bool tail = false;
         if constexpr (TAILS) {
           const int mt = t / n_tiles;
-          while (e_cur + 1 < E && st.tp[e_cur + 1] <= mt) ++e_cur;
-          const int len = st.off[e_cur + 1] - st.off[e_cur];
-          tail = fused_tail<PAIR, TAILS>(len) && mt - st.tp[e_cur] == len / P::TILE_ROWS - 1;
+          while (p_cur + 1 < E && st.tp[p_cur + 1] <= mt) ++p_cur;
+          const int e = ord[p_cur];
+          const int len = st.off[e + 1] - st.off[e];
+          tail = fused_tail<PAIR, TAILS>(len) && mt - st.tp[p_cur] == len / P::TILE_ROWS - 1;
         }
         if (!wait_or_abort(&st.tempty[acc], (uses >> acc & 1u) ^ 1u, abort_flag, status,
                            wait_limit))
@@ -695,11 +720,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     const uint32_t tempty0 = PAIR ? ptx::mapa_shared(ptx::smem_u32(&st.tempty[0]), 0) : 0u;
     const uint32_t hempty0 = PAIR ? ptx::mapa_shared(ptx::smem_u32(&st.hempty[0]), 0) : 0u;
     for (int t = unit; t < total; t += units) {
-      const TileInfo ti = decode_tile<PAIR, TAILS>(st, t, n_tiles, E, rank);
+      const TileInfo ti = decode_tile<PAIR, TAILS>(st, t, n_tiles, E, rank, ord);
       const bool tail = TAILS && ti.tail > 0;
       // the next tile puts its tail in this tile's head: release it early
       const bool next_tail = TAILS && t + units < total &&
-                             decode_tile<PAIR, TAILS>(st, t + units, n_tiles, E, rank).tail > 0;
+                             decode_tile<PAIR, TAILS>(st, t + units, n_tiles, E, rank, ord).tail > 0;
       bool ok = wait_or_abort(&st.tfull[acc], fills >> acc & 1u, abort_flag, status, wait_limit);
       if (gemm1_mode(MODE) && tail) {
         // the gate and up warps of a GEMM1 tail wait on each other below:
