@@ -226,6 +226,18 @@ def test_pipeline_wait_limit_control(lib):
 
 
 @needs_nvcc
+def test_gemm_tuning_controls(lib):
+    # host-only switches, every value accepted (the results are the same
+    # either way), and the defaults put back: pairs on, tails per launch
+    for v in (0, 1):
+        assert lib.moe_set_gemm_pairs(v) == 0
+    for v in (-1, 0, 1, 5):
+        assert lib.moe_set_gemm_tails(v) == 0
+    assert lib.moe_set_gemm_pairs(1) == 0
+    assert lib.moe_set_gemm_tails(-1) == 0
+
+
+@needs_nvcc
 def test_tiled_weights_rejected_where_unsupported(lib):
     import top_routing_dispatch_gb300 as M
     # float32 layers and the backward read row-major weights only
