@@ -11,16 +11,21 @@
 // two-stage configuration (20 KB of shared memory at E = 64) fits beside a
 // GEMM CTA, and both give bitwise equal results.
 //
-// A CTA takes 16 tokens and all E experts (8 warps, 256 threads):
-//   k loop      the x tile (16 tokens x 64 k) and the W_gate block (64 k x E)
-//               of each stage are copied by cp.async into shared memory
-//               (16-byte pieces, XOR-swizzled so the ldmatrix reads below are
-//               free of bank conflicts), STAGES - 1 stages ahead.  Warp w owns
-//               the experts of MMA n-tiles w, w + 8, ...: it takes the A
+// A CTA takes 16 (or 32) tokens and all E experts (8 warps, 256 threads):
+//   k loop      the x tile (the CTA's tokens x S k) and the W_gate block
+//               (S k x E) of each stage are copied by cp.async into shared
+//               memory (16-byte pieces, XOR-swizzled so the ldmatrix reads
+//               below are free of bank conflicts), STAGES - 1 stages ahead, the
+//               k range rotated per 32-token block so the CTAs do not all read
+//               the same rows of W_gate at once.  Warp w takes the k16 steps g
+//               with g % 8 == w for every expert (all E/8 MMA n-tiles): the A
 //               fragments with ldmatrix, the B fragments with ldmatrix.trans
-//               (W_gate is k-major with experts contiguous) and accumulates its
-//               16 x 8 blocks over every k16 step in order.  Each logit is the
-//               sum of one MMA chain, so nothing depends on the pipeline depth.
+//               (W_gate is k-major with experts contiguous), one MMA chain per
+//               warp in k order.
+//   partials    the eight warps' partial logits are added in the fixed tree
+//               ((p0 + p4) + (p2 + p6)) + ((p1 + p5) + (p3 + p7)) through
+//               shared memory, so no result depends on the stage width, the
+//               pipeline depth or the tile height.
 //   logits      + bias, stored (shared memory for the TopK, and global).
 //   TopK        warp w decides tokens w and w + 8: K+1 rounds of a warp argmax
 //               by redux.sync (larger first, ties to the lower expert id), max
