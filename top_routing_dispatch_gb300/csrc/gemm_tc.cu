@@ -23,16 +23,18 @@
 // (two B boxes), six 32 KB stages (see the kernel's comment for the protocol);
 // in the forward modes optionally with fused tails (TAILS: an expert's last
 // 1..32 rows computed transposed inside its last full window's tiles).
-// A tile is (m-tile, n-tile).  m-tiles are 128-row windows that start at each
-// expert's segment start, so every tile belongs to exactly one expert; its
-// rows past the segment end are computed but not stored (TMA zero-fills rows
-// past the tensor).  Tiles are dealt to CTAs round-robin; every tile costs the
-// same (full K loop), so the static schedule balances.  Each tile is computed
-// entirely by one CTA with a fixed k order: results do not depend on the grid
-// size.
+// A tile is (m-tile, n-tile).  m-tiles are 128-row windows (256 for a pair)
+// that start at each expert's segment start, so every tile belongs to exactly
+// one expert; its rows past the segment end are computed but not stored (TMA
+// zero-fills rows past the tensor).  Tiles are dealt to CTAs (pairs)
+// round-robin in expert order (the fused-tail GEMM1 walks the experts that
+// fuse a tail first); a tile without a tail costs a full K loop, so the static
+// schedule balances.  Each tile is computed entirely by one CTA (pair) with a
+// fixed k order: results do not depend on the grid size.
 //
 // B is the weight matrix as stored (k rows, n contiguous): an MN-major UMMA
-// operand with 128-byte swizzle.  A is K-major with 128-byte swizzle.
+// operand with 128-byte swizzle (or, tiled by moe_prepare_weights, one 64 x 64
+// tile per box).  A is K-major with 128-byte swizzle.
 #include <cuda.h>
 
 #include <atomic>
